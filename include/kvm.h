@@ -1,0 +1,224 @@
+/*
+ * kvm.h -- C ABI of the per-step working-set recall library (libkvm.so).
+ *
+ * Sources (page titles, with the section / equation / figure each call follows):
+ *   [KVMem] "KVMem: Virtualizing Million-Token Agent Workspaces on a Consumer GPU"
+ *   [InfS]  "InferScale: GPU-Native KV Injection for Personalized LLM Serving"
+ *
+ * One process, one GPU (sm_103a).  Every buffer is allocated by the caller
+ * (device memory, or pinned host memory where stated) and must outlive the
+ * calls that use it; the library never allocates or frees device memory and
+ * never frees caller memory.  All work is enqueued on the caller's stream;
+ * functions return after enqueueing unless stated otherwise.  No C++
+ * exception crosses this boundary: every function returns a kvm_status.
+ * Argument errors are detected on the host before anything is enqueued and
+ * leave the context unchanged.  Device-side range checks (block ids, page ids)
+ * skip the offending access and raise a sticky device error flag that
+ * kvm_sync() reports as KVM_ERR_DEVICE and clears.
+ *
+ * Layouts (row-major, innermost last; B = block_tokens = 32, d = head_dim):
+ *   K pages, V pages, raw K, V      [block or page][layer][kv_head][B][d]
+ *   Mean-K index                     [layer][kv_head][max_blocks][d]
+ *   RoPE-free queries                [layer][query][q_head][d]
+ *   block relevance (scores)         [n_blocks] float32
+ * Block b of the history holds tokens 32b .. 32b+31 (its original range);
+ * view slot j holds compact positions 32j .. 32j+31.
+ * RoPE pairs coordinate i with i + d/2 (rotate-half); the angle of pair i
+ * at position p is p * theta^(-2i/d), evaluated in double precision and
+ * rounded once to a float32 cos/sin table.
+ */
+#ifndef KVM_H_
+#define KVM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  NULL means the legacy default stream. */
+typedef struct CUstream_st *kvm_stream;
+
+typedef enum {
+    KVM_OK = 0,
+    KVM_ERR_INVALID_ARG = -1,          /* bad pointer, size, dtype or config field     */
+    KVM_ERR_WORKSPACE_TOO_SMALL = -2,  /* workspace smaller than kvm_workspace_bytes() */
+    KVM_ERR_CAPACITY = -3,             /* n_blocks / queries / pages beyond the config */
+    KVM_ERR_CUDA = -4,                 /* a CUDA runtime call failed (see kvm_last_error) */
+    KVM_ERR_TIMEOUT = -5,              /* a bounded device wait gave up               */
+    KVM_ERR_NOT_BOUND = -6,            /* kvm_step before kvm_bind                    */
+    KVM_ERR_INJECTED = -7,             /* failure raised by kvm_debug_inject          */
+    KVM_ERR_DEVICE = -8                /* a device-side range check fired             */
+} kvm_status;
+
+enum { KVM_F32 = 0, KVM_BF16 = 1 };              /* element types            */
+enum { KVM_DEVICE = 0, KVM_HOST_PINNED = 1 };    /* where a buffer lives     */
+
+/* Shapes and budgets of one workspace.  All fields are required. */
+typedef struct {
+    int32_t n_layers;        /* L: scored attention layers                     */
+    int32_t n_kv_heads;      /* G                                              */
+    int32_t n_q_heads;       /* H, a multiple of G (grouped-query attention)   */
+    int32_t head_dim;        /* d: 64 or 128                                   */
+    int32_t block_tokens;    /* must be 32 ([KVMem] §4.3 default block size)   */
+    double  rope_theta;      /* RoPE base                                      */
+    int32_t kv_dtype;        /* K pages, raw K, V: KVM_F32 or KVM_BF16         */
+    int32_t index_dtype;     /* Mean-K entries                                 */
+    int32_t q_dtype;         /* queries                                        */
+    int32_t sink_blocks;     /* S: always-kept leading blocks                  */
+    int32_t recent_blocks;   /* W: always-kept trailing blocks                 */
+    int32_t view_blocks;     /* V_b: execution-view budget, >= S + W + 1       */
+    int32_t max_queries;     /* largest M_q accepted                           */
+    int64_t max_blocks;      /* index capacity and largest history N           */
+    int64_t max_positions;   /* RoPE table rows: > every token position used   */
+    int32_t tile_blocks;     /* index tile for host-resident scoring ([KVMem] §5) */
+    int32_t pool_pages;      /* pages of the kvm_step page pool (>= view_blocks) */
+    int32_t index_location;  /* KVM_DEVICE or KVM_HOST_PINNED (kvm_step, kvm_score_select) */
+    int32_t repo_location;   /* where kvm_step finds raw K / V of the history  */
+    int32_t h2d_batch_blocks;/* missed blocks per pipelined H2D batch (kvm_step) */
+} kvm_config;
+
+typedef struct kvm_ctx kvm_ctx;
+
+/* Device workspace bytes a context needs for `cfg` (RoPE table, scoring
+ * scratch, index staging tiles, step descriptors).  0 if cfg is invalid. */
+size_t kvm_workspace_bytes(const kvm_config *cfg);
+
+/* Create a context.  `workspace` is caller-owned device memory of at least
+ * kvm_workspace_bytes(cfg) bytes, 256-byte aligned, used exclusively by this
+ * context until kvm_destroy.  Fills the RoPE cos/sin table on `stream`
+ * ([KVMem] §4.4: precomputed sine/cosine tables).  *out receives the context. */
+kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_bytes,
+                      kvm_stream stream, kvm_ctx **out);
+
+kvm_status kvm_destroy(kvm_ctx *ctx);
+
+/*
+ * (a) Mean-K index build -- [KVMem] §4.3 (Mean-K block representation) and §5
+ * (incremental indexing while K is still resident on the GPU).
+ *
+ * For blocks b = first_block .. first_block + n_blocks - 1:
+ *   raw K of token p = R_{-p} K_pages[b - first_block][l][g][t]   (p = 32b + t)
+ *   index[l][g][b]   = (1/32) * sum_t raw K                      (float32 sums)
+ * k_pages  device, [n_blocks][L][G][32][d], kv_dtype, K rotated at original positions.
+ * index    device, [L][G][max_blocks][d], index_dtype; entries [first_block,
+ *          first_block + n_blocks) are written, others untouched.
+ * raw_k_out nullable device, [n_blocks][L][G][32][d], kv_dtype: the
+ *          position-independent raw K (float32 rotation, rounded once).
+ * Errors: KVM_ERR_CAPACITY if first_block + n_blocks > max_blocks or the
+ * positions exceed max_positions; KVM_ERR_INVALID_ARG on NULL inputs.
+ */
+kvm_status kvm_build_index(kvm_ctx *ctx, const void *k_pages, int64_t first_block,
+                           int64_t n_blocks, void *index, void *raw_k_out, kvm_stream stream);
+
+/*
+ * (b) Query-conditioned block scoring, Eq. (10) of [KVMem] §4.3, and the
+ * default selector (sink + recent + top-k, chronological order).
+ *
+ *   s[l,m,h,b] = q[l,m,h] . index[l, g(h), b] / sqrt(d),  g(h) = h / (H/G)
+ *   R_b = 1/(L*H) * sum_{l,h} sum_m softmax_b(s[l,m,h,:])[b]
+ * over all n_blocks indexed blocks (the softmax is global over blocks, also
+ * when the index is scored tile by tile from host memory, [KVMem] §5).
+ * Selection: blocks [0,S) and [N-W,N) always; the other V_b-S-W slots go to
+ * the largest R_b (ties: lower block id; NaN last); output ascending.  If
+ * N <= V_b every block is selected.
+ *
+ * q         device, [L][n_queries][H][d], q_dtype (RoPE-free queries).
+ * index     [L][G][max_blocks][d], index_dtype; device memory when
+ *           cfg.index_location == KVM_DEVICE, pinned host memory when
+ *           KVM_HOST_PINNED (then scored in tiles of tile_blocks staged on the GPU).
+ * scores_out   device, [n_blocks] float32: R_b.
+ * sel_ids_out  device, [view_blocks] int32: selected ids, ascending; the
+ *              first min(N, V_b) entries are written.
+ * n_sel_out    nullable HOST int32: receives min(N, V_b).
+ * Errors: KVM_ERR_CAPACITY if n_blocks > max_blocks or n_queries > max_queries;
+ * KVM_ERR_INVALID_ARG if n_blocks < 1 or n_queries < 1.
+ */
+kvm_status kvm_score_select(kvm_ctx *ctx, const void *q, int32_t n_queries, const void *index,
+                            int64_t n_blocks, float *scores_out, int32_t *sel_ids_out,
+                            int32_t *n_sel_out, kvm_stream stream);
+
+/*
+ * (c) Chronological execution-view assembly -- [KVMem] §4.4 (view
+ * separation: RoPE applied to raw K at the block's compact position, V copied
+ * unchanged) and [InfS] Theorem 6 (re-rotation at a new position).
+ *
+ * For slot j < n_sel, with b = sel_ids[j] and page p = page_ids ? page_ids[j] : j:
+ *   k_pages[p][l][g][t] = R_{32j+t} raw_k_repo[b][l][g][t]   (float32, rounded once)
+ *   v_pages[p]          = v_repo[b]                           (byte copy)
+ * sel_ids, page_ids   device int32 [n_sel] (page_ids nullable).
+ * raw_k_repo, v_repo  device, [>= max id + 1][L][G][32][d], kv_dtype.
+ * k_pages, v_pages    device, [>= max page + 1][L][G][32][d]; v_repo and
+ *                     v_pages may both be NULL to skip the V copy.
+ * Ids >= max_blocks or pages < 0 are skipped and raise the device error flag.
+ */
+kvm_status kvm_assemble_view(kvm_ctx *ctx, const int32_t *sel_ids, const int32_t *page_ids,
+                             int32_t n_sel, const void *raw_k_repo, const void *v_repo,
+                             void *k_pages, void *v_pages, kvm_stream stream);
+
+/* Buffers used by kvm_step (bound once with kvm_bind). */
+typedef struct {
+    const void *index;   /* [L][G][max_blocks][d]; device or pinned host (index_location) */
+    const void *raw_k;   /* history raw K [max_blocks][L][G][32][d]; device or pinned host (repo_location) */
+    const void *v;       /* history V, same layout and location as raw_k */
+    void *pool_k;        /* device [pool_pages][L][G][32][d]: K at compact positions */
+    void *pool_v;        /* device [pool_pages][L][G][32][d]                         */
+    void *pool_raw_k;    /* device [pool_pages][L][G][32][d]: each page's raw K;
+                            required when repo_location == KVM_HOST_PINNED, else NULL */
+    int32_t *page_table; /* device [view_blocks]: page of each view slot             */
+    float *scores;       /* device [max_blocks]: R_b of the last step                */
+    int32_t *sel_ids;    /* device [view_blocks]: selected ids of the last step      */
+} kvm_buffers;
+
+kvm_status kvm_bind(kvm_ctx *ctx, const kvm_buffers *bufs);
+
+/* Forget which blocks the page pool holds (every page empty). */
+kvm_status kvm_reset_pool(kvm_ctx *ctx);
+
+typedef struct {
+    int64_t n_blocks;     /* history blocks scored                     */
+    int32_t n_sel;        /* view slots filled                         */
+    int32_t hits;         /* selected blocks already held by a page    */
+    int32_t misses;       /* selected blocks brought in (L_t^physical) */
+    int32_t reroped;      /* slots whose K was (re)written             */
+    int32_t evicted;      /* pages whose block left the pool           */
+    int32_t h2d_copies;   /* host-to-device copies issued              */
+    int64_t h2d_bytes;    /* bytes copied host to device               */
+} kvm_step_stats;
+
+/*
+ * (d) One working-set update: score + select (b), then the delta working set
+ * of [KVMem] §4.4: hits keep their page, misses (L_t^physical) take free pages
+ * in ascending order, the page table maps view slots to pages.  Misses are
+ * fetched from the repository: device-to-device inside the assembly kernel
+ * when repo_location == KVM_DEVICE; with coalesced host-to-device copies of
+ * raw K and V in batches of h2d_batch_blocks on an internal copy stream,
+ * each batch re-RoPE'd by the GPU after its copy event (the three-stage
+ * pipeline of [KVMem] §4.4, Figure 3) when KVM_HOST_PINNED.  Hits whose slot
+ * changed are re-RoPE'd from raw K.
+ * Synchronises with `stream` once (to read the selected ids) and returns
+ * with the rest enqueued; `stats` (nullable, host) is filled before return.
+ */
+kvm_status kvm_step(kvm_ctx *ctx, const void *q, int32_t n_queries, int64_t n_blocks,
+                    kvm_step_stats *stats, kvm_stream stream);
+
+/* Wait for all work of the context (its internal streams and `stream`) and
+ * report a raised device error flag (KVM_ERR_DEVICE), clearing it. */
+kvm_status kvm_sync(kvm_ctx *ctx, kvm_stream stream);
+
+const char *kvm_status_string(kvm_status s);
+
+/* Detail of the last error raised on the calling thread ("" if none). */
+const char *kvm_last_error(void);
+
+/* Host-side fault injection for tests: make the n-th (1-based) next host
+ * copy submission (what = 1) or kernel launch (what = 2) of kvm_step fail
+ * with KVM_ERR_INJECTED.  what = 0 clears.  The context stays usable. */
+kvm_status kvm_debug_inject(kvm_ctx *ctx, int32_t what, int64_t nth);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVM_H_ */

@@ -191,7 +191,7 @@ def scaled_scores(q: np.ndarray, index: np.ndarray, n_blocks: int) -> np.ndarray
     s = np.empty((L, M, H, n_blocks), dtype=np.float64)
     for h in range(H):
         g = h // r
-        s[:, :, h, :] = np.einsum("lmd,lbd->lmb", q[:, :, h, :], k[:, g, :, :])
+        s[:, :, h, :] = np.matmul(q[:, :, h, :], np.swapaxes(k[:, g, :, :], 1, 2))
     return s / np.sqrt(d)
 
 
@@ -205,16 +205,23 @@ def block_relevance(q: np.ndarray, index: np.ndarray, n_blocks: int,
     (l, h) pairs.  C is every indexed block (the method scores every
     retrievable historical block; sink and recent blocks are excluded only from
     the top-k fill).  ``q`` [L][M][H][d] and ``index`` [L][G][>=N][d] are float64.
-    With ``return_stats`` also returns the per-row max M and partition sum Z."""
+    With ``return_stats`` also returns the per-row max M and partition sum Z.
+    Evaluated one layer at a time to bound memory; the sum over layers is the
+    outer sum of the definition."""
     L, M, H, d = q.shape
-    s = scaled_scores(q, index, n_blocks)
-    mx = s.max(axis=-1, keepdims=True)
-    e = np.exp(s - mx)
-    z = e.sum(axis=-1, keepdims=True)
-    p = e / z
-    R = p.sum(axis=(0, 1, 2)) / (L * H)
+    R = np.zeros(n_blocks)
+    mxs, zs = [], []
+    for l in range(L):
+        s = scaled_scores(q[l:l + 1], index[l:l + 1], n_blocks)
+        mx = s.max(axis=-1, keepdims=True)
+        e = np.exp(s - mx)
+        z = e.sum(axis=-1, keepdims=True)
+        R += (e / z).sum(axis=(0, 1, 2))
+        mxs.append(mx[..., 0])
+        zs.append(z[..., 0])
+    R /= (L * H)
     if return_stats:
-        return R, mx[..., 0], z[..., 0]
+        return R, np.concatenate(mxs), np.concatenate(zs)
     return R
 
 

@@ -1,0 +1,179 @@
+// Execution-view assembly: gather + re-RoPE + V copy.
+//
+// KVMem (Virtualizing Million-Token Agent Workspaces on a Consumer GPU), §4.4:
+// a block entering the execution view gets RoPE applied to its position-
+// independent raw K at its compact position and the result is written into its
+// destination page; V is copied unchanged.  InferScale (GPU-Native KV Injection
+// for Personalized LLM Serving), Theorem 6: rotating stored pre-RoPE keys at
+// any chosen position yields exactly the scores they would have there.
+//
+// One CTA owns one view slot and a run of (layer, kv head) pairs.  The slot's
+// 32 rows of the cos/sin table (positions 32j .. 32j+31) are staged in shared
+// memory once.  Each thread rotates 8 (bf16) or 4 (float32) rotate-half pairs
+// of one token per pair of 16-byte loads and copies the matching 32 bytes of V.
+// HBM traffic per view token: L*G*d elements each of raw K read, K written,
+// V read, V written.
+#include "kvm_internal.cuh"
+#include "kvm_vec.cuh"
+
+namespace kvm {
+
+template <typename T, int D>
+struct SlotWork {
+    static constexpr int PPT = VecTraits<T>::N;
+    static constexpr int HD = D / 2;
+    static constexpr int TPT = HD / PPT;
+    static constexpr int NT = 32 * TPT;
+
+    // Rotate one block's K to positions pos0 + t for pairs [lg0, lg1) and copy V.
+    __device__ static void run(const T *__restrict__ src_k, const T *__restrict__ src_v,
+                               T *__restrict__ dst_k, T *__restrict__ dst_v, int64_t pos0,
+                               int lg0, int lg1, const float2 *__restrict__ table,
+                               float2 *tab) {
+        const int tid = threadIdx.x;
+        const int tok = tid / TPT, c = tid % TPT;
+        const float2 *trow = table + pos0 * HD;
+        for (int i = tid; i < kBlockTokens * HD; i += NT) tab[i] = trow[i];
+        __syncthreads();
+        float cs[PPT], sn[PPT];
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+            const float2 t = tab[tok * HD + c * PPT + i];
+            cs[i] = t.x;
+            sn[i] = t.y;
+        }
+        const size_t row = (size_t)tok * D + (size_t)c * PPT;
+        const bool do_v = (src_v != nullptr) && (dst_v != nullptr);
+#pragma unroll 2
+        for (int lg = lg0; lg < lg1; ++lg) {
+            const size_t off = (size_t)lg * kBlockTokens * D + row;
+            const uint4 vx = ld_stream(src_k + off);
+            const uint4 vy = ld_stream(src_k + off + HD);
+            uint4 wx = make_uint4(0, 0, 0, 0), wy = wx;
+            if (do_v) {
+                wx = ld_stream(src_v + off);
+                wy = ld_stream(src_v + off + HD);
+            }
+            float x[PPT], y[PPT], ox[PPT], oy[PPT];
+            VecTraits<T>::unpack(vx, x);
+            VecTraits<T>::unpack(vy, y);
+#pragma unroll
+            for (int i = 0; i < PPT; ++i) {
+                // R_p: (x cos - y sin, x sin + y cos), each product rounded
+                ox[i] = __fsub_rn(__fmul_rn(x[i], cs[i]), __fmul_rn(y[i], sn[i]));
+                oy[i] = __fadd_rn(__fmul_rn(x[i], sn[i]), __fmul_rn(y[i], cs[i]));
+            }
+            st_stream(dst_k + off, VecTraits<T>::pack(ox));
+            st_stream(dst_k + off + HD, VecTraits<T>::pack(oy));
+            if (do_v) {
+                st_stream(dst_v + off, wx);
+                st_stream(dst_v + off + HD, wy);
+            }
+        }
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(SlotWork<T, D>::NT)
+assemble_ids_kernel(const int32_t *__restrict__ sel_ids, const int32_t *__restrict__ page_ids,
+                    int64_t max_blocks, const T *raw_k_repo, const T *v_repo, T *k_pages,
+                    T *v_pages, int LG, int lg_per_cta, const float2 *__restrict__ table,
+                    int *err) {
+    __shared__ float2 tab[kBlockTokens * (D / 2)];
+    const int j = blockIdx.x;
+    const int64_t b = sel_ids[j];
+    const int64_t p = page_ids ? (int64_t)page_ids[j] : (int64_t)j;
+    if (b < 0 || b >= max_blocks || p < 0) {
+        if (threadIdx.x == 0) atomicOr(err, 1);
+        return;
+    }
+    const size_t blk = (size_t)LG * kBlockTokens * D;
+    const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
+    SlotWork<T, D>::run(raw_k_repo + b * blk, v_repo ? v_repo + b * blk : nullptr,
+                        k_pages + p * blk, v_pages ? v_pages + p * blk : nullptr,
+                        (int64_t)j * kBlockTokens, lg0, lg1, table, tab);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(SlotWork<T, D>::NT)
+assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
+                     const float2 *__restrict__ table, int64_t max_pos, int *err) {
+    __shared__ float2 tab[kBlockTokens * (D / 2)];
+    const SlotDesc sd = desc[blockIdx.x];
+    if (sd.pos0 < 0 || sd.pos0 + kBlockTokens > max_pos || sd.src_k == nullptr ||
+        sd.dst_k == nullptr) {
+        if (threadIdx.x == 0) atomicOr(err, 2);
+        return;
+    }
+    const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
+    SlotWork<T, D>::run(static_cast<const T *>(sd.src_k), static_cast<const T *>(sd.src_v),
+                        static_cast<T *>(sd.dst_k), static_cast<T *>(sd.dst_v), sd.pos0, lg0,
+                        lg1, table, tab);
+}
+
+static int lg_split(int n_slots, int LG) {
+    int lpc = LG;
+    while (lpc > 8 && (int64_t)n_slots * ((LG + lpc - 1) / lpc) < 152 * 16) lpc = (lpc + 1) / 2;
+    return lpc > 64 ? 64 : lpc;
+}
+
+template <typename T, int D>
+static cudaError_t ids_t(const int32_t *sel_ids, const int32_t *page_ids, int n_sel,
+                         int64_t max_blocks, const void *rk, const void *v, void *kp, void *vp,
+                         int LG, const float2 *table, int *err, cudaStream_t s) {
+    const int lpc = lg_split(n_sel, LG);
+    dim3 grid((unsigned)n_sel, (unsigned)((LG + lpc - 1) / lpc));
+    assemble_ids_kernel<T, D><<<grid, SlotWork<T, D>::NT, 0, s>>>(
+        sel_ids, page_ids, max_blocks, static_cast<const T *>(rk), static_cast<const T *>(v),
+        static_cast<T *>(kp), static_cast<T *>(vp), LG, lpc, table, err);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t desc_t(const SlotDesc *desc, int n_desc, int LG, const float2 *table,
+                          int64_t max_pos, int *err, cudaStream_t s) {
+    const int lpc = lg_split(n_desc, LG);
+    dim3 grid((unsigned)n_desc, (unsigned)((LG + lpc - 1) / lpc));
+    assemble_desc_kernel<T, D><<<grid, SlotWork<T, D>::NT, 0, s>>>(desc, LG, lpc, table,
+                                                                     max_pos, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_assemble_ids(int kv_dtype, int d, const int32_t *sel_ids,
+                                const int32_t *page_ids, int n_sel, int64_t max_blocks,
+                                const void *raw_k_repo, const void *v_repo, void *k_pages,
+                                void *v_pages, int LG, const float2 *table, int64_t max_pos,
+                                int *err, cudaStream_t s) {
+    (void)max_pos;  // n_sel * 32 <= max_pos is checked on the host
+    if (n_sel <= 0) return cudaSuccess;
+    if (kv_dtype == BF16 && d == 128)
+        return ids_t<__nv_bfloat16, 128>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo,
+                                         v_repo, k_pages, v_pages, LG, table, err, s);
+    if (kv_dtype == BF16 && d == 64)
+        return ids_t<__nv_bfloat16, 64>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo,
+                                        v_repo, k_pages, v_pages, LG, table, err, s);
+    if (kv_dtype == F32 && d == 128)
+        return ids_t<float, 128>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo, v_repo,
+                                 k_pages, v_pages, LG, table, err, s);
+    if (kv_dtype == F32 && d == 64)
+        return ids_t<float, 64>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo, v_repo,
+                                k_pages, v_pages, LG, table, err, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_assemble_desc(int kv_dtype, int d, const SlotDesc *desc, int n_desc, int LG,
+                                 const float2 *table, int64_t max_pos, int *err,
+                                 cudaStream_t s) {
+    if (n_desc <= 0) return cudaSuccess;
+    if (kv_dtype == BF16 && d == 128)
+        return desc_t<__nv_bfloat16, 128>(desc, n_desc, LG, table, max_pos, err, s);
+    if (kv_dtype == BF16 && d == 64)
+        return desc_t<__nv_bfloat16, 64>(desc, n_desc, LG, table, max_pos, err, s);
+    if (kv_dtype == F32 && d == 128)
+        return desc_t<float, 128>(desc, n_desc, LG, table, max_pos, err, s);
+    if (kv_dtype == F32 && d == 64)
+        return desc_t<float, 64>(desc, n_desc, LG, table, max_pos, err, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kvm

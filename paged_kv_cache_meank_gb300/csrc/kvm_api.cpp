@@ -1,0 +1,645 @@
+// Host runtime of libkvm: the C ABI of include/kvm.h.
+//
+// Owns only host metadata (config, residency of the page pool, baked
+// positions), one internal copy stream and a few events.  Device memory is the
+// caller's: one workspace carved into the RoPE table and scoring scratch, plus
+// the buffers passed to each call or bound with kvm_bind.
+//
+// Residency and page reuse follow KVMem (Virtualizing Million-Token Agent
+// Workspaces on a Consumer GPU), §4.4 (delta working set: hits keep their
+// pages, only L_t^physical is staged in; packed, pipelined rematerialization
+// with CUDA events, Figure 3) and §5 (block record: chronological id, tier,
+// baked position).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvm.h"
+#include "kvm_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvm_status fail(kvm_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+kvm_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(KVM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define KVM_CUDA(call)                                             \
+    do {                                                           \
+        cudaError_t e_ = (call);                                   \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);        \
+    } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t elt_bytes(int dt) { return dt == KVM_BF16 ? 2 : 4; }
+
+struct Layout {
+    size_t table, part_m, part_z, row_m, row_invz, partial, stage0, stage1, desc, err, total;
+    size_t stage_bytes;
+    int rows_max, chunk_cap;
+};
+
+bool config_ok(const kvm_config *c, std::string *why) {
+    auto bad = [&](const char *m) { *why = m; return false; };
+    if (!c) return bad("config is NULL");
+    if (c->n_layers < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1) return bad("L, G, H must be >= 1");
+    if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+    if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+    if (c->block_tokens != 32) return bad("block_tokens must be 32");
+    if (!(c->rope_theta > 1.0)) return bad("rope_theta must be > 1");
+    for (int dt : {c->kv_dtype, c->index_dtype, c->q_dtype})
+        if (dt != KVM_F32 && dt != KVM_BF16) return bad("dtype must be KVM_F32 or KVM_BF16");
+    if (c->sink_blocks < 0 || c->recent_blocks < 0) return bad("sink/recent must be >= 0");
+    if (c->view_blocks < c->sink_blocks + c->recent_blocks + 1)
+        return bad("view_blocks must be >= sink + recent + 1");
+    if (c->max_queries < 1) return bad("max_queries must be >= 1");
+    if ((int64_t)c->max_queries * (c->n_q_heads / c->n_kv_heads) > kvm::kMaxRows)
+        return bad("max_queries * (H/G) must be <= 256");
+    if (c->max_blocks < 1 || c->max_blocks > (int64_t)1 << 30) return bad("max_blocks out of range");
+    if (c->max_positions < 32 * (int64_t)c->view_blocks)
+        return bad("max_positions must cover the view (32 * view_blocks)");
+    if (c->index_location != KVM_DEVICE && c->index_location != KVM_HOST_PINNED)
+        return bad("index_location must be KVM_DEVICE or KVM_HOST_PINNED");
+    if (c->repo_location != KVM_DEVICE && c->repo_location != KVM_HOST_PINNED)
+        return bad("repo_location must be KVM_DEVICE or KVM_HOST_PINNED");
+    if (c->index_location == KVM_HOST_PINNED && c->tile_blocks < 1)
+        return bad("tile_blocks must be >= 1 for a host-resident index");
+    if (c->pool_pages < c->view_blocks) return bad("pool_pages must be >= view_blocks");
+    if (c->h2d_batch_blocks < 1) return bad("h2d_batch_blocks must be >= 1");
+    return true;
+}
+
+Layout layout_of(const kvm_config *c) {
+    Layout lo{};
+    const size_t LG = (size_t)c->n_layers * c->n_kv_heads;
+    lo.rows_max = c->max_queries * (c->n_q_heads / c->n_kv_heads);
+    lo.chunk_cap = kvm::kMaxChunks;
+    if (c->index_location == KVM_HOST_PINNED) {
+        const int64_t tiles = (c->max_blocks + c->tile_blocks - 1) / c->tile_blocks;
+        lo.chunk_cap = (int)std::max<int64_t>(kvm::kMaxChunks, tiles);
+    }
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    lo.table = take((size_t)c->max_positions * (c->head_dim / 2) * sizeof(float2));
+    lo.part_m = take(LG * lo.chunk_cap * lo.rows_max * sizeof(float));
+    lo.part_z = take(LG * lo.chunk_cap * lo.rows_max * sizeof(float));
+    lo.row_m = take(LG * lo.rows_max * sizeof(float));
+    lo.row_invz = take(LG * lo.rows_max * sizeof(float));
+    lo.partial = take(LG * (size_t)c->max_blocks * sizeof(float));
+    lo.stage_bytes = 0;
+    if (c->index_location == KVM_HOST_PINNED)
+        lo.stage_bytes = LG * (size_t)c->tile_blocks * c->head_dim * elt_bytes(c->index_dtype);
+    lo.stage0 = take(lo.stage_bytes);
+    lo.stage1 = take(lo.stage_bytes);
+    lo.desc = take((size_t)(c->pool_pages + c->view_blocks) * sizeof(kvm::SlotDesc));
+    lo.err = take(256);
+    lo.total = off;
+    return lo;
+}
+
+}  // namespace
+
+struct kvm_ctx {
+    kvm_config cfg{};
+    Layout lo{};
+    char *ws = nullptr;
+    float2 *table = nullptr;
+    kvm::ScoreScratch scr{};
+    void *stage[2] = {nullptr, nullptr};
+    kvm::SlotDesc *desc_dev = nullptr;
+    int *err_dev = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_ready[2] = {nullptr, nullptr};
+    cudaEvent_t ev_free[2] = {nullptr, nullptr};
+    cudaEvent_t ev_main = nullptr;
+    std::vector<cudaEvent_t> ev_batch;
+    bool bound = false;
+    kvm_buffers bufs{};
+    // residency of the page pool
+    std::vector<int64_t> block_of_page;
+    std::vector<int64_t> baked_pos;
+    std::vector<int32_t> page_of_block;
+    std::vector<uint8_t> mark;
+    // fault injection
+    int inject_what = 0;
+    int64_t inject_nth = 0, inject_seen = 0;
+    int device = 0;
+};
+
+namespace {
+
+bool injected(kvm_ctx *c, int what) {
+    if (c->inject_what != what) return false;
+    if (++c->inject_seen == c->inject_nth) {
+        c->inject_what = 0;
+        return true;
+    }
+    return false;
+}
+
+kvm::ScoreShape shape_of(const kvm_ctx *c, int n_queries, int64_t index_cap) {
+    kvm::ScoreShape sh{};
+    sh.L = c->cfg.n_layers;
+    sh.G = c->cfg.n_kv_heads;
+    sh.H = c->cfg.n_q_heads;
+    sh.d = c->cfg.head_dim;
+    sh.n_queries = n_queries;
+    sh.gqa = sh.H / sh.G;
+    sh.rows = n_queries * sh.gqa;
+    sh.index_cap = index_cap;
+    sh.chunk_cap = c->lo.chunk_cap;
+    return sh;
+}
+
+size_t block_bytes(const kvm_config &c) {
+    return (size_t)c.n_layers * c.n_kv_heads * 32 * c.head_dim * elt_bytes(c.kv_dtype);
+}
+
+void reset_pool(kvm_ctx *c) {
+    for (int64_t b : c->block_of_page)
+        if (b >= 0 && b < (int64_t)c->page_of_block.size()) c->page_of_block[b] = -1;
+    std::fill(c->block_of_page.begin(), c->block_of_page.end(), -1);
+    std::fill(c->baked_pos.begin(), c->baked_pos.end(), -1);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvm_workspace_bytes(const kvm_config *cfg) {
+    std::string why;
+    if (!config_ok(cfg, &why)) return 0;
+    return layout_of(cfg).total;
+}
+
+kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_bytes,
+                      kvm_stream stream, kvm_ctx **out) {
+    std::string why;
+    if (!out) return fail(KVM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!config_ok(cfg, &why)) return fail(KVM_ERR_INVALID_ARG, "config: %s", why.c_str());
+    Layout lo = layout_of(cfg);
+    if (!workspace) return fail(KVM_ERR_INVALID_ARG, "workspace is NULL");
+    if (((uintptr_t)workspace & 255) != 0) return fail(KVM_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (workspace_bytes < lo.total)
+        return fail(KVM_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lo.total);
+    auto *c = new (std::nothrow) kvm_ctx();
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "out of host memory");
+    c->cfg = *cfg;
+    c->lo = lo;
+    c->ws = static_cast<char *>(workspace);
+    c->table = reinterpret_cast<float2 *>(c->ws + lo.table);
+    c->scr.part_m = reinterpret_cast<float *>(c->ws + lo.part_m);
+    c->scr.part_z = reinterpret_cast<float *>(c->ws + lo.part_z);
+    c->scr.row_m = reinterpret_cast<float *>(c->ws + lo.row_m);
+    c->scr.row_invz = reinterpret_cast<float *>(c->ws + lo.row_invz);
+    c->scr.partial = reinterpret_cast<float *>(c->ws + lo.partial);
+    c->stage[0] = c->ws + lo.stage0;
+    c->stage[1] = c->ws + lo.stage1;
+    c->desc_dev = reinterpret_cast<kvm::SlotDesc *>(c->ws + lo.desc);
+    c->err_dev = reinterpret_cast<int *>(c->ws + lo.err);
+    c->block_of_page.assign(cfg->pool_pages, -1);
+    c->baked_pos.assign(cfg->pool_pages, -1);
+    c->page_of_block.assign((size_t)cfg->max_blocks, -1);
+    c->mark.assign((size_t)cfg->max_blocks, 0);
+
+    auto cleanup = [&](kvm_status s) { kvm_destroy(c); return s; };
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaGetDevice"));
+    e = cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaStreamCreateWithFlags"));
+    for (int i = 0; i < 2; ++i) {
+        if ((e = cudaEventCreateWithFlags(&c->ev_ready[i], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "cudaEventCreate"));
+    }
+    if ((e = cudaEventCreateWithFlags(&c->ev_main, cudaEventDisableTiming)) != cudaSuccess)
+        return cleanup(cuda_fail(e, "cudaEventCreate"));
+    const int n_batches =
+        (cfg->pool_pages + cfg->h2d_batch_blocks - 1) / cfg->h2d_batch_blocks + 1;
+    c->ev_batch.assign(n_batches, nullptr);
+    for (auto &ev : c->ev_batch)
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "cudaEventCreate"));
+
+    kvm::Omega om{};
+    const int hd = cfg->head_dim / 2;
+    for (int i = 0; i < hd; ++i) om.w[i] = std::pow(cfg->rope_theta, -2.0 * i / cfg->head_dim);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((e = kvm::launch_rope_table(c->table, cfg->max_positions, hd, om, s)) != cudaSuccess)
+        return cleanup(cuda_fail(e, "rope table"));
+    if ((e = cudaMemsetAsync(c->err_dev, 0, sizeof(int), s)) != cudaSuccess)
+        return cleanup(cuda_fail(e, "cudaMemsetAsync"));
+    *out = c;
+    return KVM_OK;
+}
+
+kvm_status kvm_destroy(kvm_ctx *c) {
+    if (!c) return KVM_OK;
+    if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+    for (auto ev : {c->ev_ready[0], c->ev_ready[1], c->ev_free[0], c->ev_free[1], c->ev_main})
+        if (ev) cudaEventDestroy(ev);
+    for (auto ev : c->ev_batch)
+        if (ev) cudaEventDestroy(ev);
+    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    delete c;
+    return KVM_OK;
+}
+
+kvm_status kvm_build_index(kvm_ctx *c, const void *k_pages, int64_t first_block,
+                           int64_t n_blocks, void *index, void *raw_k_out, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!k_pages || !index) return fail(KVM_ERR_INVALID_ARG, "k_pages and index are required");
+    if (first_block < 0 || n_blocks < 0) return fail(KVM_ERR_INVALID_ARG, "negative block range");
+    if (first_block + n_blocks > c->cfg.max_blocks)
+        return fail(KVM_ERR_CAPACITY, "blocks [%lld, %lld) beyond max_blocks %lld",
+                    (long long)first_block, (long long)(first_block + n_blocks),
+                    (long long)c->cfg.max_blocks);
+    if ((first_block + n_blocks) * 32 > c->cfg.max_positions)
+        return fail(KVM_ERR_CAPACITY, "positions up to %lld beyond max_positions %lld",
+                    (long long)((first_block + n_blocks) * 32), (long long)c->cfg.max_positions);
+    if (n_blocks == 0) return KVM_OK;
+    const cudaError_t e = kvm::launch_meank(
+        c->cfg.kv_dtype, c->cfg.index_dtype, c->cfg.head_dim, k_pages, raw_k_out, index,
+        c->cfg.max_blocks, first_block, n_blocks, c->cfg.n_layers * c->cfg.n_kv_heads,
+        c->table, c->err_dev, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "meank launch");
+    return KVM_OK;
+}
+
+static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void *q,
+                               const void *index, int64_t N, float *scores, cudaStream_t s) {
+    const int nch = kvm::score_chunks(sh, N, kvm::kMaxChunks);
+    cudaError_t e;
+    if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0, 0, N,
+                                     0, nch, c->scr, s)) != cudaSuccess)
+        return cuda_fail(e, "score pass 1");
+    if ((e = kvm::launch_score_combine(sh, nch, c->scr, s)) != cudaSuccess)
+        return cuda_fail(e, "score combine");
+    if ((e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0, 0, N,
+                                     nch, c->scr, c->cfg.max_blocks, s)) != cudaSuccess)
+        return cuda_fail(e, "score pass 2");
+    if ((e = kvm::launch_score_reduce(sh, N, c->scr, c->cfg.max_blocks, scores, s)) != cudaSuccess)
+        return cuda_fail(e, "score reduce");
+    return KVM_OK;
+}
+
+// Index in pinned host memory: tiles of tile_blocks staged through two device
+// buffers on the copy stream; the softmax stays global because pass 1 only
+// records per-chunk (max, sum) and the combine folds every tile's chunks
+// before pass 2 re-streams the tiles (KVMem §5, tiled retrieval).
+static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q,
+                                   const void *index, int64_t N, float *scores, cudaStream_t s) {
+    const int64_t tile = c->cfg.tile_blocks;
+    const int64_t T = (N + tile - 1) / tile;
+    const int cpt = std::max(1, std::min(kvm::score_chunks(sh, tile, kvm::kMaxChunks),
+                                         (int)(c->lo.chunk_cap / T)));
+    const size_t eb = elt_bytes(c->cfg.index_dtype);
+    const size_t row = (size_t)c->cfg.head_dim * eb;
+    const size_t LG = (size_t)c->cfg.n_layers * c->cfg.n_kv_heads;
+    cudaError_t e;
+    KVM_CUDA(cudaEventRecord(c->ev_main, s));
+    KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0));
+    kvm::ScoreShape tsh = sh;
+    tsh.index_cap = tile;
+    for (int pass = 1; pass <= 2; ++pass) {
+        for (int64_t t = 0; t < T; ++t) {
+            const int buf = (int)(t & 1);
+            const int64_t b0 = t * tile, nb = std::min(tile, N - b0);
+            KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
+            KVM_CUDA(cudaMemcpy2DAsync(c->stage[buf], tile * row,
+                                       static_cast<const char *>(index) + b0 * row,
+                                       (size_t)c->cfg.max_blocks * row, nb * row, LG,
+                                       cudaMemcpyHostToDevice, c->copy_stream));
+            KVM_CUDA(cudaEventRecord(c->ev_ready[buf], c->copy_stream));
+            KVM_CUDA(cudaStreamWaitEvent(s, c->ev_ready[buf], 0));
+            if (pass == 1)
+                e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
+                                            c->stage[buf], b0, b0, b0 + nb, (int)(t * cpt), cpt,
+                                            c->scr, s);
+            else
+                e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
+                                            c->stage[buf], b0, b0, b0 + nb, cpt, c->scr,
+                                            c->cfg.max_blocks, s);
+            if (e != cudaSuccess) return cuda_fail(e, "tiled score pass");
+            KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
+        }
+        if (pass == 1 && (e = kvm::launch_score_combine(sh, (int)(T * cpt), c->scr, s)) != cudaSuccess)
+            return cuda_fail(e, "score combine");
+    }
+    if ((e = kvm::launch_score_reduce(sh, N, c->scr, c->cfg.max_blocks, scores, s)) != cudaSuccess)
+        return cuda_fail(e, "score reduce");
+    return KVM_OK;
+}
+
+kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const void *index,
+                            int64_t n_blocks, float *scores_out, int32_t *sel_ids_out,
+                            int32_t *n_sel_out, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!q || !index || !scores_out || !sel_ids_out)
+        return fail(KVM_ERR_INVALID_ARG, "q, index, scores_out and sel_ids_out are required");
+    if (n_queries < 1 || n_blocks < 1) return fail(KVM_ERR_INVALID_ARG, "n_queries and n_blocks must be >= 1");
+    if (n_queries > c->cfg.max_queries)
+        return fail(KVM_ERR_CAPACITY, "n_queries %d > max_queries %d", n_queries, c->cfg.max_queries);
+    if (n_blocks > c->cfg.max_blocks)
+        return fail(KVM_ERR_CAPACITY, "n_blocks %lld > max_blocks %lld", (long long)n_blocks,
+                    (long long)c->cfg.max_blocks);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const kvm::ScoreShape sh = shape_of(c, n_queries, c->cfg.max_blocks);
+    kvm_status st = c->cfg.index_location == KVM_DEVICE
+                        ? score_device(c, sh, q, index, n_blocks, scores_out, s)
+                        : score_host_tiled(c, sh, q, index, n_blocks, scores_out, s);
+    if (st != KVM_OK) return st;
+    const cudaError_t e = kvm::launch_select(scores_out, n_blocks, c->cfg.sink_blocks,
+                                             c->cfg.recent_blocks, c->cfg.view_blocks,
+                                             sel_ids_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "select launch");
+    if (n_sel_out) *n_sel_out = (int32_t)std::min<int64_t>(n_blocks, c->cfg.view_blocks);
+    return KVM_OK;
+}
+
+kvm_status kvm_assemble_view(kvm_ctx *c, const int32_t *sel_ids, const int32_t *page_ids,
+                             int32_t n_sel, const void *raw_k_repo, const void *v_repo,
+                             void *k_pages, void *v_pages, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!sel_ids || !raw_k_repo || !k_pages)
+        return fail(KVM_ERR_INVALID_ARG, "sel_ids, raw_k_repo and k_pages are required");
+    if ((v_repo == nullptr) != (v_pages == nullptr))
+        return fail(KVM_ERR_INVALID_ARG, "v_repo and v_pages must both be set or both be NULL");
+    if (n_sel < 0) return fail(KVM_ERR_INVALID_ARG, "n_sel < 0");
+    if ((int64_t)n_sel * 32 > c->cfg.max_positions)
+        return fail(KVM_ERR_CAPACITY, "view of %d slots beyond max_positions", n_sel);
+    if (n_sel == 0) return KVM_OK;
+    const cudaError_t e = kvm::launch_assemble_ids(
+        c->cfg.kv_dtype, c->cfg.head_dim, sel_ids, page_ids, n_sel, c->cfg.max_blocks,
+        raw_k_repo, v_repo, k_pages, v_pages, c->cfg.n_layers * c->cfg.n_kv_heads, c->table,
+        c->cfg.max_positions, c->err_dev, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "assemble launch");
+    return KVM_OK;
+}
+
+kvm_status kvm_bind(kvm_ctx *c, const kvm_buffers *b) {
+    if (!c || !b) return fail(KVM_ERR_INVALID_ARG, "ctx and buffers are required");
+    if (!b->index || !b->raw_k || !b->v || !b->pool_k || !b->pool_v || !b->page_table ||
+        !b->scores || !b->sel_ids)
+        return fail(KVM_ERR_INVALID_ARG, "a required buffer is NULL");
+    if (c->cfg.repo_location == KVM_HOST_PINNED && !b->pool_raw_k)
+        return fail(KVM_ERR_INVALID_ARG, "pool_raw_k is required with a host-resident repository");
+    c->bufs = *b;
+    c->bound = true;
+    reset_pool(c);
+    return KVM_OK;
+}
+
+kvm_status kvm_reset_pool(kvm_ctx *c) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    reset_pool(c);
+    return KVM_OK;
+}
+
+kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
+                    kvm_step_stats *stats, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!c->bound) return fail(KVM_ERR_NOT_BOUND, "kvm_step before kvm_bind");
+    const kvm_config &cfg = c->cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t n_sel = 0;
+    kvm_status st = kvm_score_select(c, q, n_queries, c->bufs.index, n_blocks, c->bufs.scores,
+                                     c->bufs.sel_ids, &n_sel, stream);
+    if (st != KVM_OK) return st;
+
+    // the selected ids drive the host-side residency diff
+    std::vector<int32_t> sel(n_sel);
+    KVM_CUDA(cudaMemcpyAsync(sel.data(), c->bufs.sel_ids, n_sel * sizeof(int32_t),
+                             cudaMemcpyDeviceToHost, s));
+    KVM_CUDA(cudaStreamSynchronize(s));
+
+    // delta working set: hits keep their pages, misses take free pages in
+    // ascending page order, in ascending slot order
+    const int P = cfg.pool_pages;
+    std::vector<int32_t> page_of_slot(n_sel, -1);
+    std::vector<uint8_t> is_hit(n_sel, 0);
+    for (int j = 0; j < n_sel; ++j) {
+        const int32_t b = sel[j];
+        if (b < 0 || b >= cfg.max_blocks) return fail(KVM_ERR_DEVICE, "selected id %d out of range", b);
+        c->mark[b] = 1;
+        if (c->page_of_block[b] >= 0) {
+            page_of_slot[j] = c->page_of_block[b];
+            is_hit[j] = 1;
+        }
+    }
+    std::vector<int32_t> free_pages;
+    free_pages.reserve(P);
+    for (int p = 0; p < P; ++p) {
+        const int64_t b = c->block_of_page[p];
+        if (b < 0 || !c->mark[b]) free_pages.push_back(p);
+    }
+    for (int j = 0; j < n_sel; ++j) c->mark[sel[j]] = 0;
+    int n_miss = 0;
+    for (int j = 0; j < n_sel; ++j) n_miss += !is_hit[j];
+    if (n_miss > (int)free_pages.size())
+        return fail(KVM_ERR_CAPACITY, "%d misses but only %zu free pages", n_miss, free_pages.size());
+    {
+        int f = 0;
+        for (int j = 0; j < n_sel; ++j)
+            if (!is_hit[j]) page_of_slot[j] = free_pages[f++];
+    }
+
+    const size_t blk = block_bytes(cfg);
+    const bool host_repo = cfg.repo_location == KVM_HOST_PINNED;
+    auto P_k = [&](int p) { return static_cast<char *>(c->bufs.pool_k) + (size_t)p * blk; };
+    auto P_v = [&](int p) { return static_cast<char *>(c->bufs.pool_v) + (size_t)p * blk; };
+    auto P_r = [&](int p) { return static_cast<char *>(c->bufs.pool_raw_k) + (size_t)p * blk; };
+    auto R_k = [&](int64_t b) { return static_cast<const char *>(c->bufs.raw_k) + (size_t)b * blk; };
+    auto R_v = [&](int64_t b) { return static_cast<const char *>(c->bufs.v) + (size_t)b * blk; };
+
+    // descriptors: shifted hits first (no copy to wait for), then misses in slot order
+    std::vector<kvm::SlotDesc> desc;
+    desc.reserve(n_sel);
+    int n_rope = 0, evicted = 0;
+    for (int j = 0; j < n_sel; ++j) {
+        if (!is_hit[j]) continue;
+        const int p = page_of_slot[j];
+        if (c->baked_pos[p] == (int64_t)j * 32) continue;
+        kvm::SlotDesc d{};
+        d.src_k = host_repo ? P_r(p) : R_k(sel[j]);
+        d.dst_k = P_k(p);
+        d.pos0 = (int64_t)j * 32;
+        desc.push_back(d);
+    }
+    const int n_hit_rope = (int)desc.size();
+    std::vector<int> miss_slots;
+    for (int j = 0; j < n_sel; ++j) {
+        if (is_hit[j]) continue;
+        miss_slots.push_back(j);
+        const int p = page_of_slot[j];
+        kvm::SlotDesc d{};
+        if (host_repo) {
+            d.src_k = P_r(p);
+        } else {
+            d.src_k = R_k(sel[j]);
+            d.src_v = R_v(sel[j]);
+            d.dst_v = P_v(p);
+        }
+        d.dst_k = P_k(p);
+        d.pos0 = (int64_t)j * 32;
+        desc.push_back(d);
+    }
+    n_rope = (int)desc.size();
+
+    auto abort_step = [&](kvm_status err) {
+        // pages may be partly overwritten: forget the whole pool
+        reset_pool(c);
+        return err;
+    };
+    const int LG = cfg.n_layers * cfg.n_kv_heads;
+    int64_t h2d_bytes = 0;
+    int h2d_copies = 0;
+    cudaError_t e;
+    if (n_rope > 0) {
+        if ((e = cudaMemcpyAsync(c->desc_dev, desc.data(), desc.size() * sizeof(kvm::SlotDesc),
+                                 cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return abort_step(cuda_fail(e, "descriptor upload"));
+    }
+    if (!host_repo) {
+        if (n_rope > 0) {
+            if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
+            if ((e = kvm::launch_assemble_desc(cfg.kv_dtype, cfg.head_dim, c->desc_dev, n_rope, LG,
+                                               c->table, cfg.max_positions, c->err_dev, s)) != cudaSuccess)
+                return abort_step(cuda_fail(e, "assemble launch"));
+        }
+    } else {
+        if (n_hit_rope > 0) {
+            if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
+            if ((e = kvm::launch_assemble_desc(cfg.kv_dtype, cfg.head_dim, c->desc_dev, n_hit_rope,
+                                               LG, c->table, cfg.max_positions, c->err_dev, s)) != cudaSuccess)
+                return abort_step(cuda_fail(e, "re-RoPE launch"));
+        }
+        // misses: coalesced H2D of raw K and V straight into their pages on the
+        // copy stream, one event per batch; the GPU re-RoPEs batch i while
+        // batch i+1 is in flight
+        if ((e = cudaEventRecord(c->ev_main, s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0)) != cudaSuccess)
+            return abort_step(cuda_fail(e, "stream join"));
+        const int nb_batch = cfg.h2d_batch_blocks;
+        int batch = 0;
+        for (size_t i0 = 0; i0 < miss_slots.size(); i0 += nb_batch, ++batch) {
+            const size_t i1 = std::min(miss_slots.size(), i0 + nb_batch);
+            size_t i = i0;
+            while (i < i1) {
+                // a run: consecutive block ids landing in consecutive pages
+                size_t k = i + 1;
+                while (k < i1 && sel[miss_slots[k]] == sel[miss_slots[k - 1]] + 1 &&
+                       page_of_slot[miss_slots[k]] == page_of_slot[miss_slots[k - 1]] + 1)
+                    ++k;
+                const int64_t b0 = sel[miss_slots[i]];
+                const int p0 = page_of_slot[miss_slots[i]];
+                const size_t bytes = (k - i) * blk;
+                if (injected(c, 1)) return abort_step(fail(KVM_ERR_INJECTED, "injected copy failure"));
+                if ((e = cudaMemcpyAsync(P_r(p0), R_k(b0), bytes, cudaMemcpyHostToDevice,
+                                         c->copy_stream)) != cudaSuccess ||
+                    (e = cudaMemcpyAsync(P_v(p0), R_v(b0), bytes, cudaMemcpyHostToDevice,
+                                         c->copy_stream)) != cudaSuccess)
+                    return abort_step(cuda_fail(e, "H2D copy"));
+                h2d_bytes += 2 * (int64_t)bytes;
+                h2d_copies += 2;
+                i = k;
+            }
+            cudaEvent_t ev = c->ev_batch[batch % c->ev_batch.size()];
+            if ((e = cudaEventRecord(ev, c->copy_stream)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, ev, 0)) != cudaSuccess)
+                return abort_step(cuda_fail(e, "batch event"));
+            if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
+            if ((e = kvm::launch_assemble_desc(cfg.kv_dtype, cfg.head_dim,
+                                               c->desc_dev + n_hit_rope + i0, (int)(i1 - i0), LG,
+                                               c->table, cfg.max_positions, c->err_dev, s)) != cudaSuccess)
+                return abort_step(cuda_fail(e, "re-RoPE launch"));
+        }
+    }
+    if ((e = cudaMemcpyAsync(c->bufs.page_table, page_of_slot.data(), n_sel * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return abort_step(cuda_fail(e, "page table upload"));
+
+    // commit the new residency
+    for (int j : miss_slots) {
+        const int p = page_of_slot[j];
+        const int64_t old = c->block_of_page[p];
+        if (old >= 0) {
+            c->page_of_block[old] = -1;
+            ++evicted;
+        }
+        c->block_of_page[p] = sel[j];
+        c->page_of_block[sel[j]] = p;
+    }
+    for (int j = 0; j < n_sel; ++j) c->baked_pos[page_of_slot[j]] = (int64_t)j * 32;
+
+    if (stats) {
+        stats->n_blocks = n_blocks;
+        stats->n_sel = n_sel;
+        stats->misses = (int32_t)miss_slots.size();
+        stats->hits = n_sel - stats->misses;
+        stats->reroped = n_rope;
+        stats->evicted = evicted;
+        stats->h2d_copies = h2d_copies;
+        stats->h2d_bytes = h2d_bytes;
+    }
+    return KVM_OK;
+}
+
+kvm_status kvm_sync(kvm_ctx *c, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    KVM_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    KVM_CUDA(cudaStreamSynchronize(c->copy_stream));
+    int flag = 0;
+    KVM_CUDA(cudaMemcpy(&flag, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost));
+    if (flag) {
+        KVM_CUDA(cudaMemset(c->err_dev, 0, sizeof(int)));
+        return fail(KVM_ERR_DEVICE, "device range check raised flag 0x%x", flag);
+    }
+    return KVM_OK;
+}
+
+const char *kvm_status_string(kvm_status s) {
+    switch (s) {
+        case KVM_OK: return "ok";
+        case KVM_ERR_INVALID_ARG: return "invalid argument";
+        case KVM_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case KVM_ERR_CAPACITY: return "capacity exceeded";
+        case KVM_ERR_CUDA: return "CUDA error";
+        case KVM_ERR_TIMEOUT: return "device wait timed out";
+        case KVM_ERR_NOT_BOUND: return "buffers not bound";
+        case KVM_ERR_INJECTED: return "injected failure";
+        case KVM_ERR_DEVICE: return "device range check failed";
+    }
+    return "unknown status";
+}
+
+const char *kvm_last_error(void) { return g_last_error.c_str(); }
+
+kvm_status kvm_debug_inject(kvm_ctx *c, int32_t what, int64_t nth) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (what < 0 || what > 2 || (what != 0 && nth < 1))
+        return fail(KVM_ERR_INVALID_ARG, "what must be 0..2 and nth >= 1");
+    c->inject_what = what;
+    c->inject_nth = nth;
+    c->inject_seen = 0;
+    return KVM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal declarations shared by the kernels and the host runtime of libkvm.
+// Layouts and semantics are those of include/kvm.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvm {
+
+constexpr int kBlockTokens = 32;
+constexpr int kMaxHalfDim = 64;       // head_dim <= 128
+constexpr int kMaxRows = 256;         // query rows per KV head (M_q * H/G)
+constexpr int kMaxChunks = 64;        // block chunks per (layer, kv head) in scoring
+
+enum DType { F32 = 0, BF16 = 1 };
+
+struct Omega {
+    double w[kMaxHalfDim];            // theta^(-2i/d), double precision
+};
+
+// One view slot to (re)materialise: K = RoPE(src_k, pos0 + t) into dst_k, and
+// optionally V copied from src_v to dst_v.  Pointers address one whole block
+// ([L][G][32][d]).
+struct SlotDesc {
+    const void *src_k;
+    const void *src_v;
+    void *dst_k;
+    void *dst_v;
+    int64_t pos0;
+};
+
+struct ScoreShape {
+    int L, G, H, d, n_queries;
+    int gqa;            // H / G
+    int rows;           // n_queries * gqa: query rows that read one KV head
+    int64_t index_cap;  // row stride (in blocks) of the index buffer being read
+    int chunk_cap;      // chunk stride of the (max, sum) scratch per (layer, kv head)
+};
+
+// ---- rope_table.cu
+cudaError_t launch_rope_table(float2 *table, int64_t n_pos, int half_d, const Omega &om,
+                              cudaStream_t s);
+
+// ---- meank.cu
+cudaError_t launch_meank(int kv_dtype, int index_dtype, int d, const void *k_pages,
+                         void *raw_out, void *index, int64_t index_cap, int64_t first_block,
+                         int64_t n_blocks, int LG, const float2 *table, int *err,
+                         cudaStream_t s);
+
+// ---- assemble.cu
+// Slots given by (sel_ids, page_ids) against repository / page base pointers.
+cudaError_t launch_assemble_ids(int kv_dtype, int d, const int32_t *sel_ids,
+                                const int32_t *page_ids, int n_sel, int64_t max_blocks,
+                                const void *raw_k_repo, const void *v_repo, void *k_pages,
+                                void *v_pages, int LG, const float2 *table, int64_t max_pos,
+                                int *err, cudaStream_t s);
+// Slots given by explicit descriptors (device array).
+cudaError_t launch_assemble_desc(int kv_dtype, int d, const SlotDesc *desc, int n_desc, int LG,
+                                 const float2 *table, int64_t max_pos, int *err,
+                                 cudaStream_t s);
+
+// ---- score.cu
+// Scratch for one scoring call (device pointers inside the workspace).
+struct ScoreScratch {
+    float *part_m;     // [LG][chunk_cap][rows]  running max (log2 units)
+    float *part_z;     // [LG][chunk_cap][rows]  partition sum at part_m
+    float *row_m;      // [LG][rows]
+    float *row_invz;   // [LG][rows]
+    float *partial;    // [LG][max_blocks]   per-(layer, kv head) relevance
+};
+
+// Pass 1 over blocks [b_begin, b_end) of the index (rows of `index` addressed
+// relative to b_index0), writing chunks [chunk0, chunk0 + n_chunks).
+cudaError_t launch_score_pass1(int q_dtype, int index_dtype, const ScoreShape &sh,
+                               const void *q, const void *index, int64_t b_index0,
+                               int64_t b_begin, int64_t b_end, int chunk0, int n_chunks,
+                               const ScoreScratch &scr, cudaStream_t s);
+cudaError_t launch_score_combine(const ScoreShape &sh, int n_chunks_total,
+                                 const ScoreScratch &scr, cudaStream_t s);
+cudaError_t launch_score_pass2(int q_dtype, int index_dtype, const ScoreShape &sh,
+                               const void *q, const void *index, int64_t b_index0,
+                               int64_t b_begin, int64_t b_end, int n_chunks,
+                               const ScoreScratch &scr, int64_t partial_stride,
+                               cudaStream_t s);
+cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks,
+                                const ScoreScratch &scr, int64_t partial_stride,
+                                float *scores_out, cudaStream_t s);
+// Number of chunks used for a range of n blocks.
+int score_chunks(const ScoreShape &sh, int64_t n_blocks, int max_chunks);
+
+// ---- select.cu
+cudaError_t launch_select(const float *scores, int64_t n_blocks, int sink, int recent,
+                          int view_blocks, int32_t *sel_ids, cudaStream_t s);
+
+}  // namespace kvm

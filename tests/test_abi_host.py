@@ -1,0 +1,85 @@
+"""The C ABI library on the host: it loads, exports every entry point the
+header declares, and rejects bad configurations before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_meank_gb300 import _abi, config_for, configs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvm.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvm_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        from paged_kv_cache_meank_gb300 import build
+        build.build()
+    return _abi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "kvm_build_index" in names and "kvm_step" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_abi.SIGNATURES), (set(names) ^ set(_abi.SIGNATURES))
+
+
+def test_status_strings(lib):
+    for code in _abi.STATUS:
+        assert lib.kvm_status_string(code)
+    assert lib.kvm_status_string(0) == b"ok"
+
+
+def test_workspace_bytes_and_validation(lib):
+    cfg = config_for(configs.TINY)
+    n = lib.kvm_workspace_bytes(ctypes.byref(cfg))
+    assert n > cfg.max_positions * 32 * 8  # at least the cos/sin table
+    for field, bad in [("head_dim", 96), ("block_tokens", 16), ("n_q_heads", 5),
+                       ("view_blocks", 5), ("kv_dtype", 7), ("max_blocks", 0),
+                       ("pool_pages", 1), ("max_queries", 1000)]:
+        c = config_for(configs.TINY)
+        setattr(c, field, bad)
+        assert lib.kvm_workspace_bytes(ctypes.byref(c)) == 0, field
+        h = ctypes.c_void_p()
+        st = lib.kvm_create(ctypes.byref(c), None, 0, None, ctypes.byref(h))
+        assert st == -1 and not h.value, field
+
+
+def test_create_rejects_small_or_misaligned_workspace(lib):
+    cfg = config_for(configs.TINY)
+    n = lib.kvm_workspace_bytes(ctypes.byref(cfg))
+    h = ctypes.c_void_p()
+    # host-side checks fire before any CUDA call; the pointers are never dereferenced
+    assert lib.kvm_create(ctypes.byref(cfg), ctypes.c_void_p(4096), n - 1, None,
+                          ctypes.byref(h)) == -2
+    assert lib.kvm_create(ctypes.byref(cfg), ctypes.c_void_p(4097), n, None,
+                          ctypes.byref(h)) == -1
+    assert b"aligned" in lib.kvm_last_error()
+
+
+def test_calls_reject_null_context(lib):
+    assert lib.kvm_build_index(None, None, 0, 0, None, None, None) == -1
+    assert lib.kvm_score_select(None, None, 1, None, 1, None, None, None, None) == -1
+    assert lib.kvm_assemble_view(None, None, None, 0, None, None, None, None, None) == -1
+    assert lib.kvm_step(None, None, 1, 1, None, None) == -1
+    assert lib.kvm_destroy(None) == 0
+
+
+def test_layout_sizes_follow_the_workloads():
+    # index footprint: 16 layers x 8 KV heads x 128 d x 2 B = 32 KiB per block, the
+    # per-block index size the KVMem scaling table implies (0.25 GiB at 256K tokens)
+    assert configs.W1M.index_entry_bytes == 32 * 1024
+    assert configs.W256K.n_blocks * configs.W1M.index_entry_bytes == 256 * 1024 ** 2
+    # KV bytes per block 2 * L * c * h * d * b (InferScale §4 storage cost) for c = 32
+    w = configs.W256K
+    assert 2 * w.block_bytes == 2 * w.n_layers * 32 * w.n_kv_heads * w.head_dim * 2

@@ -1,0 +1,217 @@
+"""Per-call parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Sizes span several scoring chunks, a ragged tail, both head dims and both
+element types.  Inputs come from the seeded generator (raw K / V, queries,
+directly drawn Mean-K) and from the oracle (K rotated at original positions,
+as a prefill writes it); nothing the oracle consumes comes from the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.kvmem as ora
+from gpu_helpers import (MID, MID64, SMALL, assert_meank_close, assert_scores_close,
+                         assert_storage_close, check_selection, from_np, to_np)
+from recall_ref import prefill_k_pages
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvm():
+    import paged_kv_cache_meank_gb300 as kvm
+    from paged_kv_cache_meank_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    return kvm
+
+
+def _ctx(kvm, wl, **kw):
+    return kvm.Context(kvm.config_for(wl, **kw))
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_build_index(kvm, wl):
+    from paged_kv_cache_meank_gb300 import workload
+    ws = workload.make_workspace(wl, seed=1, with_q=False)
+    raw = to_np(ws.raw_k, wl.kv_dtype)
+    kp = prefill_k_pages(raw, wl.kv_dtype, wl.rope_theta)
+    N = wl.n_blocks
+    ctx = _ctx(kvm, wl, max_blocks=N + 5)
+    kp_d = from_np(kp, wl.kv_dtype)
+    index = torch.full(ctx.index_shape(), 7.0, dtype=ctx.index_dtype, device="cuda")
+    raw_out = torch.zeros(ctx.block_shape(N), dtype=ctx.kv_dtype, device="cuda")
+    # two incremental calls, as blocks complete during prefill
+    cut = N // 3
+    ctx.build_index(kp_d[:cut], 0, cut, index, raw_out[:cut])
+    ctx.build_index(kp_d[cut:], cut, N - cut, index, raw_out[cut:])
+    ctx.sync()
+    ref = ora.meank(kp, wl.kv_dtype, 0, wl.rope_theta)
+    got = to_np(index[:, :, :N], wl.index_dtype)
+    rms = float(np.sqrt(np.mean(ora.as_f64(raw, wl.kv_dtype) ** 2)))
+    assert_meank_close(got, ref, wl.index_dtype, rms, wl.name)
+    # entries past the built range are untouched
+    assert torch.all(index[:, :, N:].float() == 7.0)
+    exact = assert_storage_close(to_np(raw_out, wl.kv_dtype),
+                                 ora.raw_k(kp, wl.kv_dtype, 0, wl.rope_theta), wl.kv_dtype,
+                                 wl.name + " raw K")
+    assert exact > 0.999
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_score_select(kvm, wl):
+    from paged_kv_cache_meank_gb300 import workload
+    ws = workload.make_index_direct(wl, seed=2)
+    N = wl.n_blocks
+    ctx = _ctx(kvm, wl)
+    index = ws.index.to("cuda")
+    q = ws.q.to("cuda")
+    scores = torch.empty(N, dtype=torch.float32, device="cuda")
+    sel = torch.full((wl.view_blocks,), -1, dtype=torch.int32, device="cuda")
+    n_sel = ctx.score_select(q, wl.n_queries, index, N, scores, sel)
+    ctx.sync()
+    assert n_sel == min(N, wl.view_blocks)
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q, wl.q_dtype), wl.q_dtype),
+                            ora.as_f64(to_np(ws.index, wl.index_dtype), wl.index_dtype), N)
+    assert_scores_close(scores.cpu().numpy(), R, wl.name)
+    band = check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks,
+                           wl.view_blocks, wl.name)
+    if band == 0:
+        want = ora.select_blocks(R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+        assert np.array_equal(sel.cpu().numpy(), want)
+    # planted blocks carry the query direction and must all be chosen
+    assert set(ws.planted.tolist()) <= set(sel.cpu().tolist())
+    # run twice: bitwise identical
+    scores2, sel2 = torch.empty_like(scores), torch.empty_like(sel)
+    ctx.score_select(q, wl.n_queries, index, N, scores2, sel2)
+    ctx.sync()
+    assert torch.equal(scores, scores2) and torch.equal(sel, sel2)
+
+
+def test_score_select_fewer_queries_and_ragged(kvm):
+    """n_queries below the configured maximum, N not a multiple of any tile."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=1237, view_blocks=100)
+    ws = workload.make_index_direct(wl, seed=3)
+    ctx = _ctx(kvm, wl, max_queries=wl.n_queries)
+    nq = 7
+    q = ws.q[:, :nq].contiguous().to("cuda")
+    scores = torch.empty(wl.n_blocks, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.score_select(q, nq, ws.index.to("cuda"), wl.n_blocks, scores, sel)
+    ctx.sync()
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q[:, :nq], "bf16"), "bf16"),
+                            ora.as_f64(to_np(ws.index, "bf16"), "bf16"), wl.n_blocks)
+    assert_scores_close(scores.cpu().numpy(), R, "fewer queries")
+    assert abs(float(scores.double().sum()) - nq) < 1e-3 * nq
+    check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+
+
+def test_select_ties_and_small_histories(kvm):
+    """Equal Mean-K everywhere: all scores tie and the lowest ids win; histories
+    of N <= V_b select everything; N = V_b + 1 leaves out exactly one block."""
+    wl = MID64
+    ctx = _ctx(kvm, wl)
+    q = torch.randn(wl.n_layers, wl.n_queries, wl.n_q_heads, wl.head_dim,
+                    device="cuda").to(torch.bfloat16)
+    for N in (1, 5, wl.view_blocks, wl.view_blocks + 1, 200):
+        index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+        index[:, :, :N] = 0.25
+        scores = torch.empty(N, device="cuda")
+        sel = torch.full((wl.view_blocks,), -1, dtype=torch.int32, device="cuda")
+        n_sel = ctx.score_select(q, wl.n_queries, index, N, scores, sel)
+        ctx.sync()
+        got = sel[:n_sel].cpu().numpy()
+        want = ora.select_blocks(np.full(N, 1.0 / N), wl.sink_blocks, wl.recent_blocks,
+                                 wl.view_blocks)
+        assert np.array_equal(got, want), (N, got, want)
+        assert torch.allclose(scores, torch.full_like(scores, wl.n_queries / N), rtol=1e-5)
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_assemble_view(kvm, wl):
+    from paged_kv_cache_meank_gb300 import workload
+    ws = workload.make_workspace(wl, seed=4, with_q=False)
+    N, V = wl.n_blocks, wl.view_blocks
+    ctx = _ctx(kvm, wl)
+    rng = np.random.default_rng(5)
+    ids = np.sort(rng.choice(N, size=V, replace=False)).astype(np.int32)
+    pages = rng.permutation(V + 3)[:V].astype(np.int32)
+    raw_d = ws.raw_k.to("cuda")
+    v_d = ws.v.to("cuda")
+    kp = torch.full(ctx.block_shape(V + 3), 3.0, dtype=ctx.kv_dtype, device="cuda")
+    vp = torch.full(ctx.block_shape(V + 3), 3.0, dtype=ctx.kv_dtype, device="cuda")
+    ctx.assemble_view(torch.from_numpy(ids).cuda(), torch.from_numpy(pages).cuda(), V, raw_d,
+                      v_d, kp, vp)
+    ctx.sync()
+    raw = to_np(ws.raw_k, wl.kv_dtype)
+    ref = ora.view_k(raw[ids], wl.kv_dtype, wl.rope_theta)
+    got = to_np(kp, wl.kv_dtype)[pages]
+    exact = assert_storage_close(got, ref, wl.kv_dtype, wl.name + " view K")
+    assert exact > 0.999
+    assert np.array_equal(to_np(vp, wl.kv_dtype)[pages], to_np(ws.v, wl.kv_dtype)[ids])
+    untouched = sorted(set(range(V + 3)) - set(pages.tolist()))
+    assert torch.all(kp[untouched].float() == 3.0) and torch.all(vp[untouched].float() == 3.0)
+    # without page ids slot j lands in page j; without V only K is written
+    kp2 = torch.zeros(ctx.block_shape(V), dtype=ctx.kv_dtype, device="cuda")
+    ctx.assemble_view(torch.from_numpy(ids).cuda(), None, V, raw_d, None, kp2, None)
+    ctx.sync()
+    assert torch.equal(kp2, kp[torch.from_numpy(pages).long().cuda()])
+
+
+def test_assemble_roundtrip_at_original_positions(kvm):
+    """Every block selected in order lands at its original positions: the view
+    K equals the prefill K (KVMem §4.4; InferScale Theorem 6)."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=40, view_blocks=40)
+    ws = workload.make_workspace(wl, seed=6, with_q=False)
+    raw = to_np(ws.raw_k, "bf16")
+    kp_ref = prefill_k_pages(raw, "bf16", wl.rope_theta)
+    ctx = _ctx(kvm, wl)
+    out = torch.empty(ctx.block_shape(40), dtype=torch.bfloat16, device="cuda")
+    ids = torch.arange(40, dtype=torch.int32, device="cuda")
+    ctx.assemble_view(ids, None, 40, ws.raw_k.cuda(), None, out, None)
+    ctx.sync()
+    assert np.array_equal(to_np(out, "bf16"), kp_ref)
+
+
+def test_device_range_checks(kvm):
+    """Out-of-range ids are skipped and reported by kvm_sync, and the context
+    stays usable."""
+    wl = MID64
+    ctx = _ctx(kvm, wl)
+    raw = torch.zeros(ctx.block_shape(4), dtype=torch.bfloat16, device="cuda")
+    pages = torch.zeros(ctx.block_shape(4), dtype=torch.bfloat16, device="cuda")
+    bad = torch.tensor([0, wl.n_blocks + 10], dtype=torch.int32, device="cuda")
+    ctx.assemble_view(bad, None, 2, raw, None, pages, None)
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.sync()
+    assert ei.value.name == "KVM_ERR_DEVICE"
+    ok = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    ctx.assemble_view(ok, None, 2, raw, None, pages, None)
+    ctx.sync()
+
+
+def test_host_side_errors(kvm):
+    wl = MID64
+    ctx = _ctx(kvm, wl)
+    q = torch.zeros(wl.n_layers, wl.n_queries, wl.n_q_heads, wl.head_dim, dtype=torch.bfloat16,
+                    device="cuda")
+    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+    scores = torch.empty(wl.n_blocks + 10, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.score_select(q, wl.n_queries, index, wl.n_blocks + 1, scores, sel)
+    assert ei.value.name == "KVM_ERR_CAPACITY"
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.score_select(q, wl.n_queries + 1, index, wl.n_blocks, scores, sel)
+    assert ei.value.name == "KVM_ERR_CAPACITY"
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.build_index(q, wl.n_blocks, 1, index)
+    assert ei.value.name == "KVM_ERR_CAPACITY"
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.step(q, wl.n_queries, wl.n_blocks)
+    assert ei.value.name == "KVM_ERR_NOT_BOUND"
+    # still usable
+    ctx.score_select(q, wl.n_queries, index, wl.n_blocks, scores, sel)
+    ctx.sync()

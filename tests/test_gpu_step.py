@@ -1,0 +1,167 @@
+"""The whole recall path through kvm_step against the oracle: Mean-K build,
+scoring and selection, the delta working set over a bounded page pool, and the
+materialised view, over several consecutive steps, with the history's raw K / V
+in device memory or in pinned host memory (packed, pipelined H2D)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.kvmem as ora
+from gpu_helpers import (MID, assert_meank_close, assert_scores_close, assert_storage_close,
+                         check_selection, from_np, to_np)
+from recall_ref import prefill_k_pages
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvm():
+    import paged_kv_cache_meank_gb300 as kvm
+    from paged_kv_cache_meank_gb300 import build
+    build.build()
+    return kvm
+
+
+def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_step,
+               pool_extra=6, batch=7):
+    from paged_kv_cache_meank_gb300 import workload
+    N_max = max(n_blocks_per_step)
+    ws = workload.make_workspace(wl, seed=11, n_blocks=N_max, with_q=False)
+    raw_np = to_np(ws.raw_k, wl.kv_dtype)
+    v_np = to_np(ws.v, wl.kv_dtype)
+    kp = prefill_k_pages(raw_np, wl.kv_dtype, wl.rope_theta)
+    cfg = kvm.config_for(
+        wl, max_blocks=N_max, pool_pages=wl.view_blocks + pool_extra,
+        repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
+        index_location=kvm.KVM_HOST_PINNED if index_host else kvm.KVM_DEVICE,
+        h2d_batch_blocks=batch)
+    cfg.tile_blocks = 64
+    ctx = kvm.Context(cfg)
+    # (a) the GPU builds the index and raw K from the prefill K pages
+    index_d = torch.zeros(ctx.index_shape(), dtype=ctx.index_dtype, device="cuda")
+    raw_d = torch.empty(ctx.block_shape(N_max), dtype=ctx.kv_dtype, device="cuda")
+    ctx.build_index(from_np(kp, wl.kv_dtype), 0, N_max, index_d, raw_d)
+    ctx.sync()
+    v_d = from_np(v_np, wl.kv_dtype)
+    if repo_host:
+        raw_repo = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
+        raw_repo.copy_(raw_d)
+        v_repo = torch.empty(v_d.shape, dtype=v_d.dtype, pin_memory=True)
+        v_repo.copy_(v_d)
+    else:
+        raw_repo, v_repo = raw_d, v_d
+    if index_host:
+        index = torch.empty(index_d.shape, dtype=index_d.dtype, pin_memory=True)
+        index.copy_(index_d)
+    else:
+        index = index_d
+    P = cfg.pool_pages
+    pool_k = torch.zeros(ctx.block_shape(P), dtype=ctx.kv_dtype, device="cuda")
+    pool_v = torch.zeros_like(pool_k)
+    pool_raw = torch.zeros_like(pool_k) if repo_host else None
+    page_table = torch.full((wl.view_blocks,), -1, dtype=torch.int32, device="cuda")
+    scores = torch.empty(N_max, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.bind(index=index, raw_k=raw_repo, v=v_repo, pool_k=pool_k, pool_v=pool_v,
+             pool_raw_k=pool_raw, page_table=page_table, scores=scores, sel_ids=sel)
+
+    # the oracle's own chain: Mean-K and raw K from the same prefill pages
+    index_ref = ora.meank(kp, wl.kv_dtype, 0, wl.rope_theta)
+    raw_ref = ora.raw_k(kp, wl.kv_dtype, 0, wl.rope_theta)
+    rms = float(np.sqrt(np.mean(ora.as_f64(raw_np, wl.kv_dtype) ** 2)))
+    assert_meank_close(to_np(index_d[:, :, :N_max], wl.index_dtype), index_ref,
+                       wl.index_dtype, rms, "index")
+    index_ref_stored = ora.as_f64(ora.round_to(index_ref.astype(np.float32), wl.index_dtype),
+                                  wl.index_dtype)
+    bop, bp = [-1] * P, [-1] * P
+    history = []
+    for step, (q, N) in enumerate(zip(queries, n_blocks_per_step)):
+        st = ctx.step(q.to("cuda"), wl.n_queries, N)
+        ctx.sync()
+        R = ora.block_relevance(ora.as_f64(to_np(q, wl.q_dtype), wl.q_dtype),
+                                index_ref_stored, N)
+        assert_scores_close(scores[:N].cpu().numpy(), R, f"step {step}")
+        g_sel = sel[:min(N, wl.view_blocks)].cpu().numpy()
+        check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks,
+                        f"step {step}")
+        # residency: the oracle's delta rule applied to the GPU's selection
+        page, hit, rope, bop, bp = ora.residency_step(bop, bp, g_sel)
+        assert page_table[:len(g_sel)].cpu().tolist() == page, f"step {step} page table"
+        assert st["hits"] == sum(hit) and st["misses"] == len(hit) - sum(hit)
+        assert st["reroped"] == sum(rope)
+        blk = ctx.block_shape(1)
+        nbytes = int(np.prod(blk)) * (2 if wl.kv_dtype == "bf16" else 4)
+        if repo_host:
+            assert st["h2d_bytes"] == 2 * nbytes * st["misses"]
+        # the view: K at compact positions from the oracle's raw K, V unchanged
+        got_k = to_np(pool_k, wl.kv_dtype)[page]
+        ref_k = ora.view_k(raw_ref[g_sel], wl.kv_dtype, wl.rope_theta)
+        assert_storage_close(got_k, ref_k, wl.kv_dtype, f"step {step} view K")
+        assert np.array_equal(to_np(pool_v, wl.kv_dtype)[page], v_np[g_sel])
+        if repo_host:
+            assert np.array_equal(to_np(pool_raw, wl.kv_dtype)[page], to_np(raw_d, wl.kv_dtype)[g_sel])
+        history.append(st)
+    return history
+
+
+@pytest.mark.parametrize("repo_host", [False, True], ids=["repo-device", "repo-host"])
+def test_step_sequence(kvm, repo_host):
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    g = torch.Generator().manual_seed(21)
+    u = workload.unit_vectors(2, wl.head_dim, g, "cpu")
+    qa = workload.make_queries(wl, g, "cpu", u[0])
+    qb = workload.make_queries(wl, g, "cpu", u[1])
+    qs = [qa, qb, qb, qa]
+    ns = [260, 280, 280, 300]   # the history grows between steps
+    hist = _run_steps(kvm, wl, repo_host, False, qs, ns)
+    assert hist[0]["misses"] == wl.view_blocks and hist[0]["hits"] == 0
+    # same queries, same history: every block is a hit and nothing moves
+    assert hist[2]["misses"] == 0 and hist[2]["reroped"] == 0
+
+
+def test_step_host_index_tiled(kvm):
+    """Index in pinned host memory, scored in 64-block tiles (KVMem §5)."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    g = torch.Generator().manual_seed(22)
+    u = workload.unit_vectors(1, wl.head_dim, g, "cpu")
+    q = workload.make_queries(wl, g, "cpu", u[0])
+    _run_steps(kvm, wl, True, True, [q, q], [300, 300])
+
+
+def test_step_failure_injection(kvm):
+    """A failed copy submission or kernel launch inside kvm_step returns
+    KVM_ERR_INJECTED; the pool is forgotten and the next step rebuilds it."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=200, view_blocks=40)
+    ws = workload.make_workspace(wl, seed=13)
+    ctx = kvm.Context(kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED, h2d_batch_blocks=5))
+    kp = prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta)
+    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+    raw_d = torch.empty(ctx.block_shape(200), dtype=torch.bfloat16, device="cuda")
+    ctx.build_index(from_np(kp, "bf16"), 0, 200, index, raw_d)
+    raw_h = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
+    raw_h.copy_(raw_d)
+    v_h = ws.v.pin_memory()
+    P = ctx.cfg.pool_pages
+    pool_k = torch.zeros(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+    pool_v, pool_r = torch.zeros_like(pool_k), torch.zeros_like(pool_k)
+    pt = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    scores = torch.empty(200, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.bind(index=index, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
+             page_table=pt, scores=scores, sel_ids=sel)
+    q = ws.q.cuda()
+    for what, nth in ((1, 3), (2, 2)):
+        ctx.debug_inject(what, nth)
+        with pytest.raises(kvm.KvmError) as ei:
+            ctx.step(q, wl.n_queries, 200)
+        assert ei.value.name == "KVM_ERR_INJECTED"
+        ctx.sync()
+        st = ctx.step(q, wl.n_queries, 200)   # recovers: the pool starts empty again
+        ctx.sync()
+        assert st["misses"] == wl.view_blocks
+    ref = ora.view_k(to_np(raw_d, "bf16")[sel.cpu().numpy()], "bf16", wl.rope_theta)
+    got = to_np(pool_k, "bf16")[pt.cpu().numpy()]
+    assert_storage_close(got, ref, "bf16", "after recovery")
