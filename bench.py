@@ -1,0 +1,462 @@
+"""Benchmark of the per-step working-set recall path on one GB300.
+
+One step = the whole hot path over one synthetic workspace:
+  (a) Mean-K index build over the history's K pages (raw K written to the
+      repository),
+  (b) Eq. (10) scoring of every block + budgeted top-k selection,
+  (c) assembly of the chronological execution view (gather + re-RoPE + V copy).
+Default workload: the Qwen-27B-class 256K-token single step (64 layers, 8 KV
+heads, 48 query heads, d = 128, bf16, 8192 blocks, 32 queries, 1024-block view),
+everything resident in HBM.
+
+Prints ONE JSON line.  `value` is scored blocks per second over whole steps
+(all ranks); `components` splits the step; `roofline` is the dominant kernel
+against the measured HBM copy bandwidth; `e2e` repeats the step through the
+same C-ABI calls with the inputs in pinned host memory (H2D inside the timed
+region); `cpu_baseline` times the CPU oracle on a bounded slice of the step.
+
+  python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_meank_gb300 import configs, workload  # noqa: E402
+
+METRIC = ("Mean-K scored blocks/s & HBM GB/s; view-assembly tokens/s; per-step recall ms")
+L2_BYTES = 129 * 1024 ** 2
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return ws, rank, local, dist
+    return 1, 0, 0, None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((int(parts[0]), float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if dev.isdigit() and any(r[0] == int(dev) for r in rows):
+            rows = [r for r in rows if r[0] == int(dev)]
+        else:
+            first = rows[0][0]
+            rows = [r for r in rows if r[0] == first]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in rows])),
+                "sm_max_mhz": float(max(r[2] for r in rows)), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# the recall step on the GPU
+# ----------------------------------------------------------------------------
+
+class Step:
+    def __init__(self, wl, seed, device, stream):
+        import paged_kv_cache_meank_gb300 as kvm
+        self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        N, V = wl.n_blocks, wl.view_blocks
+        self.ctx = kvm.Context(kvm.config_for(wl, index_location=kvm.KVM_DEVICE,
+                                              repo_location=kvm.KVM_DEVICE), device=device,
+                               stream=stream)
+        with torch.cuda.stream(stream):
+            ws = workload.make_workspace(wl, seed=seed, device=device)
+            self.q = ws.q
+            self.raw = ws.raw_k          # becomes the repository raw K (a1 output)
+            self.v = ws.v
+            # K pages as a prefill leaves them: every block rotated at its original
+            # positions (identity selection places block b at positions 32b..)
+            self.k_pages = torch.empty_like(self.raw)
+            ident = torch.arange(N, dtype=torch.int32, device=device)
+            self.ctx.assemble_view(ident, None, N, self.raw, None, self.k_pages, None,
+                                   stream=stream)
+            self.index = torch.empty(self.ctx.index_shape(), dtype=self.ctx.index_dtype,
+                                     device=device)
+            self.scores = torch.empty(N, dtype=torch.float32, device=device)
+            self.sel = torch.empty(V, dtype=torch.int32, device=device)
+            self.pool_k = torch.empty(self.ctx.block_shape(V), dtype=self.ctx.kv_dtype,
+                                      device=device)
+            self.pool_v = torch.empty_like(self.pool_k)
+        self.ctx.sync(stream)
+        self.planted = ws.planted
+        self.launches_per_step = 1 + 5 + 1
+
+    def run(self, ev=None, q=None, k_pages=None, v=None):
+        """One step; ev = list of 4 events to bracket build / score / assemble."""
+        wl, s = self.wl, self.stream
+        q = self.q if q is None else q
+        k_pages = self.k_pages if k_pages is None else k_pages
+        v = self.v if v is None else v
+        if ev:
+            ev[0].record(s)
+        self.ctx.build_index(k_pages, 0, wl.n_blocks, self.index, self.raw, stream=s)
+        if ev:
+            ev[1].record(s)
+        self.ctx.score_select(q, wl.n_queries, self.index, wl.n_blocks, self.scores, self.sel,
+                              stream=s)
+        if ev:
+            ev[2].record(s)
+        self.ctx.assemble_view(self.sel, None, wl.view_blocks, self.raw, v, self.pool_k,
+                               self.pool_v, stream=s)
+        if ev:
+            ev[3].record(s)
+
+
+def algorithmic_bytes(wl):
+    """Per-step algorithmic HBM bytes of each kernel (reads + writes that the
+    definition needs once)."""
+    LG = wl.n_layers * wl.n_kv_heads
+    e = wl.elem_bytes("kv_dtype")
+    ei = wl.elem_bytes("index_dtype")
+    d = wl.head_dim
+    per_lgb_build = 32 * d * e + 32 * d * e + d * ei   # K in, raw K out, Mean-K out
+    build = LG * wl.n_blocks * per_lgb_build
+    score = LG * wl.n_blocks * d * ei                   # the index, read once
+    assemble = wl.view_tokens * 4 * LG * d * e          # raw K + V in, K + V out
+    return {"build": build, "score_select": score, "assemble": assemble}
+
+
+def bench_ours(args, wl, world, rank, local, dist):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    step = Step(wl, args.seed + rank, dev, stream)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = Clocks()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        step.run(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / K
+    parts = {
+        "build": float(np.mean([e[0].elapsed_time(e[1]) for e in evs])),
+        "score_select": float(np.mean([e[1].elapsed_time(e[2]) for e in evs])),
+        "assemble": float(np.mean([e[2].elapsed_time(e[3]) for e in evs])),
+    }
+    ab = algorithmic_bytes(wl)
+    peak, peak_kind = _peaks()
+    kern = {k: {"ms": parts[k], "gbs": ab[k] / (parts[k] * 1e-3) / 1e9,
+                "frac_hbm": ab[k] / (parts[k] * 1e-3) / 1e9 / peak} for k in parts}
+    dom = max(parts, key=parts.get)
+    traffic = _traffic_from_profile(dom)
+    out = {
+        "metric": METRIC,
+        "value": world * wl.n_blocks / (ms * 1e-3),
+        "unit": "scored blocks/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1/128) raw K/V, 2% planted blocks, RoPE-free queries)",
+        "config": {"workload": wl.name, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
+                   "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "history_blocks": wl.n_blocks,
+                   "history_tokens": wl.n_tokens, "queries": wl.n_queries,
+                   "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
+                   "recent_blocks": wl.recent_blocks, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (K pages %.1f GB), no flush" %
+                         (wl.n_blocks * wl.block_bytes / 1e9)},
+        "components": {
+            "recall_ms": parts["score_select"] + parts["assemble"],
+            "build_ms": parts["build"], "score_select_ms": parts["score_select"],
+            "assemble_ms": parts["assemble"],
+            "index_hbm_gbs": kern["score_select"]["gbs"],
+            "assembly_tokens_per_s": wl.view_tokens / (parts["assemble"] * 1e-3),
+            "kernels": kern,
+        },
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"],
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": kern[dom]["frac_hbm"], "traffic": traffic,
+                     "algorithmic_bytes": ab[dom]},
+        "gpu_launches": step.launches_per_step * K,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        out["e2e"] = bench_e2e(args, step, dev, stream, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, step, args.cpu_layers)
+    return out
+
+
+def _traffic_from_profile(kernel):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    when one matches the current kernel build (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        import hashlib
+        with open(p) as f:
+            d = json.load(f).get(kernel)
+        if not d:
+            return None
+        with open(os.path.join(ROOT, d["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != d["sha256_16"]:
+                return None   # the kernel changed since the counters were taken
+        return d["bytes"]
+    except Exception:
+        return None
+
+
+def bench_e2e(args, step, dev, stream, world, dist):
+    """The same step through the same C-ABI calls with the step's inputs (K pages,
+    V, queries) in pinned host memory: H2D of the inputs and D2H of the result
+    (selected ids and block scores) inside the timed region."""
+    wl = step.wl
+    k_h = torch.empty(step.k_pages.shape, dtype=step.k_pages.dtype, pin_memory=True)
+    v_h = torch.empty(step.v.shape, dtype=step.v.dtype, pin_memory=True)
+    q_h = torch.empty(step.q.shape, dtype=step.q.dtype, pin_memory=True)
+    k_h.copy_(step.k_pages)
+    v_h.copy_(step.v)
+    q_h.copy_(step.q)
+    sel_h = torch.empty(step.sel.shape, dtype=step.sel.dtype, pin_memory=True)
+    sc_h = torch.empty(step.scores.shape, dtype=step.scores.dtype, pin_memory=True)
+    k_d, v_d, q_d = torch.empty_like(step.k_pages), torch.empty_like(step.v), torch.empty_like(step.q)
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        with torch.cuda.stream(stream):
+            k_d.copy_(k_h, non_blocking=True)
+            v_d.copy_(v_h, non_blocking=True)
+            q_d.copy_(q_h, non_blocking=True)
+            step.run(q=q_d, k_pages=k_d, v=v_d)
+            sel_h.copy_(step.sel, non_blocking=True)
+            sc_h.copy_(step.scores, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = k_h.numel() * k_h.element_size() + v_h.numel() * v_h.element_size() + \
+        q_h.numel() * q_h.element_size()
+    d2h = sel_h.numel() * 4 + sc_h.numel() * 4
+    del k_d, v_d, q_d
+    return {"value": world * wl.n_blocks / (ms * 1e-3), "unit": "scored blocks/s",
+            "ms_per_step": ms, "steps": steps, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "h2d_gbs": h2d / (ms * 1e-3) / 1e9}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle, timed on a bounded slice of the step
+# ----------------------------------------------------------------------------
+
+def _oracle_step_slice(wl, k_pages, v, q, layers):
+    """The oracle's recall step restricted to the first `layers` layers of every
+    block (all blocks scored, the full view assembled for those layers)."""
+    import oracle.kvmem as ora
+    kd = wl.kv_dtype
+    index = ora.meank(k_pages, kd, 0, wl.rope_theta)
+    rk = ora.raw_k(k_pages, kd, 0, wl.rope_theta)
+    idx_stored = ora.as_f64(ora.round_to(index.astype(np.float32), wl.index_dtype),
+                            wl.index_dtype)
+    R = ora.block_relevance(ora.as_f64(q, wl.q_dtype), idx_stored, wl.n_blocks)
+    sel = ora.select_blocks(R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+    vk = ora.view_k(rk[sel], kd, wl.rope_theta)
+    vv = v[sel]
+    return sel, vk, vv
+
+
+def _np_bits(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def cpu_sample(wl, k_pages, v, q, layers):
+    kp = _np_bits(k_pages[:, :layers])
+    vv = _np_bits(v[:, :layers])
+    qq = _np_bits(q[:layers])
+    t0 = time.perf_counter()
+    _oracle_step_slice(wl.with_(n_layers=layers), kp, vv, qq, layers)
+    dt = time.perf_counter() - t0
+    full = dt * wl.n_layers / layers
+    return dt, full
+
+
+def cpu_baseline(wl, step, layers):
+    dt, full = cpu_sample(wl, step.k_pages, step.v, step.q, layers)
+    return {"value": wl.n_blocks / full, "unit": "scored blocks/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one step restricted to {layers} of {wl.n_layers} layers "
+                      f"(all {wl.n_blocks} blocks, {wl.view_blocks}-block view); "
+                      f"{dt:.1f} s measured, scaled by {wl.n_layers}/{layers} layers",
+            "sample_seconds": dt}
+
+
+def bench_reference(args, wl, world, rank):
+    """The CPU oracle as the reference arm: each step is the oracle's recall step
+    on a bounded slice (args.cpu_layers layers) of the same workload, scaled to
+    the whole step."""
+    if rank != 0:
+        return None
+    gen_dev = "cpu"
+    ws = workload.make_workspace(wl.with_(n_layers=args.cpu_layers), seed=args.seed,
+                                 device=gen_dev)
+    import oracle.kvmem as ora
+    raw = _np_bits(ws.raw_k)
+    pos = ora.block_positions(np.arange(wl.n_blocks))
+    kp32 = np.empty(raw.shape, dtype=np.float32)
+    r32 = ora.as_f32(raw, wl.kv_dtype)
+    for i in range(wl.n_blocks):
+        c, s = ora.cos_sin_f32(pos[i], wl.head_dim, wl.rope_theta)
+        kp32[i] = ora.rope_f32(r32[i], c, s)
+    kp = ora.round_to(kp32, wl.kv_dtype)
+    vv, qq = _np_bits(ws.v), _np_bits(ws.q)
+    sub = wl.with_(n_layers=args.cpu_layers)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        _oracle_step_slice(sub, kp, vv, qq, args.cpu_layers)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step_slice(sub, kp, vv, qq, args.cpu_layers)
+        times.append(time.perf_counter() - t0)
+    dt = float(np.mean(times))
+    full = dt * wl.n_layers / args.cpu_layers
+    val = wl.n_blocks / full
+    return {
+        "metric": METRIC, "value": val, "unit": "scored blocks/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl.name, "parallelism": "rank0 only"},
+        "cpu_baseline": {"value": val, "unit": "scored blocks/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"each step restricted to {args.cpu_layers} of "
+                                   f"{wl.n_layers} layers, scaled to the whole step"},
+        "e2e": {"value": val, "unit": "scored blocks/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=configs.W256K.name, choices=sorted(configs.ALL))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="override the history length (small cases for profiling)")
+    args = ap.parse_args()
+    wl = configs.ALL[args.workload]
+    if args.blocks:
+        wl = wl.with_(n_blocks=args.blocks, view_blocks=min(wl.view_blocks, args.blocks // 2),
+                      name=f"{wl.name}@{args.blocks}blocks")
+    world, rank, local, dist = _dist()
+    if args.impl == "reference":
+        out = bench_reference(args, wl, world, rank)
+    else:
+        from paged_kv_cache_meank_gb300 import build
+        if rank == 0:
+            build.build()
+        if dist:
+            dist.barrier()
+        out = bench_ours(args, wl, world, rank, local, dist)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

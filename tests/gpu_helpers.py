@@ -73,16 +73,23 @@ def assert_storage_close(gpu: np.ndarray, ref: np.ndarray, dtype: str, what: str
     return float((gpu == ref).mean())
 
 
-def assert_meank_close(gpu: np.ndarray, ref64: np.ndarray, dtype: str, k_rms: float, what: str):
-    """Mean-K: bf16 within 1 ulp of the float64 mean; float32 within
-    1e-6 * rms(K) absolute."""
+def assert_meank_close(gpu: np.ndarray, ref64: np.ndarray, dtype: str, k_rms: float, what: str,
+                       k_max: float | None = None):
+    """Mean-K against the float64 mean.
+
+    The kernel un-rotates in float32 (one rounding per product and sum) and
+    sums 32 float32 terms before one rounding to the index dtype, so its error
+    before that rounding is at most (2 + 31) * 2^-24 * max|K| in absolute terms.
+    bf16: within 1 ulp of the reference plus that bound (the bound only matters
+    for means that nearly cancel); float32: within 1e-6 * rms(K) absolute."""
     if dtype == "bf16":
         g = ora.bf16_to_f32(gpu).astype(np.float64)
         mag = np.abs(ref64)
         ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.maximum(mag, 1e-300))) - 7), 0.0)
+        acc = 33 * 2.0 ** -24 * (k_max if k_max is not None else 8 * k_rms)
         err = np.abs(g - ref64)
-        bad = err > ulp * (1 + 1e-9) + 1e-38
-        assert not bad.any(), f"{what}: {int(bad.sum())} Mean-K entries beyond 1 bf16 ulp"
+        bad = err > ulp * (1 + 1e-9) + acc
+        assert not bad.any(), f"{what}: {int(bad.sum())} Mean-K entries beyond 1 bf16 ulp + {acc:.2g}"
     else:
         err = np.abs(gpu.astype(np.float64) - ref64)
         assert err.max() <= 1e-6 * k_rms, f"{what}: Mean-K error {err.max()}"

@@ -69,8 +69,9 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
     index_ref = ora.meank(kp, wl.kv_dtype, 0, wl.rope_theta)
     raw_ref = ora.raw_k(kp, wl.kv_dtype, 0, wl.rope_theta)
     rms = float(np.sqrt(np.mean(ora.as_f64(raw_np, wl.kv_dtype) ** 2)))
+    kmax = float(np.abs(ora.as_f64(kp, wl.kv_dtype)).max()) * 2 ** 0.5
     assert_meank_close(to_np(index_d[:, :, :N_max], wl.index_dtype), index_ref,
-                       wl.index_dtype, rms, "index")
+                       wl.index_dtype, rms, "index", kmax)
     index_ref_stored = ora.as_f64(ora.round_to(index_ref.astype(np.float32), wl.index_dtype),
                                   wl.index_dtype)
     bop, bp = [-1] * P, [-1] * P
@@ -154,6 +155,7 @@ def test_step_failure_injection(kvm):
              page_table=pt, scores=scores, sel_ids=sel)
     q = ws.q.cuda()
     for what, nth in ((1, 3), (2, 2)):
+        ctx.reset_pool()          # every selected block is a miss again
         ctx.debug_inject(what, nth)
         with pytest.raises(kvm.KvmError) as ei:
             ctx.step(q, wl.n_queries, 200)
