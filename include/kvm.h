@@ -203,6 +203,39 @@ typedef struct {
 kvm_status kvm_step(kvm_ctx *ctx, const void *q, int32_t n_queries, int64_t n_blocks,
                     kvm_step_stats *stats, kvm_stream stream);
 
+/*
+ * kvm_score_select without any device allocation: the paper has no
+ * counterpart; this is a deployment convenience.
+ *
+ * Computes exactly what kvm_score_select computes for a device-resident index
+ * (same kernels, same results), but needs no context and no workspace: its
+ * scratch is a fixed 32 MiB array in the library's own device memory.  It is
+ * meant for callers that cannot allocate device memory -- for example a plugin
+ * inside an inference engine whose memory planner already owns the whole
+ * device, or a latency-critical caller that cannot afford cudaMalloc/cudaFree,
+ * which may synchronise the device.  The call allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * cfg      host; the shape fields, dtypes, sink/recent/view budget and
+ *          max_blocks (the index row stride) are used; index_location must be
+ *          KVM_DEVICE.  The other arguments are those of kvm_score_select.
+ * Limit:   the scratch needs about 4 * L * G * n_blocks bytes (plus a little
+ *          per query row); calls needing more than 32 MiB return
+ *          KVM_ERR_CAPACITY with a message, before any work is enqueued.
+ * Set-up:  the first call on each device looks up the array's device address
+ *          (cudaGetSymbolAddress) with that device current; make that first
+ *          call before any stream capture.
+ * Sharing: every call on a device uses the same array.  Calls that overlap on
+ *          the GPU (unordered streams or threads) race on it; order them.
+ *          Leftover contents of earlier calls are never read, so nothing has
+ *          to be cleared between calls.
+ * The array stays allocated on every GPU that loaded the library until the
+ * process exits.
+ */
+kvm_status kvm_score_select_static(const kvm_config *cfg, const void *q, int32_t n_queries,
+                                   const void *index, int64_t n_blocks, float *scores_out,
+                                   int32_t *sel_ids_out, int32_t *n_sel_out, kvm_stream stream);
+
 /* Wait for all work of the context (its internal streams and `stream`) and
  * report a raised device error flag (KVM_ERR_DEVICE), clearing it. */
 kvm_status kvm_sync(kvm_ctx *ctx, kvm_stream stream);

@@ -67,6 +67,21 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream
 
 
+def score_select_static(cfg: KvmConfig, q, n_queries: int, index, n_blocks: int, scores_out,
+                        sel_ids_out, stream=None) -> int:
+    """kvm_score_select_static: scoring + selection for callers that cannot
+    allocate device memory.  Needs no Context and no workspace; the library's
+    fixed 32 MiB device scratch is used instead (calls must not overlap on the
+    GPU).  Returns the number of selected blocks."""
+    lib = load()
+    n_sel = ctypes.c_int32()
+    check(lib.kvm_score_select_static(ctypes.byref(cfg), _ptr(q), n_queries, _ptr(index),
+                                      n_blocks, _ptr(scores_out), _ptr(sel_ids_out),
+                                      ctypes.byref(n_sel), _stream(stream)),
+          "kvm_score_select_static")
+    return n_sel.value
+
+
 class Context:
     """A kvm_ctx plus its caller-owned device workspace (a torch uint8 tensor)."""
 

@@ -69,6 +69,10 @@ SIGNATURES = {
     "kvm_reset_pool": (ctypes.c_int, [ctypes.c_void_p]),
     "kvm_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                 ctypes.c_int64, ctypes.POINTER(KvmStepStats), ctypes.c_void_p]),
+    "kvm_score_select_static": (ctypes.c_int, [ctypes.POINTER(KvmConfig), ctypes.c_void_p,
+                                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                               ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     "kvm_sync": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "kvm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvm_last_error": (ctypes.c_char_p, []),

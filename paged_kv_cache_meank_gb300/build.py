@@ -27,6 +27,7 @@ SOURCES = [
     "score_dispatch.cu",
     "select.cu",
     "assemble.cu",
+    "score_static.cu",
     "kvm_api.cpp",
 ]
 

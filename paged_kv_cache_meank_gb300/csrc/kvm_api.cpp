@@ -115,6 +115,8 @@ Layout layout_of(const kvm_config *c) {
 
 }  // namespace
 
+void kvm::set_last_error(const std::string &msg) { g_last_error = msg; }
+
 struct kvm_ctx {
     kvm_config cfg{};
     Layout lo{};

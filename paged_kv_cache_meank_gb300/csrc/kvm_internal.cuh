@@ -6,7 +6,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace kvm {
+
+// Sets the message kvm_last_error() returns on the calling thread.
+void set_last_error(const std::string &msg);
 
 constexpr int kBlockTokens = 32;
 constexpr int kMaxHalfDim = 64;       // head_dim <= 128

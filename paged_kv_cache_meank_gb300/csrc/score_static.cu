@@ -1,0 +1,148 @@
+// kvm_score_select_static: block scoring + selection with no device allocation
+// by anyone.
+//
+// kvm_score_select needs a context, and a context needs a caller-allocated
+// device workspace.  Some callers cannot allocate device memory at all: a
+// plugin inside an inference engine whose memory planner has already handed
+// the whole device to its own pools (a cudaMalloc there fails or fragments the
+// engine's pool), or a latency-critical caller that cannot pay for
+// cudaMalloc / cudaFree, which may synchronise the device.  For them this
+// entry point keeps its scratch in a fixed file-scope device array and takes
+// only inputs and outputs.
+//
+// The array is SCRATCH_BYTES (32 MiB) per device.  Every GPU on which the
+// library is loaded holds it until the process exits.  It is shared by every
+// call: two calls that overlap on the GPU (different streams, or different
+// host threads without ordering) race on it and produce garbage.  Every byte a
+// call reads from it is written earlier in the same call, so leftover contents
+// of a previous call are harmless and nothing needs clearing.
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "kvm.h"
+#include "kvm_internal.cuh"
+
+namespace {
+
+constexpr size_t SCRATCH_BYTES = size_t(32) << 20;
+
+static __device__ __align__(256) unsigned char g_scratch[SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_ptr[kMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The device address of g_scratch on the current device.  In host code the
+// name g_scratch is only a host-side stand-in, so the address is looked up
+// once per device with that device current and then reused.
+kvm_status scratch_for_current_device(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        kvm::set_last_error(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+        return KVM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        kvm::set_last_error("device ordinal beyond the supported range");
+        return KVM_ERR_INVALID_ARG;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            kvm::set_last_error(std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+            return KVM_ERR_CUDA;
+        }
+        g_ptr[dev] = p;
+    }
+    *out = g_ptr[dev];
+    return KVM_OK;
+}
+
+}  // namespace
+
+extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void *q,
+                                              int32_t n_queries, const void *index,
+                                              int64_t n_blocks, float *scores_out,
+                                              int32_t *sel_ids_out, int32_t *n_sel_out,
+                                              kvm_stream stream) {
+    auto bad = [](kvm_status s, const char *m) { kvm::set_last_error(m); return s; };
+    if (!cfg) return bad(KVM_ERR_INVALID_ARG, "config is NULL");
+    if (!q || !index || !scores_out || !sel_ids_out)
+        return bad(KVM_ERR_INVALID_ARG, "q, index, scores_out and sel_ids_out are required");
+    if (cfg->n_layers < 1 || cfg->n_kv_heads < 1 || cfg->n_q_heads < 1 ||
+        cfg->n_q_heads % cfg->n_kv_heads != 0)
+        return bad(KVM_ERR_INVALID_ARG, "layers / heads invalid");
+    if (cfg->head_dim != 64 && cfg->head_dim != 128)
+        return bad(KVM_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+    for (int dt : {cfg->index_dtype, cfg->q_dtype})
+        if (dt != KVM_F32 && dt != KVM_BF16) return bad(KVM_ERR_INVALID_ARG, "dtype invalid");
+    if (cfg->index_location != KVM_DEVICE)
+        return bad(KVM_ERR_INVALID_ARG, "the index must be in device memory");
+    if (cfg->sink_blocks < 0 || cfg->recent_blocks < 0 ||
+        cfg->view_blocks < cfg->sink_blocks + cfg->recent_blocks + 1)
+        return bad(KVM_ERR_INVALID_ARG, "view_blocks must be >= sink + recent + 1");
+    if (n_queries < 1 || n_blocks < 1) return bad(KVM_ERR_INVALID_ARG, "empty input");
+    if (n_blocks > cfg->max_blocks)
+        return bad(KVM_ERR_CAPACITY, "n_blocks beyond max_blocks (the index row stride)");
+    const int gqa = cfg->n_q_heads / cfg->n_kv_heads;
+    if ((int64_t)n_queries * gqa > kvm::kMaxRows)
+        return bad(KVM_ERR_CAPACITY, "n_queries * (H/G) must be <= 256");
+
+    kvm::ScoreShape sh{};
+    sh.L = cfg->n_layers;
+    sh.G = cfg->n_kv_heads;
+    sh.H = cfg->n_q_heads;
+    sh.d = cfg->head_dim;
+    sh.n_queries = n_queries;
+    sh.gqa = gqa;
+    sh.rows = n_queries * gqa;
+    sh.index_cap = cfg->max_blocks;
+    const int nch = kvm::score_chunks(sh, n_blocks, kvm::kMaxChunks);
+    sh.chunk_cap = nch;
+
+    const size_t LG = (size_t)sh.L * sh.G;
+    const size_t part = up256(LG * nch * sh.rows * sizeof(float));
+    const size_t rowb = up256(LG * sh.rows * sizeof(float));
+    const size_t partial = up256(LG * (size_t)n_blocks * sizeof(float));
+    const size_t need = 2 * part + 2 * rowb + partial;
+    if (need > SCRATCH_BYTES) {
+        char msg[200];
+        snprintf(msg, sizeof msg,
+                 "needs %zu bytes of scratch, more than the fixed %zu: layers * kv_heads * "
+                 "n_blocks must shrink (use kvm_score_select with a workspace)",
+                 need, SCRATCH_BYTES);
+        return bad(KVM_ERR_CAPACITY, msg);
+    }
+
+    void *base = nullptr;
+    kvm_status st = scratch_for_current_device(&base);
+    if (st != KVM_OK) return st;
+    char *b = static_cast<char *>(base);
+    kvm::ScoreScratch scr{};
+    scr.part_m = reinterpret_cast<float *>(b);
+    scr.part_z = reinterpret_cast<float *>(b + part);
+    scr.row_m = reinterpret_cast<float *>(b + 2 * part);
+    scr.row_invz = reinterpret_cast<float *>(b + 2 * part + rowb);
+    scr.partial = reinterpret_cast<float *>(b + 2 * part + 2 * rowb);
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if ((e = kvm::launch_score_pass1(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, 0, n_blocks,
+                                     0, nch, scr, s)) != cudaSuccess ||
+        (e = kvm::launch_score_combine(sh, nch, scr, s)) != cudaSuccess ||
+        (e = kvm::launch_score_pass2(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, 0,
+                                     n_blocks, nch, scr, n_blocks, s)) != cudaSuccess ||
+        (e = kvm::launch_score_reduce(sh, n_blocks, scr, n_blocks, scores_out, s)) != cudaSuccess ||
+        (e = kvm::launch_select(scores_out, n_blocks, cfg->sink_blocks, cfg->recent_blocks,
+                                cfg->view_blocks, sel_ids_out, s)) != cudaSuccess) {
+        kvm::set_last_error(std::string("launch: ") + cudaGetErrorString(e));
+        return KVM_ERR_CUDA;
+    }
+    if (n_sel_out) *n_sel_out = (int32_t)(n_blocks < cfg->view_blocks ? n_blocks : cfg->view_blocks);
+    return KVM_OK;
+}
