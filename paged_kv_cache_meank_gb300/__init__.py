@@ -34,7 +34,7 @@ _TDT = {KVM_F32: torch.float32, KVM_BF16: torch.bfloat16}
 def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: int | None = None,
                pool_pages: int | None = None, index_location: int | None = None,
                repo_location: int | None = None, h2d_batch_blocks: int = 64,
-               max_queries: int | None = None) -> KvmConfig:
+               max_queries: int | None = None, score_variant: int = 0) -> KvmConfig:
     """A kvm_config for a workload shape."""
     mb = max_blocks if max_blocks is not None else wl.n_blocks + wl.steps * wl.append_blocks
     mp = max_positions if max_positions is not None else max(mb, wl.view_blocks) * BLOCK_TOKENS
@@ -50,7 +50,8 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         view_blocks=wl.view_blocks, max_queries=max_queries or wl.n_queries, max_blocks=mb,
         max_positions=mp, tile_blocks=wl.tile_blocks,
         pool_pages=pool_pages if pool_pages is not None else wl.view_blocks + wl.append_blocks,
-        index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks)
+        index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
+        score_variant=score_variant)
 
 
 def _ptr(t) -> int | None:

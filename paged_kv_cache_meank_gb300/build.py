@@ -24,6 +24,7 @@ SOURCES = [
     "rope_table.cu",
     "meank.cu",
     "score.cu",
+    "score_tc.cu",
     "score_dispatch.cu",
     "select.cu",
     "assemble.cu",

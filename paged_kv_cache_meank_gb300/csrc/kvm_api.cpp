@@ -82,6 +82,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
         return bad("tile_blocks must be >= 1 for a host-resident index");
     if (c->pool_pages < c->view_blocks) return bad("pool_pages must be >= view_blocks");
     if (c->h2d_batch_blocks < 1) return bad("h2d_batch_blocks must be >= 1");
+    if (c->score_variant != 0 && c->score_variant != 1) return bad("score_variant must be 0 or 1");
     return true;
 }
 
@@ -166,6 +167,7 @@ kvm::ScoreShape shape_of(const kvm_ctx *c, int n_queries, int64_t index_cap) {
     sh.rows = n_queries * sh.gqa;
     sh.index_cap = index_cap;
     sh.chunk_cap = c->lo.chunk_cap;
+    sh.variant = c->cfg.score_variant;
     return sh;
 }
 
@@ -216,6 +218,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->stage[1] = c->ws + lo.stage1;
     c->desc_dev = reinterpret_cast<kvm::SlotDesc *>(c->ws + lo.desc);
     c->err_dev = reinterpret_cast<int *>(c->ws + lo.err);
+    c->scr.err = c->err_dev;
     c->block_of_page.assign(cfg->pool_pages, -1);
     c->baked_pos.assign(cfg->pool_pages, -1);
     c->page_of_block.assign((size_t)cfg->max_blocks, -1);
@@ -612,6 +615,7 @@ kvm_status kvm_sync(kvm_ctx *c, kvm_stream stream) {
     KVM_CUDA(cudaMemcpy(&flag, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost));
     if (flag) {
         KVM_CUDA(cudaMemset(c->err_dev, 0, sizeof(int)));
+        if (flag & 4) return fail(KVM_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", flag);
         return fail(KVM_ERR_DEVICE, "device range check raised flag 0x%x", flag);
     }
     return KVM_OK;

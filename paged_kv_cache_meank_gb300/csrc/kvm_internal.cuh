@@ -41,6 +41,7 @@ struct ScoreShape {
     int rows;           // n_queries * gqa: query rows that read one KV head
     int64_t index_cap;  // row stride (in blocks) of the index buffer being read
     int chunk_cap;      // chunk stride of the (max, sum) scratch per (layer, kv head)
+    int variant;        // 0: tensor cores where supported, 1: CUDA cores
 };
 
 // ---- rope_table.cu
@@ -73,6 +74,7 @@ struct ScoreScratch {
     float *row_m;      // [LG][rows]
     float *row_invz;   // [LG][rows]
     float *partial;    // [LG][max_blocks]   per-(layer, kv head) relevance
+    int *err;          // device error flag (bit 4: a bounded wait gave up)
 };
 
 // Pass 1 over blocks [b_begin, b_end) of the index (rows of `index` addressed

@@ -23,4 +23,14 @@ cudaError_t launch_score_pass2_simt(int q_dtype, int index_dtype, const ScoreSha
                                     const ScoreScratch &scr, int64_t partial_stride,
                                     cudaStream_t s);
 
+bool score_tc_supported(int q_dtype, int index_dtype, const ScoreShape &sh);
+cudaError_t launch_score_pass1_tc(const ScoreShape &sh, const void *q, const void *index,
+                                  int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
+                                  int n_chunks, const ScoreScratch &scr, int *err,
+                                  cudaStream_t s);
+cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const void *index,
+                                  int64_t b_index0, int64_t b_begin, int64_t b_end, int n_chunks,
+                                  const ScoreScratch &scr, int64_t partial_stride, int *err,
+                                  cudaStream_t s);
+
 }  // namespace kvm

@@ -104,12 +104,13 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     sh.index_cap = cfg->max_blocks;
     const int nch = kvm::score_chunks(sh, n_blocks, kvm::kMaxChunks);
     sh.chunk_cap = nch;
+    sh.variant = cfg->score_variant;
 
     const size_t LG = (size_t)sh.L * sh.G;
     const size_t part = up256(LG * nch * sh.rows * sizeof(float));
     const size_t rowb = up256(LG * sh.rows * sizeof(float));
     const size_t partial = up256(LG * (size_t)n_blocks * sizeof(float));
-    const size_t need = 2 * part + 2 * rowb + partial;
+    const size_t need = 256 + 2 * part + 2 * rowb + partial;
     if (need > SCRATCH_BYTES) {
         char msg[200];
         snprintf(msg, sizeof msg,
@@ -122,13 +123,14 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     void *base = nullptr;
     kvm_status st = scratch_for_current_device(&base);
     if (st != KVM_OK) return st;
-    char *b = static_cast<char *>(base);
+    char *b = static_cast<char *>(base) + 256;   // the first 256 bytes hold an error word
     kvm::ScoreScratch scr{};
     scr.part_m = reinterpret_cast<float *>(b);
     scr.part_z = reinterpret_cast<float *>(b + part);
     scr.row_m = reinterpret_cast<float *>(b + 2 * part);
     scr.row_invz = reinterpret_cast<float *>(b + 2 * part + rowb);
     scr.partial = reinterpret_cast<float *>(b + 2 * part + 2 * rowb);
+    scr.err = static_cast<int *>(base);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

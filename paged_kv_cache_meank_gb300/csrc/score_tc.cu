@@ -1,0 +1,344 @@
+// Tensor-core (tcgen05) variant of the two scoring passes of Eq. (10), KVMem
+// (Virtualizing Million-Token Agent Workspaces on a Consumer GPU) §4.3, for
+// bf16 queries and a bf16 Mean-K index.
+//
+// For one (layer l, kv head g) the scaled scores are a dense contraction
+// S = Q_g . Kbar^T with Q_g the rows x d query rows that read kv head g and
+// Kbar a tile of 128 Mean-K vectors.  Products of bf16 values are exact in
+// fp32 and the tensor cores accumulate in fp32, so only the summation order
+// differs from the CUDA-core variant.
+//
+// CTA = 6 warps, one SM (the shared-memory ring and the 512 TMEM columns):
+//   warp 0       TMA producer: 128-block index tiles into a 4-stage ring of
+//                128-byte-swizzled shared memory (one copy per 64-element K atom)
+//   warp 1       MMA issuer: one thread issues tcgen05.mma into one of two TMEM
+//                accumulators and commits to mbarriers
+//   warps 2..5   epilogue: tcgen05.ld of the accumulator, one TMEM lane each
+// Pass 1 computes D[query row][block] (M = 128 query rows per tile, N = 128
+// blocks): each epilogue thread owns one query row and keeps its running max
+// and rescaled partition sum in registers -- no cross-thread reduction.
+// Pass 2 computes D[block][query row] (M = 128 blocks, N = rows rounded to 16):
+// each thread owns one block and sums 2^(s*c - M - log2 Z) over its query rows
+// in registers.  Every mbarrier wait is bounded; on timeout the kernel raises
+// the device error flag (bit 4) and winds down, freeing its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "kvm_internal.cuh"
+#include "score_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace kvm {
+
+namespace {
+
+constexpr int TB = 128;             // index blocks per tile
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kQRows = 256;         // query rows padded to two M = 128 tiles
+
+template <int D>
+struct Lay {
+    static constexpr int KA = D / 64;              // 128-byte K atoms per row
+    static constexpr int ATOM_TILE = TB * 128;     // one K atom of an index tile
+    static constexpr int TILE = KA * ATOM_TILE;
+    static constexpr int Q_ATOM = kQRows * 128;
+    static constexpr int QB = KA * Q_ATOM;
+    static constexpr int OFF_Q = kStages * TILE;
+    static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
+    static constexpr int OFF_BAR = OFF_O + kQRows * 4;
+    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+};
+
+}  // namespace
+
+template <int D, int PASS>
+__global__ void __launch_bounds__(kThreads, 1)
+score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *__restrict__ q,
+                ScoreShape sh, int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
+                int64_t chunk_blocks, ScoreScratch scr, int64_t partial_stride,
+                float scale_log2, int *err) {
+    using LY = Lay<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *tiles = smem;
+    uint8_t *qs = smem + LY::OFF_Q;
+    float *o_r = reinterpret_cast<float *>(smem + LY::OFF_O);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lg = blockIdx.y;
+    const int l = lg / sh.G, g = lg - l * sh.G;
+    const int rows = sh.rows;
+    const int chunk = blockIdx.x;
+    const int64_t cb0 = b_begin + (int64_t)chunk * chunk_blocks;
+    const int64_t cb1 = min(b_end, cb0 + chunk_blocks);
+    const int n_tiles = cb1 > cb0 ? (int)((cb1 - cb0 + TB - 1) / TB) : 0;
+    const int n2 = (rows + 15) & ~15;              // pass-2 N
+    const int qtiles = rows > 128 ? 2 : 1;         // pass-1 M tiles
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tempty[b], 128);
+        }
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // Query rows of (l, g) into the swizzled K-major layout; padding rows are 0.
+    for (int i = tid; i < kQRows * (D / 8); i += kThreads) {
+        const int r = i / (D / 8), c16 = i - r * (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < rows) {
+            const int m = r / sh.gqa, hl = r - m * sh.gqa;
+            const __nv_bfloat16 *src =
+                q + (((size_t)l * sh.n_queries + m) * sh.H + (size_t)g * sh.gqa + hl) * D + c16 * 8;
+            v = *reinterpret_cast<const uint4 *>(src);
+        }
+        const int a = c16 >> 3, cc = c16 & 7;
+        *reinterpret_cast<uint4 *>(qs + a * LY::Q_ATOM + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+    }
+    if (PASS == 2) {
+        for (int r = tid; r < kQRows; r += kThreads) {
+            float o = INFINITY;
+            if (r < rows) {
+                const size_t k = (size_t)lg * rows + r;
+                o = scr.row_m[k] - log2f(scr.row_invz[k]);   // M + log2 Z, log2 units
+            }
+            o_r[r] = o;
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % kStages;
+                const uint32_t ph = (i / kStages) & 1;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
+                tc::mbar_expect_tx(&full[s], LY::TILE);
+                const int64_t gb = cb0 + (int64_t)i * TB;
+                const int32_t y = (int32_t)((int64_t)lg * sh.index_cap + (gb - b_index0));
+#pragma unroll
+                for (int a = 0; a < LY::KA; ++a)
+                    tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
+                                    a * 64, y);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t qbase = tc::smem_u32(qs);
+            const uint32_t tbase = tc::smem_u32(tiles);
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % kStages;
+                const uint32_t ph = (i / kStages) & 1;
+                const int buf = i & 1;
+                const uint32_t bph = (i >> 1) & 1;
+                if (!tc::mbar_wait(&full[s], ph, kWaitLimit)) { atomicOr(err, 4); break; }
+                if (!tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
+                tc::tc_fence_after();
+                const uint32_t d = tmem + buf * 256;
+                const uint32_t tile = tbase + s * LY::TILE;
+                if (PASS == 1) {
+                    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, TB);
+                    for (int t = 0; t < qtiles; ++t) {
+#pragma unroll
+                        for (int a = 0; a < LY::KA; ++a) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = tc::sdesc_sw128(
+                                    qbase + a * LY::Q_ATOM + t * 128 * 128 + kk * 32);
+                                const uint64_t bd =
+                                    tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
+                                tc::mma_bf16(d + t * 128, ad, bd, idesc, (a | kk) != 0);
+                            }
+                        }
+                    }
+                } else {
+                    const uint32_t idesc = tc::idesc_bf16_f32(128, n2);
+#pragma unroll
+                    for (int a = 0; a < LY::KA; ++a) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
+                            const uint64_t bd = tc::sdesc_sw128(qbase + a * LY::Q_ATOM + kk * 32);
+                            tc::mma_bf16(d, ad, bd, idesc, (a | kk) != 0);
+                        }
+                    }
+                }
+                tc::mma_commit(&empty[s]);
+                tc::mma_commit(&tfull[buf]);
+            }
+        }
+    } else {
+        const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
+        const int lrow = quad * 32 + lane;
+        float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
+        for (int i = 0; i < n_tiles; ++i) {
+            const int buf = i & 1;
+            const uint32_t bph = (i >> 1) & 1;
+            const bool ok = tc::mbar_wait(&tfull[buf], bph, kWaitLimit);
+            if (!ok) { atomicOr(err, 4); break; }
+            tc::tc_fence_after();
+            const int64_t gb0 = cb0 + (int64_t)i * TB;
+            const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * 256;
+            if (PASS == 1) {
+                for (int t = 0; t < qtiles; ++t) {
+                    for (int c = 0; c * 32 < nvalid; ++c) {
+                        float v[32];
+                        tc::tmem_ld32(taddr + t * 128 + c * 32, v);
+                        const int nv = min(32, nvalid - c * 32);
+                        float cmax = -INFINITY;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (k < nv) cmax = fmaxf(cmax, v[k]);
+                        const float mn = fmaxf(m_run[t], cmax * scale_log2);
+                        float zs = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (k < nv) zs += fast_exp2(fmaf(v[k], scale_log2, -mn));
+                        z_run[t] = z_run[t] * fast_exp2(m_run[t] - mn) + zs;
+                        m_run[t] = mn;
+                    }
+                }
+            } else {
+                float sum = 0.f;
+                int c = 0;
+                for (; c + 32 <= n2; c += 32) {
+                    float v[32];
+                    tc::tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        sum += fast_exp2(fmaf(v[k], scale_log2, -o_r[c + k]));
+                }
+                if (c < n2) {
+                    float v[16];
+                    tc::tmem_ld16(taddr + c, v);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        sum += fast_exp2(fmaf(v[k], scale_log2, -o_r[c + k]));
+                }
+                if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&tempty[buf]);
+        }
+        if (PASS == 1) {
+            for (int t = 0; t < qtiles; ++t) {
+                const int r = t * 128 + lrow;
+                if (r < rows) {
+                    const size_t o = ((size_t)lg * sh.chunk_cap + chunk0 + chunk) * rows + r;
+                    scr.part_m[o] = m_run[t];
+                    scr.part_z[o] = z_run[t];
+                }
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D view of an index buffer: rows = LG * index_cap Mean-K vectors of d bf16.
+static bool make_index_map(CUtensorMap *m, const void *index, int d, int64_t n_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, TB};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(index), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool score_tc_supported(int q_dtype, int index_dtype, const ScoreShape &sh) {
+    return q_dtype == BF16 && index_dtype == BF16 && (sh.d == 64 || sh.d == 128) &&
+           sh.rows >= 1 && sh.rows <= kQRows && encode_fn() != nullptr;
+}
+
+template <int D, int PASS>
+static cudaError_t tc_t(const ScoreShape &sh, const void *q, const void *index, int64_t b_index0,
+                        int64_t b_begin, int64_t b_end, int chunk0, int n_chunks,
+                        const ScoreScratch &scr, int64_t partial_stride, int *err,
+                        cudaStream_t s) {
+    CUtensorMap map;
+    if (((uintptr_t)index & 15) != 0) return cudaErrorMisalignedAddress;
+    if (!make_index_map(&map, index, D, (int64_t)sh.L * sh.G * sh.index_cap))
+        return cudaErrorInvalidValue;
+    auto kern = score_tc_kernel<D, PASS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t n = b_end - b_begin;
+    const int64_t chunk_blocks = (n + n_chunks - 1) / n_chunks;
+    dim3 grid((unsigned)n_chunks, (unsigned)(sh.L * sh.G));
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+    kern<<<grid, kThreads, Lay<D>::SMEM, s>>>(map, static_cast<const __nv_bfloat16 *>(q), sh,
+                                              b_index0, b_begin, b_end, chunk0, chunk_blocks,
+                                              scr, partial_stride, scale_log2, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score_pass1_tc(const ScoreShape &sh, const void *q, const void *index,
+                                  int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
+                                  int n_chunks, const ScoreScratch &scr, int *err,
+                                  cudaStream_t s) {
+    if (sh.d == 128)
+        return tc_t<128, 1>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0,
+                            err, s);
+    return tc_t<64, 1>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0, err, s);
+}
+
+cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const void *index,
+                                  int64_t b_index0, int64_t b_begin, int64_t b_end, int n_chunks,
+                                  const ScoreScratch &scr, int64_t partial_stride, int *err,
+                                  cudaStream_t s) {
+    if (sh.d == 128)
+        return tc_t<128, 2>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                            partial_stride, err, s);
+    return tc_t<64, 2>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr, partial_stride,
+                       err, s);
+}
+
+}  // namespace kvm

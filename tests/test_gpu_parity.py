@@ -59,12 +59,13 @@ def test_build_index(kvm, wl):
     assert exact > 0.999
 
 
+@pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-def test_score_select(kvm, wl):
+def test_score_select(kvm, wl, variant):
     from paged_kv_cache_meank_gb300 import workload
     ws = workload.make_index_direct(wl, seed=2)
     N = wl.n_blocks
-    ctx = _ctx(kvm, wl)
+    ctx = _ctx(kvm, wl, score_variant=variant)
     index = ws.index.to("cuda")
     q = ws.q.to("cuda")
     scores = torch.empty(N, dtype=torch.float32, device="cuda")
@@ -87,12 +88,13 @@ def test_score_select(kvm, wl):
     assert torch.equal(scores, scores2) and torch.equal(sel, sel2)
 
 
-def test_score_select_fewer_queries_and_ragged(kvm):
+@pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
+def test_score_select_fewer_queries_and_ragged(kvm, variant):
     """n_queries below the configured maximum, N not a multiple of any tile."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID.with_(n_blocks=1237, view_blocks=100)
     ws = workload.make_index_direct(wl, seed=3)
-    ctx = _ctx(kvm, wl, max_queries=wl.n_queries)
+    ctx = _ctx(kvm, wl, max_queries=wl.n_queries, score_variant=variant)
     nq = 7
     q = ws.q[:, :nq].contiguous().to("cuda")
     scores = torch.empty(wl.n_blocks, device="cuda")
