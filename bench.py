@@ -118,12 +118,18 @@ class Clocks:
 # ----------------------------------------------------------------------------
 
 class Step:
-    def __init__(self, wl, seed, device, stream):
+    """The full step on a device-resident workspace: Mean-K build, scoring and
+    selection, view assembly."""
+    parts = ["build", "score_select", "assemble"]
+    launches_per_step = 1 + 5 + 1
+
+    def __init__(self, wl, seed, device, stream, score_variant=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         N, V = wl.n_blocks, wl.view_blocks
         self.ctx = kvm.Context(kvm.config_for(wl, index_location=kvm.KVM_DEVICE,
-                                              repo_location=kvm.KVM_DEVICE), device=device,
+                                              repo_location=kvm.KVM_DEVICE,
+                                              score_variant=score_variant), device=device,
                                stream=stream)
         with torch.cuda.stream(stream):
             ws = workload.make_workspace(wl, seed=seed, device=device)
@@ -145,7 +151,12 @@ class Step:
             self.pool_v = torch.empty_like(self.pool_k)
         self.ctx.sync(stream)
         self.planted = ws.planted
-        self.launches_per_step = 1 + 5 + 1
+
+    def inputs(self):
+        return {"k_pages": self.k_pages, "v": self.v, "q": self.q}
+
+    def outputs(self):
+        return [self.sel, self.scores]
 
     def run(self, ev=None, q=None, k_pages=None, v=None):
         """One step; ev = list of 4 events to bracket build / score / assemble."""
@@ -167,6 +178,68 @@ class Step:
         if ev:
             ev[3].record(s)
 
+    def cpu_sample(self, layers):
+        return cpu_sample(self.wl, self.k_pages, self.v, self.q, layers)
+
+
+class ScoreStep:
+    """Scoring + selection only, over a Mean-K index drawn directly in HBM (the
+    10M-token index-scaling workload)."""
+    parts = ["score_select"]
+    launches_per_step = 5
+
+    def __init__(self, wl, seed, device, stream, score_variant=0):
+        import paged_kv_cache_meank_gb300 as kvm
+        self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        self.ctx = kvm.Context(kvm.config_for(wl, index_location=kvm.KVM_DEVICE,
+                                              repo_location=kvm.KVM_DEVICE,
+                                              max_positions=wl.view_blocks * 32,
+                                              score_variant=score_variant),
+                               device=device, stream=stream)
+        with torch.cuda.stream(stream):
+            ws = workload.make_index_direct(wl, seed=seed, device=device)
+            self.index, self.q = ws.index, ws.q
+            self.scores = torch.empty(wl.n_blocks, dtype=torch.float32, device=device)
+            self.sel = torch.empty(wl.view_blocks, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+        self.planted = ws.planted
+
+    def inputs(self):
+        return {"index": self.index, "q": self.q}
+
+    def outputs(self):
+        return [self.sel, self.scores]
+
+    def run(self, ev=None, q=None, index=None):
+        wl, s = self.wl, self.stream
+        q = self.q if q is None else q
+        index = self.index if index is None else index
+        if ev:
+            ev[0].record(s)
+        self.ctx.score_select(q, wl.n_queries, index, wl.n_blocks, self.scores, self.sel,
+                              stream=s)
+        if ev:
+            ev[1].record(s)
+
+    def cpu_sample(self, layers):
+        """The oracle's Eq. (10) + selection on `layers` layers and the first
+        1/16 of the blocks (at least 4096), scaled to the whole step."""
+        import oracle.kvmem as ora
+        wl = self.wl
+        nb = max(4096, wl.n_blocks // 16)
+        idx = _np_bits(self.index[:layers, :, :nb])
+        qq = _np_bits(self.q[:layers])
+        t0 = time.perf_counter()
+        R = ora.block_relevance(ora.as_f64(qq, wl.q_dtype), ora.as_f64(idx, wl.index_dtype), nb)
+        ora.select_blocks(R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+        dt = time.perf_counter() - t0
+        return dt, dt * (wl.n_layers / layers) * (wl.n_blocks / nb), \
+            f"Eq. (10) + selection on {layers} of {wl.n_layers} layers and {nb} of " \
+            f"{wl.n_blocks} blocks"
+
+
+STEP_KIND = {"tiny-4k": Step, "q27-256k": Step, "q27-10m-score": ScoreStep}
+
 
 def algorithmic_bytes(wl):
     """Per-step algorithmic HBM bytes of each kernel (reads + writes that the
@@ -186,13 +259,15 @@ def bench_ours(args, wl, world, rank, local, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    step = Step(wl, args.seed + rank, dev, stream)
+    kind = STEP_KIND.get(wl.name.split("@")[0], Step)
+    step = kind(wl, args.seed + rank, dev, stream, score_variant=args.score_variant)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    npart = len(step.parts)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(npart + 1)] for _ in range(K)]
     clocks = Clocks()
     if dist:
         dist.barrier()
@@ -214,11 +289,8 @@ def bench_ours(args, wl, world, rank, local, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms = total_ms / K
-    parts = {
-        "build": float(np.mean([e[0].elapsed_time(e[1]) for e in evs])),
-        "score_select": float(np.mean([e[1].elapsed_time(e[2]) for e in evs])),
-        "assemble": float(np.mean([e[2].elapsed_time(e[3]) for e in evs])),
-    }
+    parts = {p: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs]))
+             for i, p in enumerate(step.parts)}
     ab = algorithmic_bytes(wl)
     peak, peak_kind = _peaks()
     kern = {k: {"ms": parts[k], "gbs": ab[k] / (parts[k] * 1e-3) / 1e9,
@@ -240,11 +312,11 @@ def bench_ours(args, wl, world, rank, local, dist):
                    "l2": "inputs larger than L2 (K pages %.1f GB), no flush" %
                          (wl.n_blocks * wl.block_bytes / 1e9)},
         "components": {
-            "recall_ms": parts["score_select"] + parts["assemble"],
-            "build_ms": parts["build"], "score_select_ms": parts["score_select"],
-            "assemble_ms": parts["assemble"],
+            "recall_ms": parts["score_select"] + parts.get("assemble", 0.0),
+            **{f"{p}_ms": parts[p] for p in parts},
             "index_hbm_gbs": kern["score_select"]["gbs"],
-            "assembly_tokens_per_s": wl.view_tokens / (parts["assemble"] * 1e-3),
+            **({"assembly_tokens_per_s": wl.view_tokens / (parts["assemble"] * 1e-3)}
+               if "assemble" in parts else {}),
             "kernels": kern,
         },
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"],
@@ -259,6 +331,25 @@ def bench_ours(args, wl, world, rank, local, dist):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, step, args.cpu_layers)
     return out
+
+
+def h2d_peak(dev, stream, nbytes=256 << 20, reps=20):
+    """Pinned host -> device copy bandwidth of one cudaMemcpyAsync of 256 MiB,
+    median of 20, measured in the same run (the link roofline for H2D)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        d.copy_(h, non_blocking=True)
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            d.copy_(h, non_blocking=True)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    return nbytes / (ms * 1e-3) / 1e9
 
 
 def _traffic_from_profile(kernel):
@@ -286,25 +377,22 @@ def bench_e2e(args, step, dev, stream, world, dist):
     V, queries) in pinned host memory: H2D of the inputs and D2H of the result
     (selected ids and block scores) inside the timed region."""
     wl = step.wl
-    k_h = torch.empty(step.k_pages.shape, dtype=step.k_pages.dtype, pin_memory=True)
-    v_h = torch.empty(step.v.shape, dtype=step.v.dtype, pin_memory=True)
-    q_h = torch.empty(step.q.shape, dtype=step.q.dtype, pin_memory=True)
-    k_h.copy_(step.k_pages)
-    v_h.copy_(step.v)
-    q_h.copy_(step.q)
-    sel_h = torch.empty(step.sel.shape, dtype=step.sel.dtype, pin_memory=True)
-    sc_h = torch.empty(step.scores.shape, dtype=step.scores.dtype, pin_memory=True)
-    k_d, v_d, q_d = torch.empty_like(step.k_pages), torch.empty_like(step.v), torch.empty_like(step.q)
+    ins = step.inputs()
+    host = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in ins.items()}
+    for k in ins:
+        host[k].copy_(ins[k])
+    outs = step.outputs()
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    devc = {k: torch.empty_like(t) for k, t in ins.items()}
     steps = max(1, min(args.steps, 5))
 
     def one():
         with torch.cuda.stream(stream):
-            k_d.copy_(k_h, non_blocking=True)
-            v_d.copy_(v_h, non_blocking=True)
-            q_d.copy_(q_h, non_blocking=True)
-            step.run(q=q_d, k_pages=k_d, v=v_d)
-            sel_h.copy_(step.sel, non_blocking=True)
-            sc_h.copy_(step.scores, non_blocking=True)
+            for k in ins:
+                devc[k].copy_(host[k], non_blocking=True)
+            step.run(**devc)
+            for o, oh in zip(outs, outs_h):
+                oh.copy_(o, non_blocking=True)
 
     one()
     torch.cuda.synchronize(dev)
@@ -322,13 +410,14 @@ def bench_e2e(args, step, dev, stream, world, dist):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    h2d = k_h.numel() * k_h.element_size() + v_h.numel() * v_h.element_size() + \
-        q_h.numel() * q_h.element_size()
-    d2h = sel_h.numel() * 4 + sc_h.numel() * 4
-    del k_d, v_d, q_d
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    del devc
+    peak = h2d_peak(dev, stream)
     return {"value": world * wl.n_blocks / (ms * 1e-3), "unit": "scored blocks/s",
             "ms_per_step": ms, "steps": steps, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "h2d_gbs": h2d / (ms * 1e-3) / 1e9}
+            "d2h_bytes_per_step": int(d2h), "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
+            "h2d_peak_gbs": peak, "inputs": sorted(host)}
 
 
 # ----------------------------------------------------------------------------
@@ -366,16 +455,16 @@ def cpu_sample(wl, k_pages, v, q, layers):
     _oracle_step_slice(wl.with_(n_layers=layers), kp, vv, qq, layers)
     dt = time.perf_counter() - t0
     full = dt * wl.n_layers / layers
-    return dt, full
+    return dt, full, (f"one step restricted to {layers} of {wl.n_layers} layers (all "
+                      f"{wl.n_blocks} blocks, {wl.view_blocks}-block view)")
 
 
 def cpu_baseline(wl, step, layers):
-    dt, full = cpu_sample(wl, step.k_pages, step.v, step.q, layers)
+    dt, full, what = step.cpu_sample(layers)
     return {"value": wl.n_blocks / full, "unit": "scored blocks/s",
             "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one step restricted to {layers} of {wl.n_layers} layers "
-                      f"(all {wl.n_blocks} blocks, {wl.view_blocks}-block view); "
-                      f"{dt:.1f} s measured, scaled by {wl.n_layers}/{layers} layers",
+            "sample": f"{what}; {dt:.1f} s measured, scaled to the whole step "
+                      "(NumPy float64; element-wise work on one core, matmuls on BLAS threads)",
             "sample_seconds": dt}
 
 
@@ -435,6 +524,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--score-variant", type=int, default=0,
+                    help="0: tensor-core scoring where supported, 1: CUDA cores")
     ap.add_argument("--blocks", type=int, default=0,
                     help="override the history length (small cases for profiling)")
     args = ap.parse_args()
