@@ -238,7 +238,206 @@ class ScoreStep:
             f"{wl.n_blocks} blocks"
 
 
-STEP_KIND = {"tiny-4k": Step, "q27-256k": Step, "q27-10m-score": ScoreStep}
+def build_host_workspace(kvm, wl, seed, device, stream, ctx, n_blocks, index_on_host,
+                         keep_pages_from=None):
+    """History of n_blocks blocks: raw K / V drawn on the GPU, K pages rotated at
+    original positions, Mean-K built on the GPU; raw K / V then moved to pinned
+    host memory (the repository) and the index to pinned host memory or kept in
+    HBM.  Returns (raw_h, v_h, index, planted, u, k_pages_tail)."""
+    with torch.cuda.stream(stream):
+        ws = workload.make_workspace(wl, seed=seed, device=device, n_blocks=n_blocks,
+                                     with_q=False)
+        kp = torch.empty_like(ws.raw_k)
+        ident = torch.arange(n_blocks, dtype=torch.int32, device=device)
+        ctx.assemble_view(ident, None, n_blocks, ws.raw_k, None, kp, None, stream=stream)
+        index = torch.zeros(ctx.index_shape(), dtype=ctx.index_dtype, device=device)
+        ctx.build_index(kp, 0, n_blocks, index, ws.raw_k, stream=stream)
+    ctx.sync(stream)
+    raw_h = torch.empty(ws.raw_k.shape, dtype=ws.raw_k.dtype, pin_memory=True)
+    raw_h.copy_(ws.raw_k)
+    v_h = torch.empty(ws.v.shape, dtype=ws.v.dtype, pin_memory=True)
+    v_h.copy_(ws.v)
+    tail = kp[keep_pages_from:].clone() if keep_pages_from is not None else None
+    if index_on_host:
+        idx_h = torch.empty(index.shape, dtype=index.dtype, pin_memory=True)
+        idx_h.copy_(index)
+        index = idx_h
+    planted, u, topic_of = ws.planted, ws.u, ws.topic_of
+    del ws, kp
+    torch.cuda.empty_cache()
+    return raw_h, v_h, index, planted, u, topic_of, tail
+
+
+class HostStep:
+    """One working-set update through kvm_step with the history's raw K / V and
+    the Mean-K index in pinned host memory (the 1M-token workload): host-tiled
+    scoring, selection, residency diff, packed H2D of the missed blocks and their
+    re-RoPE.  Every timed step starts from an empty page pool, so all selected
+    blocks are misses."""
+    parts = ["step"]
+    launches_per_step = 0   # counted from the step statistics
+
+    def __init__(self, wl, seed, device, stream, score_variant=0):
+        import paged_kv_cache_meank_gb300 as kvm
+        self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
+                             index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
+                             else kvm.KVM_DEVICE, h2d_batch_blocks=256,
+                             score_variant=score_variant)
+        self.ctx = kvm.Context(cfg, device=device, stream=stream)
+        (self.raw_h, self.v_h, self.index, self.planted, u, _, _) = build_host_workspace(
+            kvm, wl, seed, device, stream, self.ctx, wl.n_blocks, wl.index_loc == "host")
+        g = torch.Generator(device=device).manual_seed(seed + 1)
+        self.q = workload.make_queries(wl, g, device, u)
+        V, P = wl.view_blocks, cfg.pool_pages
+        self.pool_k = torch.empty(self.ctx.block_shape(P), dtype=self.ctx.kv_dtype, device=device)
+        self.pool_v = torch.empty_like(self.pool_k)
+        self.pool_raw = torch.empty_like(self.pool_k)
+        self.page_table = torch.empty(V, dtype=torch.int32, device=device)
+        self.scores = torch.empty(wl.n_blocks, dtype=torch.float32, device=device)
+        self.sel = torch.empty(V, dtype=torch.int32, device=device)
+        self.ctx.bind(index=self.index, raw_k=self.raw_h, v=self.v_h, pool_k=self.pool_k,
+                      pool_v=self.pool_v, pool_raw_k=self.pool_raw, page_table=self.page_table,
+                      scores=self.scores, sel_ids=self.sel)
+        self.stats = []
+        nt = (wl.n_blocks + wl.tile_blocks - 1) // wl.tile_blocks
+        self.score_launches = (2 * nt + 3) if wl.index_loc == "host" else 5
+
+    def inputs(self):
+        return {"q": self.q}
+
+    def outputs(self):
+        return [self.sel, self.scores, self.page_table]
+
+    def run(self, ev=None, q=None):
+        wl, s = self.wl, self.stream
+        q = self.q if q is None else q
+        self.ctx.reset_pool()
+        if ev:
+            ev[0].record(s)
+        st = self.ctx.step(q, wl.n_queries, wl.n_blocks, stream=s)
+        if ev:
+            ev[1].record(s)
+        self.stats.append(st)
+        b = self.ctx.cfg.h2d_batch_blocks
+        self.launches_per_step = self.score_launches + (st["misses"] + b - 1) // b + \
+            (1 if st["reroped"] > st["misses"] else 0)
+
+    def link_bytes(self):
+        """Host-to-device bytes of one step: the index tiles (streamed twice, once
+        per scoring pass, when the index is in host memory) plus the missed
+        blocks' raw K and V."""
+        wl = self.wl
+        idx = 0
+        if wl.index_loc == "host":
+            idx = 2 * wl.n_layers * wl.n_kv_heads * wl.n_blocks * wl.head_dim * 2
+        return idx + float(np.mean([s["h2d_bytes"] for s in self.stats[-8:]]))
+
+    def cpu_sample(self, layers):
+        return oracle_select_view_sample(self.wl, self.index, self.q, self.raw_h, layers)
+
+
+class ChurnStep:
+    """Consecutive agent steps over a growing history (the multi-step churn
+    workload): each step appends 64 blocks (Mean-K built from their K pages),
+    draws queries whose planted topics overlap 70% with the previous step's, and
+    runs kvm_step with the raw K / V in pinned host memory; blocks already in the
+    page pool are reused, only misses go H2D."""
+    parts = ["append_build", "step"]
+    launches_per_step = 0
+    per_step_inputs = True
+
+    def __init__(self, wl, seed, device, stream, score_variant=0):
+        import paged_kv_cache_meank_gb300 as kvm
+        self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        total = wl.n_blocks + wl.steps * wl.append_blocks
+        cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
+                             index_location=kvm.KVM_DEVICE, h2d_batch_blocks=256,
+                             score_variant=score_variant)
+        self.ctx = kvm.Context(cfg, device=device, stream=stream)
+        (self.raw_h, self.v_h, self.index, self.planted, self.u, self.topic_of,
+         self.new_pages) = build_host_workspace(kvm, wl, seed, device, stream, self.ctx, total,
+                                                False, keep_pages_from=wl.n_blocks)
+        self.topics = workload.churn_topics(wl, seed, device)
+        ws_like = workload.Workspace(wl=wl, u=self.u, planted=self.planted, topic_of=self.topic_of)
+        self.queries = [workload.churn_queries(wl, ws_like, t, self.topics[t], seed, device)
+                        for t in range(wl.steps)]
+        V, P = wl.view_blocks, cfg.pool_pages
+        self.pool_k = torch.empty(self.ctx.block_shape(P), dtype=self.ctx.kv_dtype, device=device)
+        self.pool_v = torch.empty_like(self.pool_k)
+        self.pool_raw = torch.empty_like(self.pool_k)
+        self.page_table = torch.empty(V, dtype=torch.int32, device=device)
+        self.scores = torch.empty(total, dtype=torch.float32, device=device)
+        self.sel = torch.empty(V, dtype=torch.int32, device=device)
+        self.ctx.bind(index=self.index, raw_k=self.raw_h, v=self.v_h, pool_k=self.pool_k,
+                      pool_v=self.pool_v, pool_raw_k=self.pool_raw, page_table=self.page_table,
+                      scores=self.scores, sel_ids=self.sel)
+        self.t = 0
+        self.stats = []
+        self.q = self.queries[0]
+
+    def inputs(self):
+        # every step's queries: the e2e leg copies step t's set each step
+        return {"q": torch.stack(self.queries)}
+
+    def outputs(self):
+        return [self.sel, self.scores, self.page_table]
+
+    def run(self, ev=None, q=None):
+        wl, s = self.wl, self.stream
+        t = self.t % wl.steps
+        if q is not None and q.dim() == 5:
+            q = q[t]
+        if t == 0:
+            self.ctx.reset_pool()
+        n_prev = wl.n_blocks + t * wl.append_blocks
+        n_now = n_prev + wl.append_blocks
+        if ev:
+            ev[0].record(s)
+        a = t * wl.append_blocks
+        self.ctx.build_index(self.new_pages[a:a + wl.append_blocks], n_prev, wl.append_blocks,
+                             self.index, None, stream=s)
+        if ev:
+            ev[1].record(s)
+        st = self.ctx.step(self.queries[t] if q is None else q, wl.n_queries, n_now, stream=s)
+        if ev:
+            ev[2].record(s)
+        self.stats.append(dict(st, t=t))
+        self.t += 1
+        self.launches_per_step = 1 + 5 + (st["misses"] + 255) // 256 + \
+            (1 if st["reroped"] > st["misses"] else 0)
+
+    def link_bytes(self):
+        """Host-to-device bytes of one step: the missed blocks' raw K and V."""
+        return float(np.mean([s["h2d_bytes"] for s in self.stats[-self.wl.steps:]]))
+
+    def cpu_sample(self, layers):
+        wl = self.wl
+        return oracle_select_view_sample(wl.with_(n_blocks=wl.n_blocks + wl.append_blocks),
+                                         self.index, self.queries[0], self.raw_h, layers)
+
+
+def oracle_select_view_sample(wl, index, q, raw_h, layers):
+    """The oracle's Eq. (10) + selection + view K on `layers` layers and the
+    first 1/8 of the blocks (at least 2048), scaled to the whole step."""
+    import oracle.kvmem as ora
+    nb = max(2048, wl.n_blocks // 8)
+    idx = _np_bits(index[:layers, :, :nb])
+    qq = _np_bits(q[:layers])
+    t0 = time.perf_counter()
+    R = ora.block_relevance(ora.as_f64(qq, wl.q_dtype), ora.as_f64(idx, wl.index_dtype), nb)
+    sel = ora.select_blocks(R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks * nb // wl.n_blocks)
+    rk = _np_bits(raw_h[torch.from_numpy(sel.astype(np.int64)), :layers])
+    ora.view_k(rk, wl.kv_dtype, wl.rope_theta)
+    dt = time.perf_counter() - t0
+    return dt, dt * (wl.n_layers / layers) * (wl.n_blocks / nb), \
+        (f"Eq. (10), selection and view K on {layers} of {wl.n_layers} layers and {nb} of "
+         f"{wl.n_blocks} blocks (view scaled alike)")
+
+
+STEP_KIND = {"tiny-4k": Step, "q27-256k": Step, "q27-10m-score": ScoreStep,
+             "q27x16-1m": HostStep, "q27-512k-churn": ChurnStep,
+             "q27x16-512k-churn": ChurnStep}
 
 
 def algorithmic_bytes(wl):
@@ -293,10 +492,34 @@ def bench_ours(args, wl, world, rank, local, dist):
              for i, p in enumerate(step.parts)}
     ab = algorithmic_bytes(wl)
     peak, peak_kind = _peaks()
+    link = getattr(step, "link_bytes", None)
+    if link is not None:
+        # kvm_step over a host-resident history: the bytes the step must move
+        # over the host link (index tiles + missed blocks), per step
+        ab = dict(ab, step=link(), append_build=ab["build"] * wl.append_blocks // wl.n_blocks
+                  if wl.n_blocks else 0)
+        ab["build"] = ab["append_build"]
     kern = {k: {"ms": parts[k], "gbs": ab[k] / (parts[k] * 1e-3) / 1e9,
                 "frac_hbm": ab[k] / (parts[k] * 1e-3) / 1e9 / peak} for k in parts}
     dom = max(parts, key=parts.get)
     traffic = _traffic_from_profile(dom)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"], "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_hbm"],
+            "traffic": traffic, "algorithmic_bytes": ab[dom]}
+    if link is not None and dom == "step":
+        hp = h2d_peak(dev, stream)
+        roof.update(bound="h2d", peak=hp, peak_kind="measured pinned H2D (256 MiB copy)",
+                    frac=kern[dom]["gbs"] / hp, traffic=None)
+    recall_ms = parts.get("step", parts.get("score_select", 0.0) + parts.get("assemble", 0.0))
+    comps = {"recall_ms": recall_ms, **{f"{p}_ms": parts[p] for p in parts}, "kernels": kern}
+    if "score_select" in parts:
+        comps["index_hbm_gbs"] = kern["score_select"]["gbs"]
+    if "assemble" in parts:
+        comps["assembly_tokens_per_s"] = wl.view_tokens / (parts["assemble"] * 1e-3)
+    if getattr(step, "stats", None):
+        st = step.stats[-K:]
+        comps["step_stats"] = {k: float(np.mean([s[k] for s in st]))
+                               for k in ("hits", "misses", "reroped", "h2d_bytes", "h2d_copies")}
     out = {
         "metric": METRIC,
         "value": world * wl.n_blocks / (ms * 1e-3),
@@ -309,20 +532,9 @@ def bench_ours(args, wl, world, rank, local, dist):
                    "history_tokens": wl.n_tokens, "queries": wl.n_queries,
                    "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
                    "recent_blocks": wl.recent_blocks, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (K pages %.1f GB), no flush" %
-                         (wl.n_blocks * wl.block_bytes / 1e9)},
-        "components": {
-            "recall_ms": parts["score_select"] + parts.get("assemble", 0.0),
-            **{f"{p}_ms": parts[p] for p in parts},
-            "index_hbm_gbs": kern["score_select"]["gbs"],
-            **({"assembly_tokens_per_s": wl.view_tokens / (parts["assemble"] * 1e-3)}
-               if "assemble" in parts else {}),
-            "kernels": kern,
-        },
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"],
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": kern[dom]["frac_hbm"], "traffic": traffic,
-                     "algorithmic_bytes": ab[dom]},
+                   "l2": "inputs larger than L2, no flush"},
+        "components": comps,
+        "roofline": roof,
         "gpu_launches": step.launches_per_step * K,
         "clocks": clk,
     }
@@ -386,10 +598,16 @@ def bench_e2e(args, step, dev, stream, world, dist):
     devc = {k: torch.empty_like(t) for k, t in ins.items()}
     steps = max(1, min(args.steps, 5))
 
+    per_step = getattr(step, "per_step_inputs", False)
+
     def one():
         with torch.cuda.stream(stream):
             for k in ins:
-                devc[k].copy_(host[k], non_blocking=True)
+                if per_step:       # only this step's slice crosses the link
+                    i = step.t % wl.steps
+                    devc[k][i].copy_(host[k][i], non_blocking=True)
+                else:
+                    devc[k].copy_(host[k], non_blocking=True)
             step.run(**devc)
             for o, oh in zip(outs, outs_h):
                 oh.copy_(o, non_blocking=True)
@@ -411,6 +629,8 @@ def bench_e2e(args, step, dev, stream, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
+    if per_step:
+        h2d //= wl.steps
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     del devc
     peak = h2d_peak(dev, stream)

@@ -110,4 +110,8 @@ CHURN512K = Workload(name="q27-512k-churn", n_blocks=16384, view_blocks=2048,
 W10M = Workload(name="q27-10m-score", n_blocks=312500, view_blocks=2048,
                 planted_frac=0.005, **_Q27)
 
-ALL = {w.name: w for w in (TINY, W256K, W1M, CHURN512K, W10M)}
+# The churn workload on a 16-layer slice: its 64-layer raw K / V (148 GB) does
+# not fit pinned in the 199 GB of host memory next to the rest of the process.
+CHURN512K_16 = CHURN512K.with_(name="q27x16-512k-churn", n_layers=16)
+
+ALL = {w.name: w for w in (TINY, W256K, W1M, CHURN512K, CHURN512K_16, W10M)}

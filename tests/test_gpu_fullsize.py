@@ -1,0 +1,259 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+The oracle cannot evaluate whole multi-gigabyte workspaces, so each test checks
+what it can compute one by one (sampled blocks and view slots, or Eq. (10) over
+every block when that is a few seconds of float64 work) and properties that
+hold at any size.  Inputs are seeded draws (raw K / V, Mean-K drawn directly,
+K pages drawn directly) -- nothing the oracle consumes comes from the CUDA path.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.kvmem as ora
+from gpu_helpers import (assert_meank_close, assert_scores_close, assert_storage_close,
+                         check_selection, to_np)
+from paged_kv_cache_meank_gb300 import configs, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvm():
+    import paged_kv_cache_meank_gb300 as kvm
+    from paged_kv_cache_meank_gb300 import build
+    build.build()
+    return kvm
+
+
+@pytest.fixture(autouse=True)
+def _release_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()
+
+
+def _pinned(t):
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+def _oracle_R(q, index, wl, n_blocks):
+    return ora.block_relevance(ora.as_f64(to_np(q, wl.q_dtype), wl.q_dtype),
+                               ora.as_f64(to_np(index[:, :, :n_blocks], wl.index_dtype),
+                                          wl.index_dtype), n_blocks)
+
+
+def test_256k_build_sampled(kvm):
+    """Mean-K and raw K over the full 8192-block, 64-layer history; sampled
+    blocks against the oracle."""
+    wl = configs.W256K
+    g = torch.Generator(device="cuda").manual_seed(101)
+    N = wl.n_blocks
+    ctx = kvm.Context(kvm.config_for(wl))
+    kp = torch.empty(ctx.block_shape(N), dtype=torch.bfloat16, device="cuda")
+    for i in range(0, N, 1024):     # K as a prefill leaves it, drawn directly
+        kp[i:i + 1024] = (torch.randn(kp[i:i + 1024].shape, generator=g, device="cuda")
+                          * wl.k_std).to(torch.bfloat16)
+    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+    raw = torch.empty_like(kp)
+    ctx.build_index(kp, 0, N, index, raw)
+    ctx.sync()
+    rng = np.random.default_rng(7)
+    ids = np.unique(np.concatenate([[0, 1, N - 1], rng.choice(N, 29, replace=False)]))
+    for b in ids:
+        kpb = to_np(kp[b:b + 1], "bf16")
+        ref = ora.meank(kpb, "bf16", int(b), wl.rope_theta)
+        got = to_np(index[:, :, b:b + 1], "bf16")
+        kmax = float(np.abs(ora.as_f64(kpb, "bf16")).max()) * 2 ** 0.5
+        assert_meank_close(got, ref, "bf16", wl.k_std, f"block {b}", kmax)
+        exact = assert_storage_close(to_np(raw[b:b + 1], "bf16"),
+                                     ora.raw_k(kpb, "bf16", int(b), wl.rope_theta), "bf16",
+                                     f"raw K block {b}")
+        assert exact > 0.999
+
+
+def test_256k_score_select_all_blocks(kvm):
+    """Eq. (10) over all 8192 blocks x 64 layers x 48 heads x 32 queries against
+    the float64 oracle; selection by the near-tie band rule."""
+    wl = configs.W256K
+    ws = workload.make_index_direct(wl, seed=102, device="cuda")
+    ctx = kvm.Context(kvm.config_for(wl))
+    N, V = wl.n_blocks, wl.view_blocks
+    scores = torch.empty(N, device="cuda")
+    sel = torch.empty(V, dtype=torch.int32, device="cuda")
+    ctx.score_select(ws.q, wl.n_queries, ws.index, N, scores, sel)
+    ctx.sync()
+    R = _oracle_R(ws.q, ws.index, wl, N)
+    assert_scores_close(scores.cpu().numpy(), R, "256K scores")
+    check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, V, "256K")
+    assert set(ws.planted.tolist()) <= set(sel.cpu().tolist())
+
+
+def test_256k_assemble_sampled(kvm):
+    """The full 1024-slot view over the 64-layer history; sampled slots against
+    the oracle's view, every V byte compared."""
+    wl = configs.W256K
+    ws = workload.make_workspace(wl, seed=103, device="cuda", with_q=False)
+    ctx = kvm.Context(kvm.config_for(wl))
+    N, V = wl.n_blocks, wl.view_blocks
+    rng = np.random.default_rng(8)
+    ids = np.sort(rng.choice(N, V, replace=False)).astype(np.int32)
+    kp = torch.empty(ctx.block_shape(V), dtype=torch.bfloat16, device="cuda")
+    vp = torch.empty_like(kp)
+    ctx.assemble_view(torch.from_numpy(ids).cuda(), None, V, ws.raw_k, ws.v, kp, vp)
+    ctx.sync()
+    assert torch.equal(vp, ws.v[torch.from_numpy(ids).long().cuda()])
+    for j in np.unique(np.concatenate([[0, V - 1], rng.choice(V, 14, replace=False)])):
+        b = int(ids[j])
+        raw = to_np(ws.raw_k[b:b + 1], "bf16")
+        c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
+        ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
+        assert_storage_close(to_np(kp[j:j + 1], "bf16"), ref, "bf16", f"slot {j}")
+
+
+def test_10m_scoring_properties(kvm):
+    """The 312500-block, 41 GB index: every planted block is selected, relevance
+    sums to the query count, and permuting the blocks permutes the scores."""
+    wl = configs.W10M
+    ws = workload.make_index_direct(wl, seed=104, device="cuda")
+    ctx = kvm.Context(kvm.config_for(wl, max_positions=wl.view_blocks * 32))
+    N, V = wl.n_blocks, wl.view_blocks
+    scores = torch.empty(N, device="cuda")
+    sel = torch.empty(V, dtype=torch.int32, device="cuda")
+    ctx.score_select(ws.q, wl.n_queries, ws.index, N, scores, sel)
+    ctx.sync()
+    assert abs(scores.double().sum().item() - wl.n_queries) < 1e-4 * wl.n_queries
+    got = sel.cpu().numpy()
+    assert np.all(np.diff(got) > 0) and len(got) == V
+    assert set(range(wl.sink_blocks)) <= set(got.tolist())
+    assert set(range(N - wl.recent_blocks, N)) <= set(got.tolist())
+    assert set(ws.planted.tolist()) <= set(got.tolist())
+    # the selection is consistent with the GPU's own scores (ties: lower id)
+    s_np = scores.cpu().numpy().astype(np.float64)
+    want = ora.select_blocks(s_np, wl.sink_blocks, wl.recent_blocks, V)
+    assert np.array_equal(got, want)
+    # permutation equivariance of Eq. (10)
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(5)).cuda()
+    idx_p = ws.index[:, :, perm].contiguous()
+    ws.index = None
+    scores_p = torch.empty_like(scores)
+    ctx.score_select(ws.q, wl.n_queries, idx_p, N, scores_p, sel)
+    ctx.sync()
+    rel = ((scores_p.double() - scores[perm].double()).abs() / scores[perm].double()).max()
+    assert rel.item() < 1e-4
+
+
+def test_1m_host_step(kvm):
+    """kvm_step over the 1M-token, 16-layer workspace with raw K / V (68.7 GB) and
+    the Mean-K index in pinned host memory, scored in 1024-block tiles."""
+    wl = configs.W1M
+    N, V = wl.n_blocks, wl.view_blocks
+    ws = workload.make_workspace(wl, seed=105, device="cuda", with_q=False)
+    idx = workload.make_index_direct(wl, seed=106, device="cuda")
+    raw_h, v_h, idx_h = _pinned(ws.raw_k), _pinned(ws.v), _pinned(idx.index)
+    q = idx.q
+    del ws
+    torch.cuda.empty_cache()
+    cfg = kvm.config_for(wl, h2d_batch_blocks=256)
+    ctx = kvm.Context(cfg)
+    P = cfg.pool_pages
+    pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+    pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
+    pt = torch.empty(V, dtype=torch.int32, device="cuda")
+    scores = torch.empty(N, device="cuda")
+    sel = torch.empty(V, dtype=torch.int32, device="cuda")
+    ctx.bind(index=idx_h, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
+             page_table=pt, scores=scores, sel_ids=sel)
+    st = ctx.step(q, wl.n_queries, N)
+    ctx.sync()
+    assert st["misses"] == V and st["hits"] == 0
+    R = _oracle_R(q, idx.index, wl, N)
+    assert_scores_close(scores.cpu().numpy(), R, "1M scores")
+    g_sel = sel.cpu().numpy()
+    check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, "1M")
+    page, _, _, _, _ = ora.residency_step([-1] * P, [-1] * P, g_sel)
+    assert pt.cpu().tolist() == page
+    rng = np.random.default_rng(9)
+    for j in np.unique(np.concatenate([[0, V - 1], rng.choice(V, 14, replace=False)])):
+        b, p = int(g_sel[j]), page[j]
+        raw = to_np(raw_h[b:b + 1], "bf16")
+        c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
+        ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
+        assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16", f"1M slot {j}")
+        assert torch.equal(pool_v[p].cpu(), v_h[b])
+        assert torch.equal(pool_r[p].cpu(), raw_h[b])
+
+
+def test_512k_churn_steps(kvm):
+    """Twenty agent steps over the 512K-token history (16-layer slice): each
+    step appends 64 blocks whose Mean-K the GPU builds, draws queries with 70%
+    topic overlap, and updates the page pool by the delta rule; scores and
+    selection against the oracle every fifth step, the page table every step."""
+    wl = configs.CHURN512K_16
+    total = wl.n_blocks + wl.steps * wl.append_blocks
+    V = wl.view_blocks
+    ws = workload.make_workspace(wl, seed=107, device="cuda", n_blocks=total, with_q=False)
+    raw_h, v_h = _pinned(ws.raw_k), _pinned(ws.v)
+    g = torch.Generator(device="cuda").manual_seed(108)
+    base = workload.make_index_direct(wl.with_(n_topics=1), seed=109, device="cuda",
+                                      n_blocks=wl.n_blocks)
+    new_pages = (torch.randn((wl.steps * wl.append_blocks, wl.n_layers, wl.n_kv_heads, 32,
+                              wl.head_dim), generator=g, device="cuda") * wl.k_std).to(torch.bfloat16)
+    topics = workload.churn_topics(wl, 107, "cuda")
+    cfg = kvm.config_for(wl, h2d_batch_blocks=256)
+    ctx = kvm.Context(cfg)
+    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+    index[:, :, :wl.n_blocks] = base.index
+    # the oracle's index: the same drawn base plus its own Mean-K of the appended pages
+    new_np = to_np(new_pages, "bf16")
+    ora_index = np.zeros((wl.n_layers, wl.n_kv_heads, total, wl.head_dim))
+    ora_index[:, :, :wl.n_blocks] = ora.as_f64(to_np(base.index, "bf16"), "bf16")
+    P = cfg.pool_pages
+    pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+    pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
+    pt = torch.empty(V, dtype=torch.int32, device="cuda")
+    scores = torch.empty(total, device="cuda")
+    sel = torch.empty(V, dtype=torch.int32, device="cuda")
+    ctx.bind(index=index, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
+             page_table=pt, scores=scores, sel_ids=sel)
+    del ws
+    bop, bp = [-1] * P, [-1] * P
+    rng = np.random.default_rng(10)
+    hits = []
+    for t in range(wl.steps):
+        n_prev = wl.n_blocks + t * wl.append_blocks
+        n_now = n_prev + wl.append_blocks
+        a = t * wl.append_blocks
+        ctx.build_index(new_pages[a:a + wl.append_blocks], n_prev, wl.append_blocks, index, None)
+        mk = ora.meank(new_np[a:a + wl.append_blocks], "bf16", n_prev, wl.rope_theta)
+        ora_index[:, :, n_prev:n_now] = ora.as_f64(ora.round_to(mk.astype(np.float32), "bf16"),
+                                                   "bf16")
+        ws_like = workload.Workspace(wl=wl, u=base.u[None].expand(wl.n_topics, -1),
+                                     planted=base.planted)
+        q = workload.churn_queries(wl, ws_like, t, topics[t], 107, "cuda")
+        st = ctx.step(q, wl.n_queries, n_now)
+        ctx.sync()
+        g_sel = sel[:V].cpu().numpy()
+        if t % 5 == 0 or t == wl.steps - 1:
+            R = ora.block_relevance(ora.as_f64(to_np(q, "bf16"), "bf16"), ora_index, n_now)
+            assert_scores_close(scores[:n_now].cpu().numpy(), R, f"churn step {t}")
+            check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, f"churn step {t}")
+        page, hit, rope, bop, bp = ora.residency_step(bop, bp, g_sel)
+        assert pt.cpu().tolist() == page, f"step {t} page table"
+        assert st["hits"] == sum(hit) and st["reroped"] == sum(rope)
+        hits.append(st["hits"])
+        for j in rng.choice(V, 4, replace=False):
+            b, p = int(g_sel[j]), page[j]
+            raw = to_np(raw_h[b:b + 1], "bf16")
+            c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
+            ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
+            assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16",
+                                 f"churn step {t} slot {j}")
+            assert torch.equal(pool_v[p].cpu(), v_h[b])
+    assert hits[0] == 0 and max(hits[1:]) > 0      # later steps reuse resident pages
