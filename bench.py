@@ -123,7 +123,7 @@ class Step:
     parts = ["build", "score_select", "assemble"]
     launches_per_step = 1 + 5 + 1
 
-    def __init__(self, wl, seed, device, stream, score_variant=0):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         N, V = wl.n_blocks, wl.view_blocks
@@ -188,7 +188,7 @@ class ScoreStep:
     parts = ["score_select"]
     launches_per_step = 5
 
-    def __init__(self, wl, seed, device, stream, score_variant=0):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         self.ctx = kvm.Context(kvm.config_for(wl, index_location=kvm.KVM_DEVICE,
@@ -277,13 +277,13 @@ class HostStep:
     parts = ["step"]
     launches_per_step = 0   # counted from the step statistics
 
-    def __init__(self, wl, seed, device, stream, score_variant=0):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
                              index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
                              else kvm.KVM_DEVICE, h2d_batch_blocks=256,
-                             score_variant=score_variant)
+                             score_variant=score_variant, h2d_mode=h2d_mode)
         self.ctx = kvm.Context(cfg, device=device, stream=stream)
         (self.raw_h, self.v_h, self.index, self.planted, u, _, _) = build_host_workspace(
             kvm, wl, seed, device, stream, self.ctx, wl.n_blocks, wl.index_loc == "host")
@@ -347,13 +347,13 @@ class ChurnStep:
     launches_per_step = 0
     per_step_inputs = True
 
-    def __init__(self, wl, seed, device, stream, score_variant=0):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         total = wl.n_blocks + wl.steps * wl.append_blocks
         cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
                              index_location=kvm.KVM_DEVICE, h2d_batch_blocks=256,
-                             score_variant=score_variant)
+                             score_variant=score_variant, h2d_mode=h2d_mode)
         self.ctx = kvm.Context(cfg, device=device, stream=stream)
         (self.raw_h, self.v_h, self.index, self.planted, self.u, self.topic_of,
          self.new_pages) = build_host_workspace(kvm, wl, seed, device, stream, self.ctx, total,
@@ -459,7 +459,8 @@ def bench_ours(args, wl, world, rank, local, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     kind = STEP_KIND.get(wl.name.split("@")[0], Step)
-    step = kind(wl, args.seed + rank, dev, stream, score_variant=args.score_variant)
+    step = kind(wl, args.seed + rank, dev, stream, score_variant=args.score_variant,
+                h2d_mode=args.h2d_mode)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize(dev)
@@ -746,6 +747,8 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--score-variant", type=int, default=0,
                     help="0: tensor-core scoring where supported, 1: CUDA cores")
+    ap.add_argument("--h2d-mode", type=int, default=1,
+                    help="host-resident repository: 0 copy engine, 1 GPU reads the host memory")
     ap.add_argument("--blocks", type=int, default=0,
                     help="override the history length (small cases for profiling)")
     args = ap.parse_args()

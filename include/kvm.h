@@ -77,6 +77,13 @@ typedef struct {
     int32_t index_location;  /* KVM_DEVICE or KVM_HOST_PINNED (kvm_step, kvm_score_select) */
     int32_t repo_location;   /* where kvm_step finds raw K / V of the history  */
     int32_t h2d_batch_blocks;/* missed blocks per pipelined H2D batch (kvm_step) */
+    int32_t h2d_mode;        /* kvm_step with a host-resident repository:
+                                0: copy engine -- coalesced cudaMemcpyAsync of each run of
+                                   missed blocks into its pages, batch by batch;
+                                1: the GPU reads the missed blocks from the pinned host
+                                   repository itself (one fused kernel: raw K, re-RoPE'd K
+                                   and V into the page); needs the repository pinned and
+                                   device-mapped */
     int32_t score_variant;   /* 0: tcgen05 tensor cores for bf16 q/index (d 64 or 128,
                                 <= 256 query rows per KV head), CUDA cores otherwise;
                                 1: CUDA cores always */

@@ -34,8 +34,11 @@ _TDT = {KVM_F32: torch.float32, KVM_BF16: torch.bfloat16}
 def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: int | None = None,
                pool_pages: int | None = None, index_location: int | None = None,
                repo_location: int | None = None, h2d_batch_blocks: int = 64,
-               max_queries: int | None = None, score_variant: int = 0) -> KvmConfig:
-    """A kvm_config for a workload shape."""
+               max_queries: int | None = None, score_variant: int = 0,
+               h2d_mode: int = 1) -> KvmConfig:
+    """A kvm_config for a workload shape.  With a host-resident repository the
+    GPU reads missed blocks from pinned host memory itself (h2d_mode 1) unless
+    h2d_mode=0 asks for copy-engine transfers."""
     mb = max_blocks if max_blocks is not None else wl.n_blocks + wl.steps * wl.append_blocks
     mp = max_positions if max_positions is not None else max(mb, wl.view_blocks) * BLOCK_TOKENS
     il = index_location if index_location is not None else (
@@ -51,7 +54,7 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         max_positions=mp, tile_blocks=wl.tile_blocks,
         pool_pages=pool_pages if pool_pages is not None else wl.view_blocks + wl.append_blocks,
         index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
-        score_variant=score_variant)
+        h2d_mode=h2d_mode, score_variant=score_variant)
 
 
 def _ptr(t) -> int | None:

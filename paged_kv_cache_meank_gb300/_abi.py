@@ -29,7 +29,7 @@ class KvmConfig(ctypes.Structure):
         ("max_positions", ctypes.c_int64), ("tile_blocks", ctypes.c_int32),
         ("pool_pages", ctypes.c_int32), ("index_location", ctypes.c_int32),
         ("repo_location", ctypes.c_int32), ("h2d_batch_blocks", ctypes.c_int32),
-        ("score_variant", ctypes.c_int32),
+        ("h2d_mode", ctypes.c_int32), ("score_variant", ctypes.c_int32),
     ]
 
 

@@ -29,7 +29,7 @@ struct SlotWork {
     __device__ static void run(const T *__restrict__ src_k, const T *__restrict__ src_v,
                                T *__restrict__ dst_k, T *__restrict__ dst_v, int64_t pos0,
                                int lg0, int lg1, const float2 *__restrict__ table,
-                               float2 *tab) {
+                               float2 *tab, T *__restrict__ dst_raw = nullptr) {
         const int tid = threadIdx.x;
         const int tok = tid / TPT, c = tid % TPT;
         const float2 *trow = table + pos0 * HD;
@@ -65,6 +65,10 @@ struct SlotWork {
             }
             st_stream(dst_k + off, VecTraits<T>::pack(ox));
             st_stream(dst_k + off + HD, VecTraits<T>::pack(oy));
+            if (dst_raw != nullptr) {
+                st_stream(dst_raw + off, vx);
+                st_stream(dst_raw + off + HD, vy);
+            }
             if (do_v) {
                 st_stream(dst_v + off, wx);
                 st_stream(dst_v + off + HD, wy);
@@ -108,7 +112,7 @@ assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
     const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
     SlotWork<T, D>::run(static_cast<const T *>(sd.src_k), static_cast<const T *>(sd.src_v),
                         static_cast<T *>(sd.dst_k), static_cast<T *>(sd.dst_v), sd.pos0, lg0,
-                        lg1, table, tab);
+                        lg1, table, tab, static_cast<T *>(sd.dst_raw));
 }
 
 static int lg_split(int n_slots, int LG) {

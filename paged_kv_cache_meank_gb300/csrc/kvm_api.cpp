@@ -83,6 +83,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->pool_pages < c->view_blocks) return bad("pool_pages must be >= view_blocks");
     if (c->h2d_batch_blocks < 1) return bad("h2d_batch_blocks must be >= 1");
     if (c->score_variant != 0 && c->score_variant != 1) return bad("score_variant must be 0 or 1");
+    if (c->h2d_mode != 0 && c->h2d_mode != 1) return bad("h2d_mode must be 0 or 1");
     return true;
 }
 
@@ -134,6 +135,8 @@ struct kvm_ctx {
     std::vector<cudaEvent_t> ev_batch;
     bool bound = false;
     kvm_buffers bufs{};
+    const void *repo_k_dev = nullptr;   // repository as the GPU addresses it
+    const void *repo_v_dev = nullptr;
     // residency of the page pool
     std::vector<int64_t> block_of_page;
     std::vector<int64_t> baked_pos;
@@ -406,6 +409,23 @@ kvm_status kvm_bind(kvm_ctx *c, const kvm_buffers *b) {
         return fail(KVM_ERR_INVALID_ARG, "a required buffer is NULL");
     if (c->cfg.repo_location == KVM_HOST_PINNED && !b->pool_raw_k)
         return fail(KVM_ERR_INVALID_ARG, "pool_raw_k is required with a host-resident repository");
+    c->repo_k_dev = b->raw_k;
+    c->repo_v_dev = b->v;
+    if (c->cfg.repo_location == KVM_HOST_PINNED && c->cfg.h2d_mode == 1) {
+        // device addresses of the pinned host repository (the same pointer under
+        // unified addressing; an error if the memory is not pinned and mapped)
+        void *dk = nullptr, *dv = nullptr;
+        cudaError_t e = cudaHostGetDevicePointer(&dk, const_cast<void *>(b->raw_k), 0);
+        if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, const_cast<void *>(b->v), 0);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(KVM_ERR_INVALID_ARG,
+                        "h2d_mode 1 needs a pinned, device-mapped repository: %s",
+                        cudaGetErrorString(e));
+        }
+        c->repo_k_dev = dk;
+        c->repo_v_dev = dv;
+    }
     c->bufs = *b;
     c->bound = true;
     reset_pool(c);
@@ -468,6 +488,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
 
     const size_t blk = block_bytes(cfg);
     const bool host_repo = cfg.repo_location == KVM_HOST_PINNED;
+    const bool pull = host_repo && cfg.h2d_mode == 1;
     auto P_k = [&](int p) { return static_cast<char *>(c->bufs.pool_k) + (size_t)p * blk; };
     auto P_v = [&](int p) { return static_cast<char *>(c->bufs.pool_v) + (size_t)p * blk; };
     auto P_r = [&](int p) { return static_cast<char *>(c->bufs.pool_raw_k) + (size_t)p * blk; };
@@ -495,7 +516,14 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         miss_slots.push_back(j);
         const int p = page_of_slot[j];
         kvm::SlotDesc d{};
-        if (host_repo) {
+        if (host_repo && pull) {
+            // the kernel reads the block from the pinned host repository itself and
+            // writes the page's raw K, its K at the slot's positions and its V
+            d.src_k = static_cast<const char *>(c->repo_k_dev) + (size_t)sel[j] * blk;
+            d.src_v = static_cast<const char *>(c->repo_v_dev) + (size_t)sel[j] * blk;
+            d.dst_v = P_v(p);
+            d.dst_raw = P_r(p);
+        } else if (host_repo) {
             d.src_k = P_r(p);
         } else {
             d.src_k = R_k(sel[j]);
@@ -522,7 +550,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
                                  cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return abort_step(cuda_fail(e, "descriptor upload"));
     }
-    if (!host_repo) {
+    if (!host_repo || pull) {
         if (n_rope > 0) {
             if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
             if ((e = kvm::launch_assemble_desc(cfg.kv_dtype, cfg.head_dim, c->desc_dev, n_rope, LG,
@@ -602,7 +630,8 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         stats->reroped = n_rope;
         stats->evicted = evicted;
         stats->h2d_copies = h2d_copies;
-        stats->h2d_bytes = h2d_bytes;
+        // bytes that crossed the host link: by copy engine, or read by the kernel
+        stats->h2d_bytes = pull ? 2 * (int64_t)miss_slots.size() * (int64_t)blk : h2d_bytes;
     }
     return KVM_OK;
 }

@@ -32,6 +32,7 @@ struct SlotDesc {
     const void *src_v;
     void *dst_k;
     void *dst_v;
+    void *dst_raw;      // nullable: also store the raw K as read (a page's raw-K copy)
     int64_t pos0;
 };
 

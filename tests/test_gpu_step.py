@@ -23,7 +23,7 @@ def kvm():
 
 
 def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_step,
-               pool_extra=6, batch=7):
+               pool_extra=6, batch=7, h2d_mode=0):
     from paged_kv_cache_meank_gb300 import workload
     N_max = max(n_blocks_per_step)
     ws = workload.make_workspace(wl, seed=11, n_blocks=N_max, with_q=False)
@@ -34,7 +34,7 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
         wl, max_blocks=N_max, pool_pages=wl.view_blocks + pool_extra,
         repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
         index_location=kvm.KVM_HOST_PINNED if index_host else kvm.KVM_DEVICE,
-        h2d_batch_blocks=batch)
+        h2d_batch_blocks=batch, h2d_mode=h2d_mode)
     cfg.tile_blocks = 64
     ctx = kvm.Context(cfg)
     # (a) the GPU builds the index and raw K from the prefill K pages
@@ -105,8 +105,9 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
     return history
 
 
-@pytest.mark.parametrize("repo_host", [False, True], ids=["repo-device", "repo-host"])
-def test_step_sequence(kvm, repo_host):
+@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 0), (True, 1)],
+                         ids=["repo-device", "repo-host-copy-engine", "repo-host-gpu-pull"])
+def test_step_sequence(kvm, repo_host, h2d_mode):
     from paged_kv_cache_meank_gb300 import workload
     wl = MID
     g = torch.Generator().manual_seed(21)
@@ -115,7 +116,7 @@ def test_step_sequence(kvm, repo_host):
     qb = workload.make_queries(wl, g, "cpu", u[1])
     qs = [qa, qb, qb, qa]
     ns = [260, 280, 280, 300]   # the history grows between steps
-    hist = _run_steps(kvm, wl, repo_host, False, qs, ns)
+    hist = _run_steps(kvm, wl, repo_host, False, qs, ns, h2d_mode=h2d_mode)
     assert hist[0]["misses"] == wl.view_blocks and hist[0]["hits"] == 0
     # same queries, same history: every block is a hit and nothing moves
     assert hist[2]["misses"] == 0 and hist[2]["reroped"] == 0
