@@ -5,100 +5,115 @@
 // position-independent K; §5 (incremental indexing): the mean is taken while the
 // block's K pages are still on the GPU, RoPE removed first.
 //
-// One CTA owns one block and a run of (layer, kv head) pairs.  The block's 32
-// rows of the cos/sin table are staged in shared memory once and reused for
-// every pair.  Each thread moves 16 bytes of the first half of a token row and
-// the matching 16 bytes of the second half (rotate-half partners), un-rotates
-// them in float32, optionally writes the raw K, and the 32 tokens are summed
-// with warp shuffles plus one shared-memory pass across warps.  HBM traffic per
-// (layer, kv head, block): 32*d elements read, 32*d written (raw K), d written.
+// One CTA owns one block and a run of (layer, kv head) pairs; the block's 32
+// rows of the cos/sin table are staged in shared memory once.  Each warp then
+// owns whole (layer, kv head) pairs, so no CTA barrier sits in the streaming
+// loop: a lane owns 16 bytes of the first half of a token row and the matching
+// 16 bytes of the second half (rotate-half partners) for a fixed column slice,
+// walks its share of the 32 tokens with all loads issued up front (256 bytes
+// in flight per lane), un-rotates them in float32, optionally writes the raw
+// K, and keeps the token sum in registers; two shuffle rounds finish the sum
+// across the lanes that share a column slice.  HBM traffic per (layer, kv
+// head, block): 32*d elements read, 32*d written (raw K), d written.
 #include "kvm_internal.cuh"
 #include "kvm_vec.cuh"
 
 namespace kvm {
 
+constexpr int kMeanKWarps = 4;
+
 template <typename T, typename TI, int D>
-__global__ void __launch_bounds__(32 * (D / 2) / VecTraits<T>::N)
+__global__ void __launch_bounds__(kMeanKWarps * 32, 6)
 meank_kernel(const T *__restrict__ k_pages, T *__restrict__ raw_out, TI *__restrict__ index,
              int64_t index_cap, int64_t first_block, int LG, int lg_per_cta,
              const float2 *__restrict__ table) {
-    constexpr int PPT = VecTraits<T>::N;   // rotation pairs per thread
+    constexpr int PPT = VecTraits<T>::N;     // rotation pairs per 16-byte vector
     constexpr int HD = D / 2;
-    constexpr int TPT = HD / PPT;          // threads per token row
-    constexpr int NT = 32 * TPT;
-    constexpr int NW = NT / 32;
-    __shared__ float2 tab[kBlockTokens * HD];
-    __shared__ float red[NW][D];
+    constexpr int TPT = HD / PPT;            // lanes per token row
+    constexpr int TOK = 32 / TPT;            // tokens per warp-wide sweep
+    constexpr int ITERS = 32 / TOK;          // sweeps over the block's 32 tokens
+    constexpr int GROUP = ITERS < 4 ? ITERS : 4;   // sweeps with loads in flight together
+    // cos/sin of (token, column slice): PPT pairs padded by 2 so that the eight
+    // lanes of one shared-memory phase hit distinct banks
+    constexpr int ROW = PPT + 2;
+    __shared__ __align__(16) float2 tab[kBlockTokens * TPT * ROW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tok = tid / TPT, c = tid % TPT;
+    const int c = lane % TPT, t0 = lane / TPT;
     const int64_t b = blockIdx.x;
     const int64_t gb = first_block + b;
 
     const float2 *trow = table + gb * kBlockTokens * HD;
-    for (int i = tid; i < kBlockTokens * HD; i += NT) tab[i] = trow[i];
-    __syncthreads();
-    float cs[PPT], sn[PPT];
-#pragma unroll
-    for (int i = 0; i < PPT; ++i) {
-        const float2 t = tab[tok * HD + c * PPT + i];
-        cs[i] = t.x;
-        sn[i] = t.y;
+    for (int i = tid; i < kBlockTokens * HD; i += kMeanKWarps * 32) {
+        const int t = i / HD, j = i - t * HD;
+        tab[(t * TPT + j / PPT) * ROW + j % PPT] = trow[i];
     }
+    __syncthreads();
 
     const int lg0 = blockIdx.y * lg_per_cta;
     const int lg1 = min(LG, lg0 + lg_per_cta);
-    const size_t row = (size_t)tok * D + (size_t)c * PPT;
-    auto base_of = [&](int lg) { return ((size_t)b * LG + lg) * kBlockTokens * D; };
-
-    uint4 nx = make_uint4(0, 0, 0, 0), ny = nx;
-    if (lg0 < lg1) {
-        nx = ld_stream(k_pages + base_of(lg0) + row);
-        ny = ld_stream(k_pages + base_of(lg0) + row + HD);
-    }
-    for (int lg = lg0; lg < lg1; ++lg) {
-        const uint4 vx = nx, vy = ny;
-        if (lg + 1 < lg1) {  // keep the next pair's loads in flight
-            nx = ld_stream(k_pages + base_of(lg + 1) + row);
-            ny = ld_stream(k_pages + base_of(lg + 1) + row + HD);
-        }
-        float x[PPT], y[PPT], rx[PPT], ry[PPT];
-        VecTraits<T>::unpack(vx, x);
-        VecTraits<T>::unpack(vy, y);
+    for (int lg = lg0 + warp; lg < lg1; lg += kMeanKWarps) {
+        const size_t base = ((size_t)b * LG + lg) * kBlockTokens * D;
+        const T *src = k_pages + base;
+        float ax[PPT], ay[PPT];
 #pragma unroll
-        for (int i = 0; i < PPT; ++i) {
-            // R_{-p}: (x cos + y sin, y cos - x sin), each product rounded
-            rx[i] = __fadd_rn(__fmul_rn(x[i], cs[i]), __fmul_rn(y[i], sn[i]));
-            ry[i] = __fsub_rn(__fmul_rn(y[i], cs[i]), __fmul_rn(x[i], sn[i]));
-        }
-        if (raw_out != nullptr) {
-            st_stream(raw_out + base_of(lg) + row, VecTraits<T>::pack(rx));
-            st_stream(raw_out + base_of(lg) + row + HD, VecTraits<T>::pack(ry));
+        for (int k = 0; k < PPT; ++k) ax[k] = ay[k] = 0.f;
+#pragma unroll
+        for (int g0 = 0; g0 < ITERS; g0 += GROUP) {
+            uint4 vx[GROUP], vy[GROUP];
+#pragma unroll
+            for (int i = 0; i < GROUP; ++i) {
+                const int t = t0 + (g0 + i) * TOK;
+                const size_t off = (size_t)t * D + (size_t)c * PPT;
+                vx[i] = ld_stream(src + off);
+                vy[i] = ld_stream(src + off + HD);
+            }
+#pragma unroll
+            for (int i = 0; i < GROUP; ++i) {
+                const int t = t0 + (g0 + i) * TOK;
+                float x[PPT], y[PPT], rx[PPT], ry[PPT];
+                VecTraits<T>::unpack(vx[i], x);
+                VecTraits<T>::unpack(vy[i], y);
+                const float4 *cs4 = reinterpret_cast<const float4 *>(tab + (t * TPT + c) * ROW);
+                float2 cw[PPT];
+#pragma unroll
+                for (int k = 0; k < PPT / 2; ++k) {
+                    const float4 w4 = cs4[k];
+                    cw[2 * k] = make_float2(w4.x, w4.y);
+                    cw[2 * k + 1] = make_float2(w4.z, w4.w);
+                }
+#pragma unroll
+                for (int k = 0; k < PPT; ++k) {
+                    const float2 w = cw[k];
+                    // R_{-p}: (x cos + y sin, y cos - x sin), each product rounded
+                    rx[k] = __fadd_rn(__fmul_rn(x[k], w.x), __fmul_rn(y[k], w.y));
+                    ry[k] = __fsub_rn(__fmul_rn(y[k], w.x), __fmul_rn(x[k], w.y));
+                    ax[k] += rx[k];
+                    ay[k] += ry[k];
+                }
+                if (raw_out != nullptr) {
+                    const size_t off = base + (size_t)t * D + (size_t)c * PPT;
+                    st_stream(raw_out + off, VecTraits<T>::pack(rx));
+                    st_stream(raw_out + off + HD, VecTraits<T>::pack(ry));
+                }
+            }
         }
 #pragma unroll
         for (int off = TPT; off < 32; off <<= 1) {
 #pragma unroll
-            for (int i = 0; i < PPT; ++i) {
-                rx[i] += __shfl_xor_sync(0xffffffffu, rx[i], off);
-                ry[i] += __shfl_xor_sync(0xffffffffu, ry[i], off);
+            for (int k = 0; k < PPT; ++k) {
+                ax[k] += __shfl_xor_sync(0xffffffffu, ax[k], off);
+                ay[k] += __shfl_xor_sync(0xffffffffu, ay[k], off);
             }
         }
         if (lane < TPT) {
+            TI *dst = index + ((size_t)lg * index_cap + gb) * D + (size_t)c * PPT;
 #pragma unroll
-            for (int i = 0; i < PPT; ++i) {
-                red[warp][c * PPT + i] = rx[i];
-                red[warp][HD + c * PPT + i] = ry[i];
+            for (int k = 0; k < PPT; ++k) {
+                dst[k] = from_float<TI>(ax[k] * (1.0f / kBlockTokens));
+                dst[HD + k] = from_float<TI>(ay[k] * (1.0f / kBlockTokens));
             }
         }
-        __syncthreads();
-        if (tid < D) {
-            float s = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) s += red[w][tid];
-            index[((size_t)lg * index_cap + gb) * D + tid] =
-                from_float<TI>(s * (1.0f / kBlockTokens));
-        }
-        __syncthreads();
     }
 }
 
@@ -106,16 +121,16 @@ template <typename T, typename TI, int D>
 static cudaError_t launch_meank_t(const void *k_pages, void *raw_out, void *index,
                                   int64_t index_cap, int64_t first_block, int64_t n_blocks,
                                   int LG, const float2 *table, cudaStream_t s) {
-    constexpr int NT = 32 * (D / 2) / VecTraits<T>::N;
-    // enough CTAs per block to fill the machine for small runs, long runs of
-    // (layer, kv head) pairs per CTA to amortise the table stage otherwise
+    // long runs of (layer, kv head) pairs per CTA amortise the table stage; short
+    // ones keep the machine full when few blocks are built
     int lg_per_cta = LG;
     const int64_t want_ctas = 152 * 16;
-    while (lg_per_cta > 8 && n_blocks * ((LG + lg_per_cta - 1) / lg_per_cta) < want_ctas)
+    while (lg_per_cta > kMeanKWarps &&
+           n_blocks * ((LG + lg_per_cta - 1) / lg_per_cta) < want_ctas)
         lg_per_cta = (lg_per_cta + 1) / 2;
-    if (lg_per_cta > 64) lg_per_cta = 64;
+    if (lg_per_cta > 8 * kMeanKWarps) lg_per_cta = 8 * kMeanKWarps;
     dim3 grid((unsigned)n_blocks, (unsigned)((LG + lg_per_cta - 1) / lg_per_cta));
-    meank_kernel<T, TI, D><<<grid, NT, 0, s>>>(
+    meank_kernel<T, TI, D><<<grid, kMeanKWarps * 32, 0, s>>>(
         static_cast<const T *>(k_pages), static_cast<T *>(raw_out), static_cast<TI *>(index),
         index_cap, first_block, LG, lg_per_cta, table);
     return cudaGetLastError();

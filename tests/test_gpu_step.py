@@ -138,7 +138,8 @@ def test_step_failure_injection(kvm):
     from paged_kv_cache_meank_gb300 import workload
     wl = MID.with_(n_blocks=200, view_blocks=40)
     ws = workload.make_workspace(wl, seed=13)
-    ctx = kvm.Context(kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED, h2d_batch_blocks=5))
+    ctx = kvm.Context(kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED, h2d_batch_blocks=5,
+                                     h2d_mode=0))       # copy-engine transfers can fail
     kp = prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
     raw_d = torch.empty(ctx.block_shape(200), dtype=torch.bfloat16, device="cuda")
