@@ -8,14 +8,14 @@
 // fp32 and the tensor cores accumulate in fp32, so only the summation order
 // differs from the CUDA-core variant.
 //
-// CTA = 10 warps, one SM (the shared-memory ring and the 512 TMEM columns):
+// CTA = 18 warps, one SM (the shared-memory ring and the 512 TMEM columns):
 //   warp 0       TMA producer: 128-block index tiles into a 4-stage ring of
 //                128-byte-swizzled shared memory (one copy per 64-element K atom)
 //   warp 1       MMA issuer: one thread issues tcgen05.mma into one of two TMEM
 //                accumulators and commits to mbarriers
-//   warps 2..9   epilogue, two warps per TMEM lane quadrant, each taking half
-//                of the accumulator's columns; the pair combines through
-//                shared memory, handed over with an mbarrier
+//   warps 2..17  epilogue, four warps per TMEM lane quadrant, each taking a
+//                quarter of the accumulator's columns; the four combine in a
+//                fixed order through shared memory, handed over with mbarriers
 // Pass 1 computes D[query row][block] (M = 128 query rows per tile, N = 128
 // blocks): each epilogue thread owns one query row and keeps its running max
 // and rescaled partition sum in registers -- no cross-thread reduction.
@@ -37,7 +37,7 @@ namespace {
 
 constexpr int TB = 128;             // index blocks per tile
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -52,25 +52,62 @@ struct Lay {
     static constexpr int QB = KA * Q_ATOM;
     static constexpr int OFF_Q = kStages * TILE;
     static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
-    static constexpr int OFF_X = OFF_O + kQRows * 4;   // pair exchange, 2 x 4 x 32 x 2 floats
-    static constexpr int OFF_BAR = OFF_X + 2 * 4 * 32 * 2 * 4;
+    static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 2 x 4 x 3 x 32 x 2 floats
+    static constexpr int OFF_BAR = OFF_X + 2 * 4 * 3 * 32 * 2 * 4;
     static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
-// Sum of 2^(v*c - o) over n loaded columns (n a multiple of 16), four partial
-// sums to shorten the dependency chain.
+// Sum of 2^(v*c - o) over n loaded columns (n a multiple of 16, at most 64),
+// four partial sums to shorten the dependency chain.
 __device__ __forceinline__ float exp_sum(const uint32_t *r, const float *o, int n, float c) {
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-    for (int k = 0; k < 128; k += 4) {
+    for (int k = 0; k < 64; k += 4) {
         if (k < n) {
-            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -o[k]));
-            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -o[k + 1]));
-            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -o[k + 2]));
-            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), c, -o[k + 3]));
+            const float4 o4 = *reinterpret_cast<const float4 *>(o + k);
+            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -o4.x));
+            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -o4.y));
+            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -o4.z));
+            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), c, -o4.w));
         }
     }
     return (s0 + s1) + (s2 + s3);
+}
+
+// Online softmax statistics of one query row over the first nv of 32 loaded
+// scores: running max m (log2 units) and the partition sum z rescaled to it.
+__device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c, float &m,
+                                              float &z) {
+    if (nv <= 0) return;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    if (nv == 32) {
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+            mx0 = fmaxf(mx0, __uint_as_float(r[k]));
+            mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
+    }
+    const float mn = fmaxf(m, fmaxf(mx0, mx1) * c);
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    if (nv == 32) {
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
+            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -mn));
+            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -mn));
+            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), c, -mn));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
+    }
+    z = z * fast_exp2(m - mn) + ((s0 + s1) + (s2 + s3));
+    m = mn;
 }
 
 }  // namespace
@@ -88,12 +125,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     uint8_t *tiles = smem;
     uint8_t *qs = smem + LY::OFF_Q;
     float *o_r = reinterpret_cast<float *>(smem + LY::OFF_O);
-    float *xch = reinterpret_cast<float *>(smem + LY::OFF_X);   // [2][4][32][2]
+    float *xch = reinterpret_cast<float *>(smem + LY::OFF_X);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
-    uint64_t *xfull = tempty + 2;        // [2][4]: half 1 of a pair has written its partials
+    uint64_t *xfull = tempty + 2;        // [2][4]: warps 1..3 of a quadrant wrote their partials
     uint64_t *xfin = xfull + 8;          // [4]: the same for the final pass-1 statistics
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfin + 4);
 
@@ -117,8 +154,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], kEpiWarps * 32);
         }
-        for (int k = 0; k < 8; ++k) tc::mbar_init(&xfull[k], 32);
-        for (int k = 0; k < 4; ++k) tc::mbar_init(&xfin[k], 32);
+        for (int k = 0; k < 8; ++k) tc::mbar_init(&xfull[k], 96);
+        for (int k = 0; k < 4; ++k) tc::mbar_init(&xfin[k], 96);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -215,16 +252,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             }
         }
     } else {
-        const int ew = warp - 2;                    // 0..7
+        const int ew = warp - 2;                    // 0..15
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
-        const int half = ew >> 2;                   // which half of the columns
+        const int sub = ew >> 2;                    // which quarter of the columns
         const int lrow = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        // pass-2 column split: half 0 takes the first ceil(n2/2) columns rounded
-        // up to 16, half 1 the rest
-        const int split = ((n2 / 2) + 15) & ~15;
-        const int my_c0 = PASS == 2 ? (half ? split : 0) : half * 64;
-        const int my_nc = PASS == 2 ? (half ? n2 - split : split) : 64;
+        // pass 2: the n2 columns in 16-column units, split into four near-equal runs
+        const int nu = n2 >> 4;
+        const int u0 = (sub * nu) >> 2, u1 = ((sub + 1) * nu) >> 2;
+        const int my_c0 = PASS == 2 ? u0 * 16 : sub * 32;
+        const int my_nc = PASS == 2 ? (u1 - u0) * 16 : 32;
         float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i & 1;
@@ -235,71 +272,43 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
             const uint32_t taddr = tmem + lane_base + buf * 256;
             if (PASS == 1) {
-                for (int t = 0; t < qtiles; ++t) {
-                    uint32_t r[64];
-                    tc::tmem_ld32_async(taddr + t * 128 + my_c0, r);
-                    tc::tmem_ld32_async(taddr + t * 128 + my_c0 + 32, r + 32);
-                    tc::tmem_wait_ld(r);
-                    tc::tmem_wait_ld(r + 16);
+                // this warp's 32 columns of each query-row tile, both loads in flight
+                uint32_t r[64];
+                tc::tmem_ld32_async(taddr + my_c0, r);
+                if (qtiles > 1) tc::tmem_ld32_async(taddr + 128 + my_c0, r + 32);
+                tc::tmem_wait_ld(r);
+                tc::tmem_wait_ld(r + 16);
+                if (qtiles > 1) {
                     tc::tmem_wait_ld(r + 32);
                     tc::tmem_wait_ld(r + 48);
-                    const int nv = min(64, max(0, nvalid - my_c0));
-                    if (nv == 64) {
-                        float c0 = -INFINITY, c1 = -INFINITY;
-#pragma unroll
-                        for (int k = 0; k < 64; k += 2) {
-                            c0 = fmaxf(c0, __uint_as_float(r[k]));
-                            c1 = fmaxf(c1, __uint_as_float(r[k + 1]));
-                        }
-                        const float mn = fmaxf(m_run[t], fmaxf(c0, c1) * scale_log2);
-                        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 64; k += 4) {
-                            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), scale_log2, -mn));
-                            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), scale_log2, -mn));
-                            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), scale_log2, -mn));
-                            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), scale_log2, -mn));
-                        }
-                        z_run[t] = z_run[t] * fast_exp2(m_run[t] - mn) + ((s0 + s1) + (s2 + s3));
-                        m_run[t] = mn;
-                    } else if (nv > 0) {
-                        float cmax = -INFINITY;
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (k < nv) cmax = fmaxf(cmax, __uint_as_float(r[k]));
-                        const float mn = fmaxf(m_run[t], cmax * scale_log2);
-                        float zs = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (k < nv) zs += fast_exp2(fmaf(__uint_as_float(r[k]), scale_log2, -mn));
-                        z_run[t] = z_run[t] * fast_exp2(m_run[t] - mn) + zs;
-                        m_run[t] = mn;
-                    }
                 }
+                const int nv = min(32, max(0, nvalid - my_c0));
+                for (int t = 0; t < qtiles; ++t)
+                    online_update(r + 32 * t, nv, scale_log2, m_run[t], z_run[t]);
             } else {
-                uint32_t r[128];
+                uint32_t r[64];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 2; ++k) {
                     if (k * 32 + 32 <= my_nc) tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
                     else if (k * 32 + 16 <= my_nc) tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int k = 0; k < 4; ++k)
                     if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
                 float sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
-                // pair combine: half 1 hands its partial to half 0 through shared memory
-                // (half 1 cannot reuse this slot before half 0 has read it: the
-                // tile two steps ahead needs half 0's arrival on tempty[buf])
-                float *slot = xch + ((buf * 4 + quad) * 32 + lane) * 2;
-                if (half) {
-                    slot[0] = sum;
+                // the quadrant's four warps combine in a fixed order through shared
+                // memory (a slot is not reused before warp 0 of the quadrant read it:
+                // the tile two steps ahead needs that warp's arrival on tempty[buf])
+                float *slot = xch + ((buf * 4 + quad) * 3) * 32 + lane;
+                if (sub) {
+                    slot[(sub - 1) * 32] = sum;
                     tc::mbar_arrive(&xfull[buf * 4 + quad]);
                 } else {
                     if (!tc::mbar_wait(&xfull[buf * 4 + quad], bph, kWaitLimit)) {
                         atomicOr(err, 4);
                         break;
                     }
-                    sum += slot[0];
+                    sum = ((sum + slot[0]) + slot[32]) + slot[64];
                     if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
                 }
             }
@@ -307,22 +316,26 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             tc::mbar_arrive(&tempty[buf]);
         }
         if (PASS == 1) {
-            float *slot = xch + (quad * 32 + lane) * 2;        // [t][4][32][2]
-            if (half) {
+            // [t][quad][sub-1][lane] (m, z)
+            float *slot = xch + ((quad * 3) * 32 + lane) * 2;
+            if (sub) {
                 for (int t = 0; t < qtiles; ++t) {
-                    slot[t * 4 * 32 * 2] = m_run[t];
-                    slot[t * 4 * 32 * 2 + 1] = z_run[t];
+                    slot[(t * 12 + sub - 1) * 64] = m_run[t];
+                    slot[(t * 12 + sub - 1) * 64 + 1] = z_run[t];
                 }
                 tc::mbar_arrive(&xfin[quad]);
             } else if (!tc::mbar_wait(&xfin[quad], 0, kWaitLimit)) {
                 atomicOr(err, 4);
             } else {
                 for (int t = 0; t < qtiles; ++t) {
-                    const float m1 = slot[t * 4 * 32 * 2], z1 = slot[t * 4 * 32 * 2 + 1];
-                    const float M = fmaxf(m_run[t], m1);
+                    float M = m_run[t];
+                    for (int k = 0; k < 3; ++k) M = fmaxf(M, slot[(t * 12 + k) * 64]);
                     float Z = 0.f;
-                    if (M != -INFINITY)
-                        Z = z_run[t] * fast_exp2(m_run[t] - M) + z1 * fast_exp2(m1 - M);
+                    if (M != -INFINITY) {
+                        Z = z_run[t] * fast_exp2(m_run[t] - M);
+                        for (int k = 0; k < 3; ++k)
+                            Z += slot[(t * 12 + k) * 64 + 1] * fast_exp2(slot[(t * 12 + k) * 64] - M);
+                    }
                     const int r = t * 128 + lrow;
                     if (r < rows) {
                         const size_t o = ((size_t)lg * sh.chunk_cap + chunk0 + chunk) * rows + r;
