@@ -53,7 +53,8 @@ struct Lay {
     static constexpr int OFF_Q = kStages * TILE;
     static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
     static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 2 x 4 x 3 x 32 x 2 floats
-    static constexpr int OFF_BAR = OFF_X + 2 * 4 * 3 * 32 * 2 * 4;
+    static constexpr int OFF_D = OFF_X + 2 * 4 * 3 * 32 * 2 * 4;   // 2 x 32 x 2 floats
+    static constexpr int OFF_BAR = OFF_D + 2 * 32 * 2 * 4;
     static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
@@ -74,28 +75,29 @@ __device__ __forceinline__ float exp_sum(const uint32_t *r, const float *o, int 
     return (s0 + s1) + (s2 + s3);
 }
 
-// Online softmax statistics of one query row over the first nv of 32 loaded
+// Online softmax statistics of one query row over the first nv of NV loaded
 // scores: running max m (log2 units) and the partition sum z rescaled to it.
+template <int NV>
 __device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c, float &m,
                                               float &z) {
     if (nv <= 0) return;
     float mx0 = -INFINITY, mx1 = -INFINITY;
-    if (nv == 32) {
+    if (nv == NV) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
+        for (int k = 0; k < NV; k += 2) {
             mx0 = fmaxf(mx0, __uint_as_float(r[k]));
             mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
+        for (int k = 0; k < NV; ++k)
             if (k < nv) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
     }
     const float mn = fmaxf(m, fmaxf(mx0, mx1) * c);
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    if (nv == 32) {
+    if (nv == NV) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
+        for (int k = 0; k < NV; k += 4) {
             s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
             s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -mn));
             s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -mn));
@@ -103,7 +105,7 @@ __device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
+        for (int k = 0; k < NV; ++k)
             if (k < nv) s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
     }
     z = z * fast_exp2(m - mn) + ((s0 + s1) + (s2 + s3));
@@ -126,13 +128,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     uint8_t *qs = smem + LY::OFF_Q;
     float *o_r = reinterpret_cast<float *>(smem + LY::OFF_O);
     float *xch = reinterpret_cast<float *>(smem + LY::OFF_X);
+    float *xdup = reinterpret_cast<float *>(smem + LY::OFF_D);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *xfull = tempty + 2;        // [2][4]: warps 1..3 of a quadrant wrote their partials
     uint64_t *xfin = xfull + 8;          // [4]: the same for the final pass-1 statistics
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfin + 4);
+    uint64_t *xdbar = xfin + 4;          // [2]: quadrant 2+q handed its half-row stats to q
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xdbar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lg = blockIdx.y;
@@ -144,6 +148,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     const int n_tiles = cb1 > cb0 ? (int)((cb1 - cb0 + TB - 1) / TB) : 0;
     const int n2 = (rows + 15) & ~15;              // pass-2 N
     const int qtiles = rows > 128 ? 2 : 1;         // pass-1 M tiles
+    // 128 < rows <= 192: the second tile holds rows 128..191 twice (lanes 0-63
+    // and 64-127) so that all four lane quadrants share its columns evenly
+    const bool dup = rows > 128 && rows <= 192;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -156,6 +163,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
         }
         for (int k = 0; k < 8; ++k) tc::mbar_init(&xfull[k], 96);
         for (int k = 0; k < 4; ++k) tc::mbar_init(&xfin[k], 96);
+        for (int k = 0; k < 2; ++k) tc::mbar_init(&xdbar[k], 32);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -166,8 +174,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     for (int i = tid; i < kQRows * (D / 8); i += kThreads) {
         const int r = i / (D / 8), c16 = i - r * (D / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < rows) {
-            const int m = r / sh.gqa, hl = r - m * sh.gqa;
+        const int src_r = (dup && r >= 192) ? r - 64 : r;
+        if (src_r < rows) {
+            const int m = src_r / sh.gqa, hl = src_r - m * sh.gqa;
             const __nv_bfloat16 *src =
                 q + (((size_t)l * sh.n_queries + m) * sh.H + (size_t)g * sh.gqa + hl) * D + c16 * 8;
             v = *reinterpret_cast<const uint4 *>(src);
@@ -262,6 +271,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
         const int u0 = (sub * nu) >> 2, u1 = ((sub + 1) * nu) >> 2;
         const int my_c0 = PASS == 2 ? u0 * 16 : sub * 32;
         const int my_nc = PASS == 2 ? (u1 - u0) * 16 : 32;
+        // pass 1, duplicated second tile: quadrants 0-1 take its columns 0-63,
+        // quadrants 2-3 columns 64-127, sixteen per warp
+        const int c1 = (quad >= 2 ? 64 : 0) + sub * 16;
         float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i & 1;
@@ -275,16 +287,25 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
                 // this warp's 32 columns of each query-row tile, both loads in flight
                 uint32_t r[64];
                 tc::tmem_ld32_async(taddr + my_c0, r);
-                if (qtiles > 1) tc::tmem_ld32_async(taddr + 128 + my_c0, r + 32);
+                if (qtiles > 1) {
+                    if (dup) tc::tmem_ld16_async(taddr + 128 + c1, r + 32);
+                    else tc::tmem_ld32_async(taddr + 128 + my_c0, r + 32);
+                }
                 tc::tmem_wait_ld(r);
                 tc::tmem_wait_ld(r + 16);
                 if (qtiles > 1) {
                     tc::tmem_wait_ld(r + 32);
-                    tc::tmem_wait_ld(r + 48);
+                    if (!dup) tc::tmem_wait_ld(r + 48);
                 }
                 const int nv = min(32, max(0, nvalid - my_c0));
-                for (int t = 0; t < qtiles; ++t)
-                    online_update(r + 32 * t, nv, scale_log2, m_run[t], z_run[t]);
+                online_update<32>(r, nv, scale_log2, m_run[0], z_run[0]);
+                if (qtiles > 1) {
+                    if (dup)
+                        online_update<16>(r + 32, min(16, max(0, nvalid - c1)), scale_log2,
+                                          m_run[1], z_run[1]);
+                    else
+                        online_update<32>(r + 32, nv, scale_log2, m_run[1], z_run[1]);
+                }
             } else {
                 uint32_t r[64];
 #pragma unroll
@@ -327,20 +348,44 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             } else if (!tc::mbar_wait(&xfin[quad], 0, kWaitLimit)) {
                 atomicOr(err, 4);
             } else {
+                float M[2], Z[2];
                 for (int t = 0; t < qtiles; ++t) {
-                    float M = m_run[t];
-                    for (int k = 0; k < 3; ++k) M = fmaxf(M, slot[(t * 12 + k) * 64]);
-                    float Z = 0.f;
-                    if (M != -INFINITY) {
-                        Z = z_run[t] * fast_exp2(m_run[t] - M);
+                    M[t] = m_run[t];
+                    for (int k = 0; k < 3; ++k) M[t] = fmaxf(M[t], slot[(t * 12 + k) * 64]);
+                    Z[t] = 0.f;
+                    if (M[t] != -INFINITY) {
+                        Z[t] = z_run[t] * fast_exp2(m_run[t] - M[t]);
                         for (int k = 0; k < 3; ++k)
-                            Z += slot[(t * 12 + k) * 64 + 1] * fast_exp2(slot[(t * 12 + k) * 64] - M);
+                            Z[t] += slot[(t * 12 + k) * 64 + 1] *
+                                    fast_exp2(slot[(t * 12 + k) * 64] - M[t]);
                     }
-                    const int r = t * 128 + lrow;
+                }
+                auto emit = [&](int r, float m, float z) {
                     if (r < rows) {
                         const size_t o = ((size_t)lg * sh.chunk_cap + chunk0 + chunk) * rows + r;
-                        scr.part_m[o] = M;
-                        scr.part_z[o] = Z;
+                        scr.part_m[o] = m;
+                        scr.part_z[o] = z;
+                    }
+                };
+                emit(lrow, M[0], Z[0]);
+                if (qtiles > 1) {
+                    if (!dup) {
+                        emit(128 + lrow, M[1], Z[1]);
+                    } else if (quad >= 2) {
+                        // the other half of rows 128 + 32*(quad-2) + lane goes to quadrant quad-2
+                        xdup[((quad - 2) * 32 + lane) * 2] = M[1];
+                        xdup[((quad - 2) * 32 + lane) * 2 + 1] = Z[1];
+                        tc::mbar_arrive(&xdbar[quad - 2]);
+                    } else if (!tc::mbar_wait(&xdbar[quad], 0, kWaitLimit)) {
+                        atomicOr(err, 4);
+                    } else {
+                        const float m2 = xdup[(quad * 32 + lane) * 2];
+                        const float z2 = xdup[(quad * 32 + lane) * 2 + 1];
+                        const float Mx = fmaxf(M[1], m2);
+                        float Zx = 0.f;
+                        if (Mx != -INFINITY)
+                            Zx = Z[1] * fast_exp2(M[1] - Mx) + z2 * fast_exp2(m2 - Mx);
+                        emit(128 + lrow, Mx, Zx);
                     }
                 }
             }

@@ -108,6 +108,25 @@ def test_score_select_fewer_queries_and_ragged(kvm, variant):
     check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
 
 
+@pytest.mark.parametrize("n_queries", [21, 32, 40, 42], ids=lambda n: f"rows{n * 6}")
+def test_score_select_query_row_tilings(kvm, n_queries):
+    """Query rows per KV head across the tensor-core tilings: one M = 128 tile
+    (126 rows), the duplicated second tile (129..192 rows) and two full tiles
+    (240, 252 rows)."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=517, view_blocks=50, n_queries=n_queries)
+    ws = workload.make_index_direct(wl, seed=30 + n_queries)
+    ctx = _ctx(kvm, wl)
+    scores = torch.empty(wl.n_blocks, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.score_select(ws.q.cuda(), n_queries, ws.index.cuda(), wl.n_blocks, scores, sel)
+    ctx.sync()
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q, "bf16"), "bf16"),
+                            ora.as_f64(to_np(ws.index, "bf16"), "bf16"), wl.n_blocks)
+    assert_scores_close(scores.cpu().numpy(), R, f"{n_queries * 6} rows")
+    check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+
+
 def test_select_ties_and_small_histories(kvm):
     """Equal Mean-K everywhere: all scores tie and the lowest ids win; histories
     of N <= V_b select everything; N = V_b + 1 leaves out exactly one block."""
