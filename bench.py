@@ -58,6 +58,22 @@ def _dist():
     return 1, 0, 0, None
 
 
+def max_over_ranks(dist, x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself on one rank)."""
+    if dist is None:
+        return float(x)
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if on_gpu else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, blocks_per_rank: int, slowest_ms: float) -> float:
+    """Whole-job scored blocks per second: every rank scores its own workspace
+    (weak scaling), timed by the slowest rank."""
+    return world * blocks_per_rank / (slowest_ms * 1e-3)
+
+
 class Clocks:
     """nvidia-smi samples during the timed region."""
 
@@ -483,11 +499,7 @@ def bench_ours(args, wl, world, rank, local, dist):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, t0.elapsed_time(t1), dev)
     ms = total_ms / K
     parts = {p: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs]))
              for i, p in enumerate(step.parts)}
@@ -523,7 +535,7 @@ def bench_ours(args, wl, world, rank, local, dist):
                                for k in ("hits", "misses", "reroped", "h2d_bytes", "h2d_copies")}
     out = {
         "metric": METRIC,
-        "value": world * wl.n_blocks / (ms * 1e-3),
+        "value": job_throughput(world, wl.n_blocks, ms),
         "unit": "scored blocks/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -624,18 +636,14 @@ def bench_e2e(args, step, dev, stream, world, dist):
         one()
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1) / steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, t0.elapsed_time(t1) / steps, dev)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     if per_step:
         h2d //= wl.steps
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     del devc
     peak = h2d_peak(dev, stream)
-    return {"value": world * wl.n_blocks / (ms * 1e-3), "unit": "scored blocks/s",
+    return {"value": job_throughput(world, wl.n_blocks, ms), "unit": "scored blocks/s",
             "ms_per_step": ms, "steps": steps, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
             "h2d_peak_gbs": peak, "inputs": sorted(host)}
