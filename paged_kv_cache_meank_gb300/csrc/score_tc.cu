@@ -58,21 +58,27 @@ struct Lay {
     static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
-// Sum of 2^(v*c - o) over n loaded columns (n a multiple of 16, at most 64),
-// four partial sums to shorten the dependency chain.
-__device__ __forceinline__ float exp_sum(const uint32_t *r, const float *o, int n, float c) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+// Sum of 2^(v*c + no) over n loaded columns (n a multiple of 16, at most 64;
+// no = minus the row offset).  Arguments and partial sums use the packed
+// float32x2 FMA / add of sm_100-family GPUs, two elements per instruction.
+__device__ __forceinline__ float exp_sum(const uint32_t *r, const float *no, int n, float c) {
+    const float2 c2 = make_float2(c, c);
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 64; k += 4) {
         if (k < n) {
-            const float4 o4 = *reinterpret_cast<const float4 *>(o + k);
-            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -o4.x));
-            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -o4.y));
-            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -o4.z));
-            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), c, -o4.w));
+            const float4 o4 = *reinterpret_cast<const float4 *>(no + k);
+            const float2 x01 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2,
+                make_float2(o4.x, o4.y));
+            const float2 x23 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2,
+                make_float2(o4.z, o4.w));
+            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
         }
     }
-    return (s0 + s1) + (s2 + s3);
+    return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
 // Online softmax statistics of one query row over the first nv of NV loaded
@@ -94,21 +100,27 @@ __device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c
             if (k < nv) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
     }
     const float mn = fmaxf(m, fmaxf(mx0, mx1) * c);
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float zs;
     if (nv == NV) {
+        const float2 c2 = make_float2(c, c), nm2 = make_float2(-mn, -mn);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < NV; k += 4) {
-            s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
-            s1 += fast_exp2(fmaf(__uint_as_float(r[k + 1]), c, -mn));
-            s2 += fast_exp2(fmaf(__uint_as_float(r[k + 2]), c, -mn));
-            s3 += fast_exp2(fmaf(__uint_as_float(r[k + 3]), c, -mn));
+            const float2 x01 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2, nm2);
+            const float2 x23 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2, nm2);
+            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
         }
+        zs = (a0.x + a0.y) + (a1.x + a1.y);
     } else {
+        zs = 0.f;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-            if (k < nv) s0 += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
+            if (k < nv) zs += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
     }
-    z = z * fast_exp2(m - mn) + ((s0 + s1) + (s2 + s3));
+    z = z * fast_exp2(m - mn) + zs;
     m = mn;
 }
 
@@ -191,7 +203,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
                 const size_t k = (size_t)lg * rows + r;
                 o = scr.row_m[k] - log2f(scr.row_invz[k]);   // M + log2 Z, log2 units
             }
-            o_r[r] = o;
+            o_r[r] = -o;                                     // stored negated
         }
     }
     tc::fence_proxy_async_smem();
