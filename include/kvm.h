@@ -183,6 +183,27 @@ typedef struct {
 
 kvm_status kvm_bind(kvm_ctx *ctx, const kvm_buffers *bufs);
 
+/*
+ * Proactive stage-out -- [KVMem] §4.4: once a prefill chunk completes, the KV
+ * of its completed blocks is copied to host memory asynchronously while the GPU
+ * processes the next chunk, so that outgoing blocks already have host copies
+ * when the working set changes (and §5: incremental indexing of the same
+ * blocks with kvm_build_index while their K is still on the GPU).
+ *
+ * Copies raw K and V of blocks first_block .. first_block + n_blocks - 1 from
+ * the device buffers raw_k and v (each [n_blocks][L][G][32][d], kv_dtype; raw_k
+ * is typically kvm_build_index's raw_k_out) into the bound host repository
+ * (kvm_bind's raw_k / v; requires repo_location == KVM_HOST_PINNED).  The
+ * copies run on the context's copy stream after everything already enqueued
+ * on `stream`, so work enqueued on `stream` afterwards overlaps them.  raw_k
+ * and v must stay unchanged until the copies are done: kvm_sync waits for
+ * them, and every later kvm_step orders its reads of the repository after them.
+ * Errors: KVM_ERR_NOT_BOUND, KVM_ERR_INVALID_ARG (no host repository, NULL
+ * buffers), KVM_ERR_CAPACITY (blocks beyond max_blocks).
+ */
+kvm_status kvm_stage_out(kvm_ctx *ctx, const void *raw_k, const void *v, int64_t first_block,
+                         int64_t n_blocks, kvm_stream stream);
+
 /* Forget which blocks the page pool holds (every page empty). */
 kvm_status kvm_reset_pool(kvm_ctx *ctx);
 

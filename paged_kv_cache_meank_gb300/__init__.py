@@ -152,6 +152,12 @@ class Context:
                            pool_raw_k=pool_raw_k, page_table=page_table, scores=scores,
                            sel_ids=sel_ids)
 
+    def stage_out(self, raw_k, v, first_block: int, n_blocks: int, stream=None) -> None:
+        """kvm_stage_out: copy completed blocks' raw K / V into the bound host
+        repository, overlapped with later work on `stream`."""
+        check(self.lib.kvm_stage_out(self.handle, _ptr(raw_k), _ptr(v), first_block, n_blocks,
+                                     _stream(stream)), "kvm_stage_out")
+
     def reset_pool(self) -> None:
         check(self.lib.kvm_reset_pool(self.handle), "kvm_reset_pool")
 

@@ -68,6 +68,8 @@ SIGNATURES = {
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "kvm_bind": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(KvmBuffers)]),
     "kvm_reset_pool": (ctypes.c_int, [ctypes.c_void_p]),
+    "kvm_stage_out": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "kvm_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                 ctypes.c_int64, ctypes.POINTER(KvmStepStats), ctypes.c_void_p]),
     "kvm_score_select_static": (ctypes.c_int, [ctypes.POINTER(KvmConfig), ctypes.c_void_p,

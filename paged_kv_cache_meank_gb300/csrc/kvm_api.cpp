@@ -132,6 +132,8 @@ struct kvm_ctx {
     cudaEvent_t ev_ready[2] = {nullptr, nullptr};
     cudaEvent_t ev_free[2] = {nullptr, nullptr};
     cudaEvent_t ev_main = nullptr;
+    cudaEvent_t ev_stage = nullptr;      // the last stage-out copies are done
+    bool staged = false;
     std::vector<cudaEvent_t> ev_batch;
     bool bound = false;
     kvm_buffers bufs{};
@@ -237,7 +239,8 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
             (e = cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming)) != cudaSuccess)
             return cleanup(cuda_fail(e, "cudaEventCreate"));
     }
-    if ((e = cudaEventCreateWithFlags(&c->ev_main, cudaEventDisableTiming)) != cudaSuccess)
+    if ((e = cudaEventCreateWithFlags(&c->ev_main, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_stage, cudaEventDisableTiming)) != cudaSuccess)
         return cleanup(cuda_fail(e, "cudaEventCreate"));
     const int n_batches =
         (cfg->pool_pages + cfg->h2d_batch_blocks - 1) / cfg->h2d_batch_blocks + 1;
@@ -261,7 +264,8 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
 kvm_status kvm_destroy(kvm_ctx *c) {
     if (!c) return KVM_OK;
     if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
-    for (auto ev : {c->ev_ready[0], c->ev_ready[1], c->ev_free[0], c->ev_free[1], c->ev_main})
+    for (auto ev : {c->ev_ready[0], c->ev_ready[1], c->ev_free[0], c->ev_free[1], c->ev_main,
+                    c->ev_stage})
         if (ev) cudaEventDestroy(ev);
     for (auto ev : c->ev_batch)
         if (ev) cudaEventDestroy(ev);
@@ -432,6 +436,30 @@ kvm_status kvm_bind(kvm_ctx *c, const kvm_buffers *b) {
     return KVM_OK;
 }
 
+kvm_status kvm_stage_out(kvm_ctx *c, const void *raw_k, const void *v, int64_t first_block,
+                         int64_t n_blocks, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!c->bound) return fail(KVM_ERR_NOT_BOUND, "kvm_stage_out before kvm_bind");
+    if (c->cfg.repo_location != KVM_HOST_PINNED)
+        return fail(KVM_ERR_INVALID_ARG, "stage-out needs a host-resident repository");
+    if (!raw_k || !v) return fail(KVM_ERR_INVALID_ARG, "raw_k and v are required");
+    if (first_block < 0 || n_blocks < 0) return fail(KVM_ERR_INVALID_ARG, "negative block range");
+    if (first_block + n_blocks > c->cfg.max_blocks)
+        return fail(KVM_ERR_CAPACITY, "blocks beyond max_blocks");
+    if (n_blocks == 0) return KVM_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t blk = block_bytes(c->cfg);
+    char *dk = const_cast<char *>(static_cast<const char *>(c->bufs.raw_k)) + first_block * blk;
+    char *dv = const_cast<char *>(static_cast<const char *>(c->bufs.v)) + first_block * blk;
+    KVM_CUDA(cudaEventRecord(c->ev_main, s));
+    KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0));
+    KVM_CUDA(cudaMemcpyAsync(dk, raw_k, n_blocks * blk, cudaMemcpyDeviceToHost, c->copy_stream));
+    KVM_CUDA(cudaMemcpyAsync(dv, v, n_blocks * blk, cudaMemcpyDeviceToHost, c->copy_stream));
+    KVM_CUDA(cudaEventRecord(c->ev_stage, c->copy_stream));
+    c->staged = true;
+    return KVM_OK;
+}
+
 kvm_status kvm_reset_pool(kvm_ctx *c) {
     if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
     reset_pool(c);
@@ -549,6 +577,11 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         if ((e = cudaMemcpyAsync(c->desc_dev, desc.data(), desc.size() * sizeof(kvm::SlotDesc),
                                  cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return abort_step(cuda_fail(e, "descriptor upload"));
+    }
+    if (pull && c->staged) {
+        // the kernel reads the host repository: order it after earlier stage-outs
+        if ((e = cudaStreamWaitEvent(s, c->ev_stage, 0)) != cudaSuccess)
+            return abort_step(cuda_fail(e, "stage-out wait"));
     }
     if (!host_repo || pull) {
         if (n_rope > 0) {
