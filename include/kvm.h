@@ -87,6 +87,12 @@ typedef struct {
     int32_t score_variant;   /* 0: tcgen05 tensor cores for bf16 q/index (d 64 or 128,
                                 <= 256 query rows per KV head), CUDA cores otherwise;
                                 1: CUDA cores always */
+    int32_t delta_rerope_limit; /* kvm_step, hits whose slot moved ([KVMem] §4.4 bounded
+                                delta re-RoPE): 0 = rebuild K from raw K every time;
+                                n > 0 = rotate the page's K in place by the position
+                                change, at most n times in a row, then rebuild from raw K.
+                                Each delta adds at most one rounding of the pair's
+                                magnitude, so n bounds the error growth. */
 } kvm_config;
 
 typedef struct kvm_ctx kvm_ctx;
@@ -215,7 +221,8 @@ typedef struct {
     int32_t reroped;      /* slots whose K was (re)written             */
     int32_t evicted;      /* pages whose block left the pool           */
     int32_t h2d_copies;   /* host-to-device copies issued              */
-    int64_t h2d_bytes;    /* bytes copied host to device               */
+    int64_t h2d_bytes;    /* bytes moved host to device               */
+    int32_t delta_reroped;/* hits rotated in place by their position change */
 } kvm_step_stats;
 
 /*
@@ -227,7 +234,10 @@ typedef struct {
  * raw K and V in batches of h2d_batch_blocks on an internal copy stream,
  * each batch re-RoPE'd by the GPU after its copy event (the three-stage
  * pipeline of [KVMem] §4.4, Figure 3) when KVM_HOST_PINNED.  Hits whose slot
- * changed are re-RoPE'd from raw K.
+ * changed are re-RoPE'd from raw K (the page's raw-K copy when pool_raw_k is
+ * bound, else the repository), or rotated in place by the position change
+ * under delta_rerope_limit.  pool_raw_k may be NULL unless the repository is
+ * host-resident with h2d_mode 0.
  * Synchronises with `stream` once (to read the selected ids) and returns
  * with the rest enqueued; `stats` (nullable, host) is filled before return.
  */

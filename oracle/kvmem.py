@@ -316,6 +316,48 @@ def rerope_k(k_blocks: np.ndarray, kv_dtype: str, from_pos: np.ndarray, to_pos: 
 # (d) delta working set and page reuse ([KVMem] §4.4; §5 block record)
 # ----------------------------------------------------------------------------
 
+def delta_rerope_k(k_blocks: np.ndarray, kv_dtype: str, delta: int, theta: float) -> np.ndarray:
+    """Bounded delta re-RoPE of [KVMem] §4.4: K already rotated at positions
+    p + t is moved to p + delta + t by rotating the stored (rounded) K by delta,
+    R_delta in float32 from the float32 table row |delta| (sin negated for a
+    negative delta), rounded once.  Every token of the block turns by the same
+    angle because old and new positions differ by the same delta."""
+    k32 = as_f32(k_blocks, kv_dtype)
+    d = k32.shape[-1]
+    c, s = cos_sin_f32(np.full(BLOCK, abs(int(delta))), d, theta)
+    if delta < 0:
+        s = -s
+    return round_to(rope_f32(k32, c, s), kv_dtype)
+
+
+def residency_step_delta(block_of_page: list, baked_pos: list, delta_count: list,
+                         sel: np.ndarray, limit: int):
+    """The delta working set with bounded delta re-RoPE ([KVMem] §4.4): pages as
+    in residency_step; a hit whose compact position changed is rotated in place
+    by delta = new - baked while its page has had fewer than `limit` delta
+    rotations since it was last rebuilt from raw K, and is rebuilt from raw K
+    (counter reset) otherwise; misses are built from raw K (counter 0).
+    Returns (page_of_slot, action_of_slot, new_block_of_page, new_baked_pos,
+    new_delta_count) with action "keep", "delta", "rebuild" or "miss"."""
+    page, hit, rope, bop, bp = residency_step(block_of_page, baked_pos, sel)
+    cnt = list(delta_count)
+    action = []
+    for j in range(len(sel)):
+        p = page[j]
+        if not hit[j]:
+            action.append("miss")
+            cnt[p] = 0
+        elif not rope[j]:
+            action.append("keep")
+        elif cnt[p] < limit:
+            action.append("delta")
+            cnt[p] += 1
+        else:
+            action.append("rebuild")
+            cnt[p] = 0
+    return page, action, bop, bp, cnt
+
+
 def residency_step(block_of_page: list, baked_pos: list, sel: np.ndarray):
     """One working-set transition over a bounded page pool.
 

@@ -35,7 +35,7 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
                pool_pages: int | None = None, index_location: int | None = None,
                repo_location: int | None = None, h2d_batch_blocks: int = 64,
                max_queries: int | None = None, score_variant: int = 0,
-               h2d_mode: int = 1) -> KvmConfig:
+               h2d_mode: int = 1, delta_rerope_limit: int = 0) -> KvmConfig:
     """A kvm_config for a workload shape.  With a host-resident repository the
     GPU reads missed blocks from pinned host memory itself (h2d_mode 1) unless
     h2d_mode=0 asks for copy-engine transfers."""
@@ -54,7 +54,7 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         max_positions=mp, tile_blocks=wl.tile_blocks,
         pool_pages=pool_pages if pool_pages is not None else wl.view_blocks + wl.append_blocks,
         index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
-        h2d_mode=h2d_mode, score_variant=score_variant)
+        h2d_mode=h2d_mode, score_variant=score_variant, delta_rerope_limit=delta_rerope_limit)
 
 
 def _ptr(t) -> int | None:

@@ -30,6 +30,7 @@ class KvmConfig(ctypes.Structure):
         ("pool_pages", ctypes.c_int32), ("index_location", ctypes.c_int32),
         ("repo_location", ctypes.c_int32), ("h2d_batch_blocks", ctypes.c_int32),
         ("h2d_mode", ctypes.c_int32), ("score_variant", ctypes.c_int32),
+        ("delta_rerope_limit", ctypes.c_int32),
     ]
 
 
@@ -47,6 +48,7 @@ class KvmStepStats(ctypes.Structure):
         ("n_blocks", ctypes.c_int64), ("n_sel", ctypes.c_int32), ("hits", ctypes.c_int32),
         ("misses", ctypes.c_int32), ("reroped", ctypes.c_int32), ("evicted", ctypes.c_int32),
         ("h2d_copies", ctypes.c_int32), ("h2d_bytes", ctypes.c_int64),
+        ("delta_reroped", ctypes.c_int32),
     ]
 
 

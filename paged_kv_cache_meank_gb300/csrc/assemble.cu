@@ -26,14 +26,29 @@ struct SlotWork {
     static constexpr int NT = 32 * TPT;
 
     // Rotate one block's K to positions pos0 + t for pairs [lg0, lg1) and copy V.
-    __device__ static void run(const T *__restrict__ src_k, const T *__restrict__ src_v,
-                               T *__restrict__ dst_k, T *__restrict__ dst_v, int64_t pos0,
+    // src_k and dst_k may be the same block (an in-place delta rotation), so
+    // they carry no __restrict__
+    __device__ static void run(const T *src_k, const T *__restrict__ src_v,
+                               T *dst_k, T *__restrict__ dst_v, int64_t pos0,
                                int lg0, int lg1, const float2 *__restrict__ table,
-                               float2 *tab, T *__restrict__ dst_raw = nullptr) {
+                               float2 *tab, T *__restrict__ dst_raw = nullptr,
+                               bool delta = false) {
         const int tid = threadIdx.x;
         const int tok = tid / TPT, c = tid % TPT;
-        const float2 *trow = table + pos0 * HD;
-        for (int i = tid; i < kBlockTokens * HD; i += NT) tab[i] = trow[i];
+        if (!delta) {
+            const float2 *trow = table + pos0 * HD;
+            for (int i = tid; i < kBlockTokens * HD; i += NT) tab[i] = trow[i];
+        } else {
+            // every token turns by the same angle delta * w_i: row |delta| for all
+            // tokens, sin negated for a negative delta
+            const int64_t ad = pos0 < 0 ? -pos0 : pos0;
+            const float sg = pos0 < 0 ? -1.f : 1.f;
+            const float2 *trow = table + ad * HD;
+            for (int i = tid; i < kBlockTokens * HD; i += NT) {
+                const float2 w = trow[i % HD];
+                tab[i] = make_float2(w.x, sg * w.y);
+            }
+        }
         __syncthreads();
         float cs[PPT], sn[PPT];
 #pragma unroll
@@ -104,15 +119,19 @@ assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
                      const float2 *__restrict__ table, int64_t max_pos, int *err) {
     __shared__ float2 tab[kBlockTokens * (D / 2)];
     const SlotDesc sd = desc[blockIdx.x];
-    if (sd.pos0 < 0 || sd.pos0 + kBlockTokens > max_pos || sd.src_k == nullptr ||
-        sd.dst_k == nullptr) {
+    const bool delta = (sd.flags & kSlotDelta) != 0;
+    const bool pos_ok = delta ? (sd.pos0 > -max_pos && sd.pos0 < max_pos)
+                              : (sd.pos0 >= 0 && sd.pos0 + kBlockTokens <= max_pos);
+    if (!pos_ok || sd.src_k == nullptr || sd.dst_k == nullptr) {
         if (threadIdx.x == 0) atomicOr(err, 2);
         return;
     }
+    // a delta rotation runs in place (src_k == dst_k): every thread reads its
+    // 16-byte pieces before it writes the same addresses
     const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
     SlotWork<T, D>::run(static_cast<const T *>(sd.src_k), static_cast<const T *>(sd.src_v),
                         static_cast<T *>(sd.dst_k), static_cast<T *>(sd.dst_v), sd.pos0, lg0,
-                        lg1, table, tab, static_cast<T *>(sd.dst_raw));
+                        lg1, table, tab, static_cast<T *>(sd.dst_raw), delta);
 }
 
 static int lg_split(int n_slots, int LG) {

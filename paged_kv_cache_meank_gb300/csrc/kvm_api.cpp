@@ -84,6 +84,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->h2d_batch_blocks < 1) return bad("h2d_batch_blocks must be >= 1");
     if (c->score_variant != 0 && c->score_variant != 1) return bad("score_variant must be 0 or 1");
     if (c->h2d_mode != 0 && c->h2d_mode != 1) return bad("h2d_mode must be 0 or 1");
+    if (c->delta_rerope_limit < 0) return bad("delta_rerope_limit must be >= 0");
     return true;
 }
 
@@ -142,6 +143,7 @@ struct kvm_ctx {
     // residency of the page pool
     std::vector<int64_t> block_of_page;
     std::vector<int64_t> baked_pos;
+    std::vector<int32_t> delta_count;    // delta rotations since the page's K was rebuilt
     std::vector<int32_t> page_of_block;
     std::vector<uint8_t> mark;
     // fault injection
@@ -185,6 +187,7 @@ void reset_pool(kvm_ctx *c) {
         if (b >= 0 && b < (int64_t)c->page_of_block.size()) c->page_of_block[b] = -1;
     std::fill(c->block_of_page.begin(), c->block_of_page.end(), -1);
     std::fill(c->baked_pos.begin(), c->baked_pos.end(), -1);
+    std::fill(c->delta_count.begin(), c->delta_count.end(), 0);
 }
 
 }  // namespace
@@ -226,6 +229,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->scr.err = c->err_dev;
     c->block_of_page.assign(cfg->pool_pages, -1);
     c->baked_pos.assign(cfg->pool_pages, -1);
+    c->delta_count.assign(cfg->pool_pages, 0);
     c->page_of_block.assign((size_t)cfg->max_blocks, -1);
     c->mark.assign((size_t)cfg->max_blocks, 0);
 
@@ -411,8 +415,9 @@ kvm_status kvm_bind(kvm_ctx *c, const kvm_buffers *b) {
     if (!b->index || !b->raw_k || !b->v || !b->pool_k || !b->pool_v || !b->page_table ||
         !b->scores || !b->sel_ids)
         return fail(KVM_ERR_INVALID_ARG, "a required buffer is NULL");
-    if (c->cfg.repo_location == KVM_HOST_PINNED && !b->pool_raw_k)
-        return fail(KVM_ERR_INVALID_ARG, "pool_raw_k is required with a host-resident repository");
+    if (c->cfg.repo_location == KVM_HOST_PINNED && c->cfg.h2d_mode == 0 && !b->pool_raw_k)
+        return fail(KVM_ERR_INVALID_ARG,
+                    "pool_raw_k is required with a host-resident repository and h2d_mode 0");
     c->repo_k_dev = b->raw_k;
     c->repo_v_dev = b->v;
     if (c->cfg.repo_location == KVM_HOST_PINNED && c->cfg.h2d_mode == 1) {
@@ -523,18 +528,37 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
     auto R_k = [&](int64_t b) { return static_cast<const char *>(c->bufs.raw_k) + (size_t)b * blk; };
     auto R_v = [&](int64_t b) { return static_cast<const char *>(c->bufs.v) + (size_t)b * blk; };
 
+    // where a page's K is rebuilt from: its own raw-K copy, else the repository
+    // (device memory, or the pinned host repository read by the kernel)
+    auto raw_src = [&](int64_t b, int p) -> const void * {
+        if (c->bufs.pool_raw_k) return P_r(p);
+        if (!host_repo) return R_k(b);
+        return static_cast<const char *>(c->repo_k_dev) + (size_t)b * blk;
+    };
     // descriptors: shifted hits first (no copy to wait for), then misses in slot order
     std::vector<kvm::SlotDesc> desc;
     desc.reserve(n_sel);
-    int n_rope = 0, evicted = 0;
+    std::vector<int32_t> new_count(c->delta_count);
+    int n_rope = 0, evicted = 0, n_delta = 0;
     for (int j = 0; j < n_sel; ++j) {
         if (!is_hit[j]) continue;
         const int p = page_of_slot[j];
-        if (c->baked_pos[p] == (int64_t)j * 32) continue;
+        const int64_t want = (int64_t)j * 32;
+        if (c->baked_pos[p] == want) continue;
         kvm::SlotDesc d{};
-        d.src_k = host_repo ? P_r(p) : R_k(sel[j]);
         d.dst_k = P_k(p);
-        d.pos0 = (int64_t)j * 32;
+        if (cfg.delta_rerope_limit > 0 && c->delta_count[p] < cfg.delta_rerope_limit) {
+            // bounded delta re-RoPE ([KVMem] §4.4): rotate the page's K in place
+            d.src_k = P_k(p);
+            d.pos0 = want - c->baked_pos[p];
+            d.flags = kvm::kSlotDelta;
+            new_count[p] = c->delta_count[p] + 1;
+            ++n_delta;
+        } else {
+            d.src_k = raw_src(sel[j], p);
+            d.pos0 = want;
+            new_count[p] = 0;
+        }
         desc.push_back(d);
     }
     const int n_hit_rope = (int)desc.size();
@@ -550,7 +574,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
             d.src_k = static_cast<const char *>(c->repo_k_dev) + (size_t)sel[j] * blk;
             d.src_v = static_cast<const char *>(c->repo_v_dev) + (size_t)sel[j] * blk;
             d.dst_v = P_v(p);
-            d.dst_raw = P_r(p);
+            d.dst_raw = c->bufs.pool_raw_k ? P_r(p) : nullptr;
         } else if (host_repo) {
             d.src_k = P_r(p);
         } else {
@@ -561,6 +585,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         d.dst_k = P_k(p);
         d.pos0 = (int64_t)j * 32;
         desc.push_back(d);
+        new_count[p] = 0;
     }
     n_rope = (int)desc.size();
 
@@ -654,6 +679,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         c->page_of_block[sel[j]] = p;
     }
     for (int j = 0; j < n_sel; ++j) c->baked_pos[page_of_slot[j]] = (int64_t)j * 32;
+    c->delta_count.swap(new_count);
 
     if (stats) {
         stats->n_blocks = n_blocks;
@@ -661,6 +687,7 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         stats->misses = (int32_t)miss_slots.size();
         stats->hits = n_sel - stats->misses;
         stats->reroped = n_rope;
+        stats->delta_reroped = n_delta;
         stats->evicted = evicted;
         stats->h2d_copies = h2d_copies;
         // bytes that crossed the host link: by copy engine, or read by the kernel

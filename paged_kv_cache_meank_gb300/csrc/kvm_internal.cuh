@@ -33,8 +33,10 @@ struct SlotDesc {
     void *dst_k;
     void *dst_v;
     void *dst_raw;      // nullable: also store the raw K as read (a page's raw-K copy)
-    int64_t pos0;
+    int64_t pos0;       // first position; with kSlotDelta: the position change delta
+    int32_t flags;      // kSlotDelta: rotate the K in place by pos0 (same angle per token)
 };
+constexpr int32_t kSlotDelta = 1;
 
 struct ScoreShape {
     int L, G, H, d, n_queries;

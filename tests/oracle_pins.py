@@ -352,4 +352,51 @@ def pin_residency(o):
         pass
 
 
+def pin_delta_rerope(o):
+    """A delta of 0 is the identity; a delta rotation of RoPE'd K lands within
+    float32 / bf16 rounding of the exact rotation at the new position
+    (InferScale Theorem 6 (1)); errors of repeated deltas stay within a bound
+    linear in their number; +d then -d returns close to the start."""
+    rng = np.random.default_rng(15)
+    L, G, d, theta = 2, 1, 32, 1e6
+    raw = rng.standard_normal((1, L, G, 32, d))
+    k0 = o.f32_to_bf16(_rope_pages(o, raw, 5, theta).astype(np.float32))   # at 160..191
+    assert np.array_equal(o.delta_rerope_k(k0, "bf16", 0, theta), k0)
+    h = d // 2
+    def pair_mag(x):
+        m = np.maximum(np.abs(x[..., :h]), np.abs(x[..., h:]))
+        return np.concatenate([m, m], axis=-1)
+    k = k0
+    pos = 160
+    for step, delta in enumerate([-96, 32, -64, 7, 250], start=1):
+        k = o.delta_rerope_k(k, "bf16", delta, theta)
+        pos += delta
+        exact = _rope_pages(o, raw, 0, theta)        # raw at 0..31, then moved exactly
+        exact = o.rerope_k(exact, "f32", np.arange(32)[None], np.arange(pos, pos + 32)[None],
+                           theta)
+        err = np.abs(o.bf16_to_f32(k).astype(np.float64) - exact)
+        # each delta adds at most one bf16 rounding of the pair's magnitude
+        assert np.all(err <= (step + 1) * 2.0 ** -8 * pair_mag(exact) + 1e-6), step
+    back = o.delta_rerope_k(o.delta_rerope_k(k0, "bf16", 40, theta), "bf16", -40, theta)
+    assert np.all(np.abs(o.bf16_to_f32(back).astype(np.float64) - o.bf16_to_f32(k0))
+                  <= 2 * 2.0 ** -8 * pair_mag(o.bf16_to_f32(k0).astype(np.float64)) + 1e-7)
+
+
+def pin_residency_delta(o):
+    """A worked sequence with a delta limit of 1: a moved hit is rotated once,
+    rebuilt from raw K the next time it moves, then rotated again."""
+    P = 4
+    bop, bp, cnt = [-1] * P, [-1] * P, [0] * P
+    page, act, bop, bp, cnt = o.residency_step_delta(bop, bp, cnt, np.array([5, 9]), 1)
+    assert act == ["miss", "miss"] and page == [0, 1]
+    page, act, bop, bp, cnt = o.residency_step_delta(bop, bp, cnt, np.array([2, 5, 9]), 1)
+    assert act == ["miss", "delta", "delta"] and page == [2, 0, 1] and cnt[:3] == [1, 1, 0]
+    page, act, bop, bp, cnt = o.residency_step_delta(bop, bp, cnt, np.array([1, 2, 5, 9]), 1)
+    assert act == ["miss", "delta", "rebuild", "rebuild"] and cnt == [0, 0, 1, 0]
+    page, act, bop, bp, cnt = o.residency_step_delta(bop, bp, cnt, np.array([1, 2, 5, 9]), 1)
+    assert act == ["keep"] * 4
+    page, act, bop, bp, cnt = o.residency_step_delta(bop, bp, cnt, np.array([0, 1, 2, 5]), 1)
+    assert act == ["miss", "delta", "rebuild", "delta"]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -169,3 +169,73 @@ def test_step_failure_injection(kvm):
     ref = ora.view_k(to_np(raw_d, "bf16")[sel.cpu().numpy()], "bf16", wl.rope_theta)
     got = to_np(pool_k, "bf16")[pt.cpu().numpy()]
     assert_storage_close(got, ref, "bf16", "after recovery")
+
+
+@pytest.mark.parametrize("repo_host", [False, True], ids=["repo-device", "repo-host-pull-no-raw-copy"])
+def test_step_bounded_delta_rerope(kvm, repo_host):
+    """Bounded delta re-RoPE (KVMem §4.4): hits whose slot moved are rotated in
+    place by the position change at most once in a row, then rebuilt from raw K;
+    every page is compared with the oracle's own pool that applies the same
+    actions (delta rotation of its stored page, or RoPE of raw K)."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    limit = 1
+    N_max = 300
+    ws = workload.make_workspace(wl, seed=61, n_blocks=N_max, with_q=False)
+    raw_np, v_np = to_np(ws.raw_k, "bf16"), to_np(ws.v, "bf16")
+    kp = prefill_k_pages(raw_np, "bf16", wl.rope_theta)
+    cfg = kvm.config_for(wl, max_blocks=N_max, pool_pages=wl.view_blocks + 6,
+                         repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
+                         h2d_mode=1, delta_rerope_limit=limit)
+    ctx = kvm.Context(cfg)
+    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+    raw_d = torch.empty(ctx.block_shape(N_max), dtype=torch.bfloat16, device="cuda")
+    ctx.build_index(from_np(kp, "bf16"), 0, N_max, index, raw_d)
+    ctx.sync()
+    v_d = from_np(v_np, "bf16")
+    if repo_host:
+        raw_repo = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
+        raw_repo.copy_(raw_d)
+        v_repo = torch.empty(v_d.shape, dtype=v_d.dtype, pin_memory=True)
+        v_repo.copy_(v_d)
+    else:
+        raw_repo, v_repo = raw_d, v_d
+    P = cfg.pool_pages
+    pool_k = torch.zeros(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+    pool_v = torch.zeros_like(pool_k)
+    pt = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    scores = torch.empty(N_max, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.bind(index=index, raw_k=raw_repo, v=v_repo, pool_k=pool_k, pool_v=pool_v,
+             pool_raw_k=None, page_table=pt, scores=scores, sel_ids=sel)
+    raw_ref = to_np(raw_d, "bf16")          # the repository's raw K, as the GPU stored it
+    g = torch.Generator().manual_seed(62)
+    u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
+    qs = [workload.make_queries(wl, g, "cpu", u[i % 3]) for i in range(6)]
+    ns = [240, 250, 260, 270, 285, 300]     # the history grows: selections shift slots
+    bop, bp, cnt = [-1] * P, [-1] * P, [0] * P
+    ora_pool = {}
+    n_delta = n_rebuild = 0
+    for step, (q, N) in enumerate(zip(qs, ns)):
+        st = ctx.step(q.cuda(), wl.n_queries, N)
+        ctx.sync()
+        g_sel = sel[:wl.view_blocks].cpu().numpy()
+        prev_bp = list(bp)
+        page, act, bop, bp, cnt = ora.residency_step_delta(bop, bp, cnt, g_sel, limit)
+        assert pt.cpu().tolist() == page, f"step {step} page table"
+        assert st["delta_reroped"] == act.count("delta"), (step, st, act.count("delta"))
+        for j, (p, a) in enumerate(zip(page, act)):
+            if a in ("miss", "rebuild"):
+                c, s = ora.cos_sin_f32(ora.slot_positions(j + 1)[j], wl.head_dim, wl.rope_theta)
+                ora_pool[p] = ora.round_to(ora.rope_f32(ora.as_f32(raw_ref[g_sel[j]], "bf16"), c, s),
+                                           "bf16")
+            elif a == "delta":
+                ora_pool[p] = ora.delta_rerope_k(ora_pool[p][None], "bf16", j * 32 - prev_bp[p],
+                                                 wl.rope_theta)[0]
+        n_delta += act.count("delta")
+        n_rebuild += act.count("rebuild")
+        got = to_np(pool_k, "bf16")
+        for j, p in enumerate(page):
+            assert_storage_close(got[p][None], ora_pool[p][None], "bf16", f"step {step} slot {j}")
+        assert np.array_equal(to_np(pool_v, "bf16")[page], v_np[g_sel])
+    assert n_delta > 0 and n_rebuild > 0      # both branches of the bound were taken

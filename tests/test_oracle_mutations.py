@@ -131,7 +131,31 @@ def _residency_descending(block_of_page, baked_pos, sel):
     return [P - 1 - p for p in page], hit, rope, list(reversed(bop)), list(reversed(bp))
 
 
+def _delta_sign_ignored(k_blocks, kv_dtype, delta, theta):
+    k32 = ora.as_f32(k_blocks, kv_dtype)
+    c, s = ora.cos_sin_f32(np.full(32, abs(int(delta))), k32.shape[-1], theta)
+    return ora.round_to(ora.rope_f32(k32, c, s), kv_dtype)
+
+
+def _delta_limit_inclusive(block_of_page, baked_pos, delta_count, sel, limit):
+    page, hit, rope, bop, bp = ora.residency_step(block_of_page, baked_pos, sel)
+    cnt, action = list(delta_count), []
+    for j in range(len(sel)):
+        p = page[j]
+        if not hit[j]:
+            action.append("miss"); cnt[p] = 0
+        elif not rope[j]:
+            action.append("keep")
+        elif cnt[p] <= limit:
+            action.append("delta"); cnt[p] += 1
+        else:
+            action.append("rebuild"); cnt[p] = 0
+    return page, action, bop, bp, cnt
+
+
 MUTANTS = {
+    "delta rotation ignores the sign of delta": ("delta_rerope_k", _delta_sign_ignored),
+    "delta limit off by one": ("residency_step_delta", _delta_limit_inclusive),
     "interleaved pairs": ("rotate_f64", _interleaved_rotate),
     "sin sign flipped": ("rotate_f64", _sin_sign_rotate),
     "frequency exponent missing 2": ("inv_freq", _inv_freq_no_two),
