@@ -15,10 +15,12 @@
 //                accumulators and commits to mbarriers
 //   warps 2..17  epilogue, four warps per TMEM lane quadrant, each taking a
 //                quarter of the accumulator's columns; the four combine in a
-//                fixed order through shared memory, handed over with mbarriers
+//                fixed order through shared memory, handed over with mbarriers.
+//                An accumulator goes back to the MMA warp as soon as it has
+//                been read into registers, before the exponentials.
 // Pass 1 computes D[query row][block] (M = 128 query rows per tile, N = 128
-// blocks): each epilogue thread owns one query row and keeps its running max
-// and rescaled partition sum in registers -- no cross-thread reduction.
+// blocks): each epilogue thread owns one query row and keeps a reference and
+// the partition sum relative to it in registers -- no cross-thread reduction.
 // Pass 2 computes D[block][query row] (M = 128 blocks, N = rows rounded to 16):
 // each thread owns one block and sums 2^(s*c - M - log2 Z) over its query rows
 // in registers.  Every mbarrier wait is bounded; on timeout the kernel raises
@@ -42,6 +44,7 @@ constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kQRows = 256;         // query rows padded to two M = 128 tiles
+constexpr int kPrefetch = 4;        // tiles fetched into L2 ahead of the shared-memory ring
 
 template <int D>
 struct Lay {
@@ -52,10 +55,10 @@ struct Lay {
     static constexpr int QB = KA * Q_ATOM;
     static constexpr int OFF_Q = kStages * TILE;
     static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
-    static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 2 x 4 x 3 x 32 x 2 floats
-    static constexpr int OFF_D = OFF_X + 2 * 4 * 3 * 32 * 2 * 4;   // 2 x 32 x 2 floats
+    static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 1536 floats
+    static constexpr int OFF_D = OFF_X + 1536 * 4;     // 2 x 32 x 2 floats
     static constexpr int OFF_BAR = OFF_D + 2 * 32 * 2 * 4;
-    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
 };
 
 // Sum of 2^(v*c + no) over n loaded columns (n a multiple of 16, at most 64;
@@ -79,6 +82,30 @@ __device__ __forceinline__ float exp_sum(const uint32_t *r, const float *no, int
         }
     }
     return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+// exp_sum over a compile-time count of columns (the common shapes), with no
+// per-column guards, so that the whole sum is one straight-line schedule.
+template <int NC>
+__device__ __forceinline__ float exp_sum_n(const uint32_t *r, const float *no, float c) {
+    const float2 c2 = make_float2(c, c);
+    float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int k = 0; k < NC; k += 4) {
+        const float4 o4 = *reinterpret_cast<const float4 *>(no + k);
+        const float2 x01 = __ffma2_rn(
+            make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2,
+            make_float2(o4.x, o4.y));
+        const float2 x23 = __ffma2_rn(
+            make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2,
+            make_float2(o4.z, o4.w));
+        const int j = (k >> 2) & 1;
+        a[2 * j] = __fadd2_rn(a[2 * j], make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+        a[2 * j + 1] = __fadd2_rn(a[2 * j + 1], make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
+    }
+    const float2 s01 = __fadd2_rn(a[0], a[1]), s23 = __fadd2_rn(a[2], a[3]);
+    return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
 // Online softmax statistics of one query row over the first nv of NV loaded
@@ -124,9 +151,41 @@ __device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c
     m = mn;
 }
 
+// Row statistics with the reference held fixed: while every term of a full
+// tile stays below 2^64 relative to the row's current reference m, the tile
+// only adds its terms to z (no max over the tile).  A larger term, the row's
+// first tile and a ragged tile take the exact online update, which moves m to
+// the running maximum.  (m, z) stays an exact pair for any m: the partition sum
+// is z * 2^m, and pass 2 divides by it through m + log2 z.
+template <int NV>
+__device__ __forceinline__ void row_update(const uint32_t *r, int nv, float c, float &m,
+                                           float &z) {
+    if (nv == NV && m != -INFINITY) {
+        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NV; k += 4) {
+            const float2 x01 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2, nm2);
+            const float2 x23 = __ffma2_rn(
+                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2, nm2);
+            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
+        }
+        const float zs = (a0.x + a0.y) + (a1.x + a1.y);
+        if (zs <= 0x1p64f) {   // false for inf and NaN as well
+            z += zs;
+            return;
+        }
+    }
+    online_update<NV>(r, nv, c, m, z);
+}
+
 }  // namespace
 
-template <int D, int PASS>
+// NC: columns per epilogue warp in pass 2 when fixed at compile time (48 for
+// 192 query rows), 0 for any row count.
+template <int D, int PASS, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *__restrict__ q,
                 ScoreShape sh, int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
@@ -145,8 +204,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
-    uint64_t *xfull = tempty + 2;        // [2][4]: warps 1..3 of a quadrant wrote their partials
-    uint64_t *xfin = xfull + 8;          // [4]: the same for the final pass-1 statistics
+    uint64_t *xfull = tempty + 2;        // [4][4]: warps 1..3 of a quadrant wrote their partials
+    uint64_t *xfin = xfull + 16;         // [4]: the same for the final pass-1 statistics
     uint64_t *xdbar = xfin + 4;          // [2]: quadrant 2+q handed its half-row stats to q
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xdbar + 2);
 
@@ -173,7 +232,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], kEpiWarps * 32);
         }
-        for (int k = 0; k < 8; ++k) tc::mbar_init(&xfull[k], 96);
+        for (int k = 0; k < 16; ++k) tc::mbar_init(&xfull[k], 96);
         for (int k = 0; k < 4; ++k) tc::mbar_init(&xfin[k], 96);
         for (int k = 0; k < 2; ++k) tc::mbar_init(&xdbar[k], 32);
         tc::fence_mbar_init();
@@ -183,18 +242,34 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
         tc::tmem_relinquish();
     }
     // Query rows of (l, g) into the swizzled K-major layout; padding rows are 0.
-    for (int i = tid; i < kQRows * (D / 8); i += kThreads) {
-        const int r = i / (D / 8), c16 = i - r * (D / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        const int src_r = (dup && r >= 192) ? r - 64 : r;
-        if (src_r < rows) {
-            const int m = src_r / sh.gqa, hl = src_r - m * sh.gqa;
-            const __nv_bfloat16 *src =
-                q + (((size_t)l * sh.n_queries + m) * sh.H + (size_t)g * sh.gqa + hl) * D + c16 * 8;
-            v = *reinterpret_cast<const uint4 *>(src);
+    // Each thread issues all of its loads before the first store.
+    {
+        constexpr int kQItems = kQRows * (D / 8);
+        constexpr int kPer = (kQItems + kThreads - 1) / kThreads;
+        uint4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = tid + k * kThreads;
+            v[k] = make_uint4(0, 0, 0, 0);
+            const int r = i / (D / 8), c16 = i - r * (D / 8);
+            const int src_r = (dup && r >= 192) ? r - 64 : r;
+            if (i < kQItems && src_r < rows) {
+                const int m = src_r / sh.gqa, hl = src_r - m * sh.gqa;
+                const __nv_bfloat16 *src = q + (((size_t)l * sh.n_queries + m) * sh.H +
+                                                (size_t)g * sh.gqa + hl) * D + c16 * 8;
+                v[k] = __ldg(reinterpret_cast<const uint4 *>(src));
+            }
         }
-        const int a = c16 >> 3, cc = c16 & 7;
-        *reinterpret_cast<uint4 *>(qs + a * LY::Q_ATOM + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = tid + k * kThreads;
+            if (i < kQItems) {
+                const int r = i / (D / 8), c16 = i - r * (D / 8);
+                const int a = c16 >> 3, cc = c16 & 7;
+                *reinterpret_cast<uint4 *>(qs + a * LY::Q_ATOM + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                    v[k];
+            }
+        }
     }
     if (PASS == 2) {
         for (int r = tid; r < kQRows; r += kThreads) {
@@ -214,13 +289,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
 
     if (warp == 0) {
         if (lane == 0) {
+            auto tile_y = [&](int i) {
+                return (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
+            };
+            // The ring holds a tile from its load until its MMA completes; L2
+            // prefetches keep later tiles in flight from HBM meanwhile.
+            for (int i = kStages; i < min(n_tiles, kStages + kPrefetch); ++i)
+                for (int a = 0; a < LY::KA; ++a) tc::tma_prefetch_2d(&tmap, a * 64, tile_y(i));
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
+                if (i + kStages + kPrefetch - 1 < n_tiles && i >= 1)
+                    for (int a = 0; a < LY::KA; ++a)
+                        tc::tma_prefetch_2d(&tmap, a * 64, tile_y(i + kStages + kPrefetch - 1));
                 if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
                 tc::mbar_expect_tx(&full[s], LY::TILE);
-                const int64_t gb = cb0 + (int64_t)i * TB;
-                const int32_t y = (int32_t)((int64_t)lg * sh.index_cap + (gb - b_index0));
+                const int32_t y = tile_y(i);
 #pragma unroll
                 for (int a = 0; a < LY::KA; ++a)
                     tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
@@ -309,35 +393,57 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
                     tc::tmem_wait_ld(r + 32);
                     if (!dup) tc::tmem_wait_ld(r + 48);
                 }
+                // the accumulator is in registers: hand the buffer back to the MMA warp
+                tc::tc_fence_before();
+                tc::mbar_arrive(&tempty[buf]);
                 const int nv = min(32, max(0, nvalid - my_c0));
-                online_update<32>(r, nv, scale_log2, m_run[0], z_run[0]);
+                row_update<32>(r, nv, scale_log2, m_run[0], z_run[0]);
                 if (qtiles > 1) {
                     if (dup)
-                        online_update<16>(r + 32, min(16, max(0, nvalid - c1)), scale_log2,
-                                          m_run[1], z_run[1]);
+                        row_update<16>(r + 32, min(16, max(0, nvalid - c1)), scale_log2,
+                                       m_run[1], z_run[1]);
                     else
-                        online_update<32>(r + 32, nv, scale_log2, m_run[1], z_run[1]);
+                        row_update<32>(r + 32, nv, scale_log2, m_run[1], z_run[1]);
                 }
             } else {
                 uint32_t r[64];
+                float sum;
+                if (NC == 48) {   // 192 query rows: 48 columns per warp
+                    tc::tmem_ld32_async(taddr + my_c0, r);
+                    tc::tmem_ld16_async(taddr + my_c0 + 32, r + 32);
+                    tc::tmem_wait_ld(r);
+                    tc::tmem_wait_ld(r + 16);
+                    tc::tmem_wait_ld(r + 32);
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&tempty[buf]);
+                    sum = exp_sum_n<48>(r, o_r + my_c0, scale_log2);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    if (k * 32 + 32 <= my_nc) tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
-                    else if (k * 32 + 16 <= my_nc) tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
+                    for (int k = 0; k < 2; ++k) {
+                        if (k * 32 + 32 <= my_nc)
+                            tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
+                        else if (k * 32 + 16 <= my_nc)
+                            tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&tempty[buf]);
+                    sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
-                float sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
-                // the quadrant's four warps combine in a fixed order through shared
-                // memory (a slot is not reused before warp 0 of the quadrant read it:
-                // the tile two steps ahead needs that warp's arrival on tempty[buf])
-                float *slot = xch + ((buf * 4 + quad) * 3) * 32 + lane;
+                // the quadrant's four warps combine in a fixed order through a
+                // four-deep ring of shared-memory slots.  A slot is not rewritten
+                // before warp 0 of the quadrant read it: tile i + 4 needs that
+                // warp's arrival on tempty for tile i + 2, which follows its read.
+                const int xs = i & 3;
+                const uint32_t xph = (i >> 2) & 1;
+                float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
                 if (sub) {
                     slot[(sub - 1) * 32] = sum;
-                    tc::mbar_arrive(&xfull[buf * 4 + quad]);
+                    tc::mbar_arrive(&xfull[xs * 4 + quad]);
                 } else {
-                    if (!tc::mbar_wait(&xfull[buf * 4 + quad], bph, kWaitLimit)) {
+                    if (!tc::mbar_wait(&xfull[xs * 4 + quad], xph, kWaitLimit)) {
                         atomicOr(err, 4);
                         break;
                     }
@@ -345,8 +451,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
                     if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
                 }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(&tempty[buf]);
         }
         if (PASS == 1) {
             // [t][quad][sub-1][lane] (m, z)
@@ -446,7 +550,7 @@ bool score_tc_supported(int q_dtype, int index_dtype, const ScoreShape &sh) {
            sh.rows >= 1 && sh.rows <= kQRows && encode_fn() != nullptr;
 }
 
-template <int D, int PASS>
+template <int D, int PASS, int NC>
 static cudaError_t tc_t(const ScoreShape &sh, const void *q, const void *index, int64_t b_index0,
                         int64_t b_begin, int64_t b_end, int chunk0, int n_chunks,
                         const ScoreScratch &scr, int64_t partial_stride, int *err,
@@ -455,7 +559,7 @@ static cudaError_t tc_t(const ScoreShape &sh, const void *q, const void *index, 
     if (((uintptr_t)index & 15) != 0) return cudaErrorMisalignedAddress;
     if (!make_index_map(&map, index, D, (int64_t)sh.L * sh.G * sh.index_cap))
         return cudaErrorInvalidValue;
-    auto kern = score_tc_kernel<D, PASS>;
+    auto kern = score_tc_kernel<D, PASS, NC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay<D>::SMEM);
     if (e != cudaSuccess) return e;
@@ -474,20 +578,26 @@ cudaError_t launch_score_pass1_tc(const ScoreShape &sh, const void *q, const voi
                                   int n_chunks, const ScoreScratch &scr, int *err,
                                   cudaStream_t s) {
     if (sh.d == 128)
-        return tc_t<128, 1>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0,
-                            err, s);
-    return tc_t<64, 1>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0, err, s);
+        return tc_t<128, 1, 0>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0,
+                               err, s);
+    return tc_t<64, 1, 0>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0, err,
+                          s);
 }
 
 cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const void *index,
                                   int64_t b_index0, int64_t b_begin, int64_t b_end, int n_chunks,
                                   const ScoreScratch &scr, int64_t partial_stride, int *err,
                                   cudaStream_t s) {
+    const bool n48 = ((sh.rows + 15) & ~15) == 192;
     if (sh.d == 128)
-        return tc_t<128, 2>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
-                            partial_stride, err, s);
-    return tc_t<64, 2>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr, partial_stride,
-                       err, s);
+        return n48 ? tc_t<128, 2, 48>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                                      partial_stride, err, s)
+                   : tc_t<128, 2, 0>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                                     partial_stride, err, s);
+    return n48 ? tc_t<64, 2, 48>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                                 partial_stride, err, s)
+               : tc_t<64, 2, 0>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                                partial_stride, err, s);
 }
 
 }  // namespace kvm

@@ -46,6 +46,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// Bounded wait by a whole warp: lane 0 polls, and once it has seen the phase
+// complete every lane observes that itself with one more wait, which returns
+// at once.  The result is the same in all lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit) ? 1u : 0u;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_wait(bar, parity, limit) ? 1u : 0u;
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+// One arrival on behalf of the whole warp, ordered after every lane's prior
+// memory operations (the barrier's count is in warps).
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int32_t x,
                                             int32_t y) {
@@ -54,6 +71,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+// Prefetch the box at (x, y) of a 2-D tensor map into L2 (no shared memory,
+// no completion signal).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
