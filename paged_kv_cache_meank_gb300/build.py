@@ -25,6 +25,7 @@ SOURCES = [
     "meank.cu",
     "score.cu",
     "score_tc.cu",
+    "score_tc1.cu",
     "score_dispatch.cu",
     "select.cu",
     "assemble.cu",

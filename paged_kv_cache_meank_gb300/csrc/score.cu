@@ -17,6 +17,8 @@
 // any element type.  The tensor-core variant for bf16 lives in score_mma.cu.
 #include <math.h>
 
+#include <algorithm>
+
 #include "kvm_internal.cuh"
 #include "kvm_vec.cuh"
 #include "score_common.cuh"
@@ -135,14 +137,41 @@ __global__ void score_simt_kernel(const TQ *__restrict__ q, const TI *__restrict
     }
 }
 
+static int sm_count() {
+    static int n = 0;
+    if (n <= 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            return 152;
+    }
+    return n;
+}
+
+// Chunks per (layer, kv head).  Each chunk is one CTA and the scoring kernels
+// run one CTA per SM, so the pass takes waves = ceil(L*G*chunks / SMs) rounds
+// of (tiles per chunk + about four tiles of CTA start-up).  Start from enough
+// CTAs for four waves and take the count with the fewest of those tile-times
+// among the next 16 (at least 64 blocks per chunk).
 int score_chunks(const ScoreShape &sh, int64_t n_blocks, int max_chunks) {
-    const int LG = sh.L * sh.G;
-    int64_t c = (152 * 4 + LG - 1) / LG;
-    const int64_t by_size = (n_blocks + 63) / 64;
-    if (c > by_size) c = by_size;
-    if (c > max_chunks) c = max_chunks;
-    if (c < 1) c = 1;
-    return (int)c;
+    const int64_t LG = (int64_t)sh.L * sh.G;
+    const int64_t sms = sm_count();
+    const int64_t by_size = std::max<int64_t>(1, (n_blocks + 63) / 64);
+    const int64_t hi = std::min<int64_t>(std::min<int64_t>(by_size, max_chunks), 1 << 20);
+    const int64_t lo = std::min<int64_t>(std::max<int64_t>(1, (sms * 4 + LG - 1) / LG), hi);
+    int64_t best = lo, best_cost = -1;
+    for (int64_t c = lo; c <= std::min(hi, lo + 16); ++c) {
+        const int64_t waves = (LG * c + sms - 1) / sms;
+        const int64_t tiles = ((n_blocks + c - 1) / c + 127) / 128;
+        const int64_t cost = waves * (tiles + 4);
+        if (best_cost < 0 || cost < best_cost) {
+            best = c;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 
 template <typename TQ, typename TI, int D, int PASS>

@@ -1,12 +1,14 @@
-// Tensor-core (tcgen05) variant of the two scoring passes of Eq. (10), KVMem
-// (Virtualizing Million-Token Agent Workspaces on a Consumer GPU) §4.3, for
-// bf16 queries and a bf16 Mean-K index.
+// Tensor-core (tcgen05) pass 2 of Eq. (10), KVMem (Virtualizing Million-Token
+// Agent Workspaces on a Consumer GPU) §4.3, for bf16 queries and a bf16
+// Mean-K index: for every block of a chunk, the sum over the query rows of one
+// (layer l, kv head g) of its softmax probability 2^(s*c - M - log2 Z), with
+// the per-row M and Z of pass 1 (score_tc1.cu).  Also the host helpers both
+// tensor-core passes share.
 //
-// For one (layer l, kv head g) the scaled scores are a dense contraction
-// S = Q_g . Kbar^T with Q_g the rows x d query rows that read kv head g and
-// Kbar a tile of 128 Mean-K vectors.  Products of bf16 values are exact in
-// fp32 and the tensor cores accumulate in fp32, so only the summation order
-// differs from the CUDA-core variant.
+// The scaled scores are the dense contraction D[block][query row] = Kbar . Q_g^T
+// (M = 128 blocks, N = rows rounded up to 16).  Products of bf16 values are
+// exact in fp32 and the tensor cores accumulate in fp32, so only the summation
+// order differs from the CUDA-core variant.
 //
 // CTA = 18 warps, one SM (the shared-memory ring and the 512 TMEM columns):
 //   warp 0       TMA producer: 128-block index tiles into a 4-stage ring of
@@ -14,17 +16,13 @@
 //   warp 1       MMA issuer: one thread issues tcgen05.mma into one of two TMEM
 //                accumulators and commits to mbarriers
 //   warps 2..17  epilogue, four warps per TMEM lane quadrant, each taking a
-//                quarter of the accumulator's columns; the four combine in a
-//                fixed order through shared memory, handed over with mbarriers.
+//                quarter of the accumulator's columns; each thread owns one
+//                block and sums its quarter of the rows in registers, and the
+//                four quarters combine in a fixed order through shared memory.
 //                An accumulator goes back to the MMA warp as soon as it has
 //                been read into registers, before the exponentials.
-// Pass 1 computes D[query row][block] (M = 128 query rows per tile, N = 128
-// blocks): each epilogue thread owns one query row and keeps a reference and
-// the partition sum relative to it in registers -- no cross-thread reduction.
-// Pass 2 computes D[block][query row] (M = 128 blocks, N = rows rounded to 16):
-// each thread owns one block and sums 2^(s*c - M - log2 Z) over its query rows
-// in registers.  Every mbarrier wait is bounded; on timeout the kernel raises
-// the device error flag (bit 4) and winds down, freeing its TMEM.
+// Every mbarrier wait is bounded; on timeout the kernel raises the device
+// error flag (bit 4) and winds down, freeing its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -43,8 +41,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kQRows = 256;         // query rows padded to two M = 128 tiles
-constexpr int kPrefetch = 4;        // tiles fetched into L2 ahead of the shared-memory ring
+constexpr int kQRows = 256;         // largest N (query rows per kv head)
 
 template <int D>
 struct Lay {
@@ -56,9 +53,8 @@ struct Lay {
     static constexpr int OFF_Q = kStages * TILE;
     static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
     static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 1536 floats
-    static constexpr int OFF_D = OFF_X + 1536 * 4;     // 2 x 32 x 2 floats
-    static constexpr int OFF_BAR = OFF_D + 2 * 32 * 2 * 4;
-    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static constexpr int OFF_BAR = OFF_X + 1536 * 4;
+    static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
 // Sum of 2^(v*c + no) over n loaded columns (n a multiple of 16, at most 64;
@@ -108,89 +104,16 @@ __device__ __forceinline__ float exp_sum_n(const uint32_t *r, const float *no, f
     return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
-// Online softmax statistics of one query row over the first nv of NV loaded
-// scores: running max m (log2 units) and the partition sum z rescaled to it.
-template <int NV>
-__device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c, float &m,
-                                              float &z) {
-    if (nv <= 0) return;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-    if (nv == NV) {
-#pragma unroll
-        for (int k = 0; k < NV; k += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-            mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (k < nv) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-    }
-    const float mn = fmaxf(m, fmaxf(mx0, mx1) * c);
-    float zs;
-    if (nv == NV) {
-        const float2 c2 = make_float2(c, c), nm2 = make_float2(-mn, -mn);
-        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < NV; k += 4) {
-            const float2 x01 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2, nm2);
-            const float2 x23 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2, nm2);
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
-        }
-        zs = (a0.x + a0.y) + (a1.x + a1.y);
-    } else {
-        zs = 0.f;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (k < nv) zs += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
-    }
-    z = z * fast_exp2(m - mn) + zs;
-    m = mn;
-}
-
-// Row statistics with the reference held fixed: while every term of a full
-// tile stays below 2^64 relative to the row's current reference m, the tile
-// only adds its terms to z (no max over the tile).  A larger term, the row's
-// first tile and a ragged tile take the exact online update, which moves m to
-// the running maximum.  (m, z) stays an exact pair for any m: the partition sum
-// is z * 2^m, and pass 2 divides by it through m + log2 z.
-template <int NV>
-__device__ __forceinline__ void row_update(const uint32_t *r, int nv, float c, float &m,
-                                           float &z) {
-    if (nv == NV && m != -INFINITY) {
-        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
-        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < NV; k += 4) {
-            const float2 x01 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2, nm2);
-            const float2 x23 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2, nm2);
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
-        }
-        const float zs = (a0.x + a0.y) + (a1.x + a1.y);
-        if (zs <= 0x1p64f) {   // false for inf and NaN as well
-            z += zs;
-            return;
-        }
-    }
-    online_update<NV>(r, nv, c, m, z);
-}
-
 }  // namespace
 
-// NC: columns per epilogue warp in pass 2 when fixed at compile time (48 for
-// 192 query rows), 0 for any row count.
-template <int D, int PASS, int NC>
+// NC: columns per epilogue warp when fixed at compile time (48 for 192 query
+// rows), 0 for any row count.
+template <int D, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *__restrict__ q,
-                ScoreShape sh, int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
-                int64_t chunk_blocks, ScoreScratch scr, int64_t partial_stride,
-                float scale_log2, int *err) {
+score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
+                      const __nv_bfloat16 *__restrict__ q, ScoreShape sh, int64_t b_index0,
+                      int64_t b_begin, int64_t b_end, int64_t chunk_blocks, ScoreScratch scr,
+                      int64_t partial_stride, float scale_log2, int *err) {
     using LY = Lay<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -199,15 +122,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     uint8_t *qs = smem + LY::OFF_Q;
     float *o_r = reinterpret_cast<float *>(smem + LY::OFF_O);
     float *xch = reinterpret_cast<float *>(smem + LY::OFF_X);
-    float *xdup = reinterpret_cast<float *>(smem + LY::OFF_D);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *xfull = tempty + 2;        // [4][4]: warps 1..3 of a quadrant wrote their partials
-    uint64_t *xfin = xfull + 16;         // [4]: the same for the final pass-1 statistics
-    uint64_t *xdbar = xfin + 4;          // [2]: quadrant 2+q handed its half-row stats to q
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xdbar + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lg = blockIdx.y;
@@ -217,11 +137,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     const int64_t cb0 = b_begin + (int64_t)chunk * chunk_blocks;
     const int64_t cb1 = min(b_end, cb0 + chunk_blocks);
     const int n_tiles = cb1 > cb0 ? (int)((cb1 - cb0 + TB - 1) / TB) : 0;
-    const int n2 = (rows + 15) & ~15;              // pass-2 N
-    const int qtiles = rows > 128 ? 2 : 1;         // pass-1 M tiles
-    // 128 < rows <= 192: the second tile holds rows 128..191 twice (lanes 0-63
-    // and 64-127) so that all four lane quadrants share its columns evenly
-    const bool dup = rows > 128 && rows <= 192;
+    const int n2 = (rows + 15) & ~15;              // MMA N
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -233,8 +149,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             tc::mbar_init(&tempty[b], kEpiWarps * 32);
         }
         for (int k = 0; k < 16; ++k) tc::mbar_init(&xfull[k], 96);
-        for (int k = 0; k < 4; ++k) tc::mbar_init(&xfin[k], 96);
-        for (int k = 0; k < 2; ++k) tc::mbar_init(&xdbar[k], 32);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -244,17 +158,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
     // Query rows of (l, g) into the swizzled K-major layout; padding rows are 0.
     // Each thread issues all of its loads before the first store.
     {
-        constexpr int kQItems = kQRows * (D / 8);
-        constexpr int kPer = (kQItems + kThreads - 1) / kThreads;
+        const int n_items = n2 * (D / 8);
+        constexpr int kPer = (kQRows * (D / 8) + kThreads - 1) / kThreads;
         uint4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i = tid + k * kThreads;
             v[k] = make_uint4(0, 0, 0, 0);
             const int r = i / (D / 8), c16 = i - r * (D / 8);
-            const int src_r = (dup && r >= 192) ? r - 64 : r;
-            if (i < kQItems && src_r < rows) {
-                const int m = src_r / sh.gqa, hl = src_r - m * sh.gqa;
+            if (i < n_items && r < rows) {
+                const int m = r / sh.gqa, hl = r - m * sh.gqa;
                 const __nv_bfloat16 *src = q + (((size_t)l * sh.n_queries + m) * sh.H +
                                                 (size_t)g * sh.gqa + hl) * D + c16 * 8;
                 v[k] = __ldg(reinterpret_cast<const uint4 *>(src));
@@ -263,7 +176,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i = tid + k * kThreads;
-            if (i < kQItems) {
+            if (i < n_items) {
                 const int r = i / (D / 8), c16 = i - r * (D / 8);
                 const int a = c16 >> 3, cc = c16 & 7;
                 *reinterpret_cast<uint4 *>(qs + a * LY::Q_ATOM + r * 128 + ((cc ^ (r & 7)) << 4)) =
@@ -271,15 +184,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             }
         }
     }
-    if (PASS == 2) {
-        for (int r = tid; r < kQRows; r += kThreads) {
-            float o = INFINITY;
-            if (r < rows) {
-                const size_t k = (size_t)lg * rows + r;
-                o = scr.row_m[k] - log2f(scr.row_invz[k]);   // M + log2 Z, log2 units
-            }
-            o_r[r] = -o;                                     // stored negated
+    for (int r = tid; r < kQRows; r += kThreads) {
+        float o = INFINITY;
+        if (r < rows) {
+            const size_t k = (size_t)lg * rows + r;
+            o = scr.row_m[k] - log2f(scr.row_invz[k]);   // M + log2 Z, log2 units
         }
+        o_r[r] = -o;                                     // stored negated
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -289,22 +200,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
 
     if (warp == 0) {
         if (lane == 0) {
-            auto tile_y = [&](int i) {
-                return (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
-            };
-            // The ring holds a tile from its load until its MMA completes; L2
-            // prefetches keep later tiles in flight from HBM meanwhile.
-            for (int i = kStages; i < min(n_tiles, kStages + kPrefetch); ++i)
-                for (int a = 0; a < LY::KA; ++a) tc::tma_prefetch_2d(&tmap, a * 64, tile_y(i));
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
-                if (i + kStages + kPrefetch - 1 < n_tiles && i >= 1)
-                    for (int a = 0; a < LY::KA; ++a)
-                        tc::tma_prefetch_2d(&tmap, a * 64, tile_y(i + kStages + kPrefetch - 1));
                 if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
                 tc::mbar_expect_tx(&full[s], LY::TILE);
-                const int32_t y = tile_y(i);
+                const int32_t y =
+                    (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
 #pragma unroll
                 for (int a = 0; a < LY::KA; ++a)
                     tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
@@ -315,6 +217,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
         if (lane == 0) {
             const uint32_t qbase = tc::smem_u32(qs);
             const uint32_t tbase = tc::smem_u32(tiles);
+            const uint32_t idesc = tc::idesc_bf16_f32(128, n2);
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
@@ -325,31 +228,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
                 tc::tc_fence_after();
                 const uint32_t d = tmem + buf * 256;
                 const uint32_t tile = tbase + s * LY::TILE;
-                if (PASS == 1) {
-                    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, TB);
-                    for (int t = 0; t < qtiles; ++t) {
 #pragma unroll
-                        for (int a = 0; a < LY::KA; ++a) {
+                for (int a = 0; a < LY::KA; ++a) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = tc::sdesc_sw128(
-                                    qbase + a * LY::Q_ATOM + t * 128 * 128 + kk * 32);
-                                const uint64_t bd =
-                                    tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
-                                tc::mma_bf16(d + t * 128, ad, bd, idesc, (a | kk) != 0);
-                            }
-                        }
-                    }
-                } else {
-                    const uint32_t idesc = tc::idesc_bf16_f32(128, n2);
-#pragma unroll
-                    for (int a = 0; a < LY::KA; ++a) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
-                            const uint64_t bd = tc::sdesc_sw128(qbase + a * LY::Q_ATOM + kk * 32);
-                            tc::mma_bf16(d, ad, bd, idesc, (a | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
+                        const uint64_t bd = tc::sdesc_sw128(qbase + a * LY::Q_ATOM + kk * 32);
+                        tc::mma_bf16(d, ad, bd, idesc, (a | kk) != 0);
                     }
                 }
                 tc::mma_commit(&empty[s]);
@@ -362,15 +247,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
         const int sub = ew >> 2;                    // which quarter of the columns
         const int lrow = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        // pass 2: the n2 columns in 16-column units, split into four near-equal runs
+        // the n2 columns in 16-column units, split into four near-equal runs
         const int nu = n2 >> 4;
         const int u0 = (sub * nu) >> 2, u1 = ((sub + 1) * nu) >> 2;
-        const int my_c0 = PASS == 2 ? u0 * 16 : sub * 32;
-        const int my_nc = PASS == 2 ? (u1 - u0) * 16 : 32;
-        // pass 1, duplicated second tile: quadrants 0-1 take its columns 0-63,
-        // quadrants 2-3 columns 64-127, sixteen per warp
-        const int c1 = (quad >= 2 ? 64 : 0) + sub * 16;
-        float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
+        const int my_c0 = u0 * 16;
+        const int my_nc = (u1 - u0) * 16;
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i & 1;
             const uint32_t bph = (i >> 1) & 1;
@@ -379,131 +260,49 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16 *_
             const int64_t gb0 = cb0 + (int64_t)i * TB;
             const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
             const uint32_t taddr = tmem + lane_base + buf * 256;
-            if (PASS == 1) {
-                // this warp's 32 columns of each query-row tile, both loads in flight
-                uint32_t r[64];
+            uint32_t r[64];
+            float sum;
+            if (NC == 48) {   // 192 query rows: 48 columns per warp
                 tc::tmem_ld32_async(taddr + my_c0, r);
-                if (qtiles > 1) {
-                    if (dup) tc::tmem_ld16_async(taddr + 128 + c1, r + 32);
-                    else tc::tmem_ld32_async(taddr + 128 + my_c0, r + 32);
-                }
+                tc::tmem_ld16_async(taddr + my_c0 + 32, r + 32);
                 tc::tmem_wait_ld(r);
                 tc::tmem_wait_ld(r + 16);
-                if (qtiles > 1) {
-                    tc::tmem_wait_ld(r + 32);
-                    if (!dup) tc::tmem_wait_ld(r + 48);
-                }
-                // the accumulator is in registers: hand the buffer back to the MMA warp
+                tc::tmem_wait_ld(r + 32);
                 tc::tc_fence_before();
                 tc::mbar_arrive(&tempty[buf]);
-                const int nv = min(32, max(0, nvalid - my_c0));
-                row_update<32>(r, nv, scale_log2, m_run[0], z_run[0]);
-                if (qtiles > 1) {
-                    if (dup)
-                        row_update<16>(r + 32, min(16, max(0, nvalid - c1)), scale_log2,
-                                       m_run[1], z_run[1]);
-                    else
-                        row_update<32>(r + 32, nv, scale_log2, m_run[1], z_run[1]);
-                }
+                sum = exp_sum_n<48>(r, o_r + my_c0, scale_log2);
             } else {
-                uint32_t r[64];
-                float sum;
-                if (NC == 48) {   // 192 query rows: 48 columns per warp
-                    tc::tmem_ld32_async(taddr + my_c0, r);
-                    tc::tmem_ld16_async(taddr + my_c0 + 32, r + 32);
-                    tc::tmem_wait_ld(r);
-                    tc::tmem_wait_ld(r + 16);
-                    tc::tmem_wait_ld(r + 32);
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&tempty[buf]);
-                    sum = exp_sum_n<48>(r, o_r + my_c0, scale_log2);
-                } else {
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        if (k * 32 + 32 <= my_nc)
-                            tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
-                        else if (k * 32 + 16 <= my_nc)
-                            tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
-                    }
+                for (int k = 0; k < 2; ++k) {
+                    if (k * 32 + 32 <= my_nc)
+                        tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
+                    else if (k * 32 + 16 <= my_nc)
+                        tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
+                }
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&tempty[buf]);
-                    sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
-                }
-                // the quadrant's four warps combine in a fixed order through a
-                // four-deep ring of shared-memory slots.  A slot is not rewritten
-                // before warp 0 of the quadrant read it: tile i + 4 needs that
-                // warp's arrival on tempty for tile i + 2, which follows its read.
-                const int xs = i & 3;
-                const uint32_t xph = (i >> 2) & 1;
-                float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
-                if (sub) {
-                    slot[(sub - 1) * 32] = sum;
-                    tc::mbar_arrive(&xfull[xs * 4 + quad]);
-                } else {
-                    if (!tc::mbar_wait(&xfull[xs * 4 + quad], xph, kWaitLimit)) {
-                        atomicOr(err, 4);
-                        break;
-                    }
-                    sum = ((sum + slot[0]) + slot[32]) + slot[64];
-                    if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
-                }
+                for (int k = 0; k < 4; ++k)
+                    if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
+                tc::tc_fence_before();
+                tc::mbar_arrive(&tempty[buf]);
+                sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
             }
-        }
-        if (PASS == 1) {
-            // [t][quad][sub-1][lane] (m, z)
-            float *slot = xch + ((quad * 3) * 32 + lane) * 2;
+            // the quadrant's four warps combine in a fixed order through a
+            // four-deep ring of shared-memory slots.  A slot is not rewritten
+            // before warp 0 of the quadrant read it: tile i + 4 needs that
+            // warp's arrival on tempty for tile i + 2, which follows its read.
+            const int xs = i & 3;
+            const uint32_t xph = (i >> 2) & 1;
+            float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
             if (sub) {
-                for (int t = 0; t < qtiles; ++t) {
-                    slot[(t * 12 + sub - 1) * 64] = m_run[t];
-                    slot[(t * 12 + sub - 1) * 64 + 1] = z_run[t];
-                }
-                tc::mbar_arrive(&xfin[quad]);
-            } else if (!tc::mbar_wait(&xfin[quad], 0, kWaitLimit)) {
-                atomicOr(err, 4);
+                slot[(sub - 1) * 32] = sum;
+                tc::mbar_arrive(&xfull[xs * 4 + quad]);
             } else {
-                float M[2], Z[2];
-                for (int t = 0; t < qtiles; ++t) {
-                    M[t] = m_run[t];
-                    for (int k = 0; k < 3; ++k) M[t] = fmaxf(M[t], slot[(t * 12 + k) * 64]);
-                    Z[t] = 0.f;
-                    if (M[t] != -INFINITY) {
-                        Z[t] = z_run[t] * fast_exp2(m_run[t] - M[t]);
-                        for (int k = 0; k < 3; ++k)
-                            Z[t] += slot[(t * 12 + k) * 64 + 1] *
-                                    fast_exp2(slot[(t * 12 + k) * 64] - M[t]);
-                    }
+                if (!tc::mbar_wait(&xfull[xs * 4 + quad], xph, kWaitLimit)) {
+                    atomicOr(err, 4);
+                    break;
                 }
-                auto emit = [&](int r, float m, float z) {
-                    if (r < rows) {
-                        const size_t o = ((size_t)lg * sh.chunk_cap + chunk0 + chunk) * rows + r;
-                        scr.part_m[o] = m;
-                        scr.part_z[o] = z;
-                    }
-                };
-                emit(lrow, M[0], Z[0]);
-                if (qtiles > 1) {
-                    if (!dup) {
-                        emit(128 + lrow, M[1], Z[1]);
-                    } else if (quad >= 2) {
-                        // the other half of rows 128 + 32*(quad-2) + lane goes to quadrant quad-2
-                        xdup[((quad - 2) * 32 + lane) * 2] = M[1];
-                        xdup[((quad - 2) * 32 + lane) * 2 + 1] = Z[1];
-                        tc::mbar_arrive(&xdbar[quad - 2]);
-                    } else if (!tc::mbar_wait(&xdbar[quad], 0, kWaitLimit)) {
-                        atomicOr(err, 4);
-                    } else {
-                        const float m2 = xdup[(quad * 32 + lane) * 2];
-                        const float z2 = xdup[(quad * 32 + lane) * 2 + 1];
-                        const float Mx = fmaxf(M[1], m2);
-                        float Zx = 0.f;
-                        if (Mx != -INFINITY)
-                            Zx = Z[1] * fast_exp2(M[1] - Mx) + z2 * fast_exp2(m2 - Mx);
-                        emit(128 + lrow, Mx, Zx);
-                    }
-                }
+                sum = ((sum + slot[0]) + slot[32]) + slot[64];
+                if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
             }
         }
     }
@@ -530,13 +329,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D view of an index buffer: rows = LG * index_cap Mean-K vectors of d bf16.
-static bool make_index_map(CUtensorMap *m, const void *index, int d, int64_t n_rows) {
+bool make_index_map(CUtensorMap *m, const void *index, int d, int64_t n_rows, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n_rows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    cuuint32_t box[2] = {64, TB};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(index), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -550,16 +348,16 @@ bool score_tc_supported(int q_dtype, int index_dtype, const ScoreShape &sh) {
            sh.rows >= 1 && sh.rows <= kQRows && encode_fn() != nullptr;
 }
 
-template <int D, int PASS, int NC>
-static cudaError_t tc_t(const ScoreShape &sh, const void *q, const void *index, int64_t b_index0,
-                        int64_t b_begin, int64_t b_end, int chunk0, int n_chunks,
-                        const ScoreScratch &scr, int64_t partial_stride, int *err,
-                        cudaStream_t s) {
+template <int D, int NC>
+static cudaError_t pass2_t(const ScoreShape &sh, const void *q, const void *index,
+                           int64_t b_index0, int64_t b_begin, int64_t b_end, int n_chunks,
+                           const ScoreScratch &scr, int64_t partial_stride, int *err,
+                           cudaStream_t s) {
     CUtensorMap map;
     if (((uintptr_t)index & 15) != 0) return cudaErrorMisalignedAddress;
-    if (!make_index_map(&map, index, D, (int64_t)sh.L * sh.G * sh.index_cap))
+    if (!make_index_map(&map, index, D, (int64_t)sh.L * sh.G * sh.index_cap, TB))
         return cudaErrorInvalidValue;
-    auto kern = score_tc_kernel<D, PASS, NC>;
+    auto kern = score_tc_pass2_kernel<D, NC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay<D>::SMEM);
     if (e != cudaSuccess) return e;
@@ -568,20 +366,9 @@ static cudaError_t tc_t(const ScoreShape &sh, const void *q, const void *index, 
     dim3 grid((unsigned)n_chunks, (unsigned)(sh.L * sh.G));
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
     kern<<<grid, kThreads, Lay<D>::SMEM, s>>>(map, static_cast<const __nv_bfloat16 *>(q), sh,
-                                              b_index0, b_begin, b_end, chunk0, chunk_blocks,
-                                              scr, partial_stride, scale_log2, err);
+                                              b_index0, b_begin, b_end, chunk_blocks, scr,
+                                              partial_stride, scale_log2, err);
     return cudaGetLastError();
-}
-
-cudaError_t launch_score_pass1_tc(const ScoreShape &sh, const void *q, const void *index,
-                                  int64_t b_index0, int64_t b_begin, int64_t b_end, int chunk0,
-                                  int n_chunks, const ScoreScratch &scr, int *err,
-                                  cudaStream_t s) {
-    if (sh.d == 128)
-        return tc_t<128, 1, 0>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0,
-                               err, s);
-    return tc_t<64, 1, 0>(sh, q, index, b_index0, b_begin, b_end, chunk0, n_chunks, scr, 0, err,
-                          s);
 }
 
 cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const void *index,
@@ -590,13 +377,13 @@ cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const voi
                                   cudaStream_t s) {
     const bool n48 = ((sh.rows + 15) & ~15) == 192;
     if (sh.d == 128)
-        return n48 ? tc_t<128, 2, 48>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+        return n48 ? pass2_t<128, 48>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
                                       partial_stride, err, s)
-                   : tc_t<128, 2, 0>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+                   : pass2_t<128, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
                                      partial_stride, err, s);
-    return n48 ? tc_t<64, 2, 48>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+    return n48 ? pass2_t<64, 48>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
                                  partial_stride, err, s)
-               : tc_t<64, 2, 0>(sh, q, index, b_index0, b_begin, b_end, 0, n_chunks, scr,
+               : pass2_t<64, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
                                 partial_stride, err, s);
 }
 
