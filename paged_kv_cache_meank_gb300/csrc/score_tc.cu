@@ -252,13 +252,28 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
         const int u0 = (sub * nu) >> 2, u1 = ((sub + 1) * nu) >> 2;
         const int my_c0 = u0 * 16;
         const int my_nc = (u1 - u0) * 16;
+        // warp 0 of a quadrant combines tile i - 1 while on tile i, when the
+        // other three warps' partials of tile i - 1 are long written
+        float pend = 0.f;
+        auto combine = [&](int j, float own) -> bool {
+            const int xs = j & 3;
+            if (!tc::mbar_wait(&xfull[xs * 4 + quad], (j >> 2) & 1, kWaitLimit)) return false;
+            const float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
+            const float sum = ((own + slot[0]) + slot[32]) + slot[64];
+            const int64_t gb0 = cb0 + (int64_t)j * TB;
+            if (lrow < min((int64_t)TB, cb1 - gb0))
+                scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
+            return true;
+        };
+        bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i & 1;
             const uint32_t bph = (i >> 1) & 1;
-            if (!tc::mbar_wait(&tfull[buf], bph, kWaitLimit)) { atomicOr(err, 4); break; }
+            if (!tc::mbar_wait(&tfull[buf], bph, kWaitLimit)) {
+                ok = false;
+                break;
+            }
             tc::tc_fence_after();
-            const int64_t gb0 = cb0 + (int64_t)i * TB;
-            const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
             const uint32_t taddr = tmem + lane_base + buf * 256;
             uint32_t r[64];
             float sum;
@@ -288,23 +303,22 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
             }
             // the quadrant's four warps combine in a fixed order through a
             // four-deep ring of shared-memory slots.  A slot is not rewritten
-            // before warp 0 of the quadrant read it: tile i + 4 needs that
-            // warp's arrival on tempty for tile i + 2, which follows its read.
-            const int xs = i & 3;
-            const uint32_t xph = (i >> 2) & 1;
-            float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
+            // before warp 0 of the quadrant read it: tile i + 3 needs that
+            // warp's arrival on tempty for tile i + 1, which follows its read
+            // of tile i's slots.
             if (sub) {
-                slot[(sub - 1) * 32] = sum;
-                tc::mbar_arrive(&xfull[xs * 4 + quad]);
+                xch[(((i & 3) * 4 + quad) * 3 + sub - 1) * 32 + lane] = sum;
+                tc::mbar_arrive(&xfull[(i & 3) * 4 + quad]);
             } else {
-                if (!tc::mbar_wait(&xfull[xs * 4 + quad], xph, kWaitLimit)) {
-                    atomicOr(err, 4);
+                if (i > 0 && !combine(i - 1, pend)) {
+                    ok = false;
                     break;
                 }
-                sum = ((sum + slot[0]) + slot[32]) + slot[64];
-                if (lrow < nvalid) scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
+                pend = sum;
             }
         }
+        if (sub == 0 && n_tiles > 0 && ok && !combine(n_tiles - 1, pend)) ok = false;
+        if (!ok) atomicOr(err, 4);
     }
     tc::tc_fence_before();
     __syncthreads();
