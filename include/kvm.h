@@ -93,6 +93,13 @@ typedef struct {
                                 change, at most n times in a row, then rebuild from raw K.
                                 Each delta adds at most one rounding of the pair's
                                 magnitude, so n bounds the error growth. */
+    int32_t candidate_mode;  /* the candidate set C of Eq. (10) ([KVMem] §4.3):
+                                0 = every indexed block (the softmax of each query
+                                row covers all N blocks; sink and recent blocks are
+                                only kept out of the top-k fill);
+                                1 = only the blocks the selector may still choose,
+                                [sink_blocks, N - recent_blocks): the softmax covers
+                                those, and sink / recent blocks score 0. */
 } kvm_config;
 
 typedef struct kvm_ctx kvm_ctx;

@@ -225,6 +225,27 @@ def block_relevance(q: np.ndarray, index: np.ndarray, n_blocks: int,
     return R
 
 
+def candidate_range(n_blocks: int, sink: int, recent: int):
+    """The blocks that are neither sink [0, S) nor recent [N-W, N): the
+    half-open range [c0, c1) (empty when the reserved blocks cover all)."""
+    c0 = min(sink, n_blocks)
+    c1 = max(n_blocks - recent, c0)
+    return c0, c1
+
+
+def block_relevance_excl(q: np.ndarray, index: np.ndarray, n_blocks: int, sink: int,
+                         recent: int) -> np.ndarray:
+    """The other reading of the candidate set C of Eq. (10): only the blocks the
+    selector may still choose, i.e. without the sink and recent blocks that it
+    keeps anyway ([KVMem] §4.3).  The softmax of every (l, m, h) runs over those
+    blocks alone; sink and recent blocks get R_b = 0."""
+    c0, c1 = candidate_range(n_blocks, sink, recent)
+    R = np.zeros(n_blocks)
+    if c1 > c0:
+        R[c0:c1] = block_relevance(q, index[:, :, c0:c1], c1 - c0)
+    return R
+
+
 def block_relevance_tiled(q: np.ndarray, index: np.ndarray, n_blocks: int, tile: int):
     """Eq. (10) evaluated tile by tile with the global softmax kept across
     tiles ([KVMem] §5, tiled retrieval): a first sweep over the tiles keeps a

@@ -35,10 +35,12 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
                pool_pages: int | None = None, index_location: int | None = None,
                repo_location: int | None = None, h2d_batch_blocks: int = 64,
                max_queries: int | None = None, score_variant: int = 0,
-               h2d_mode: int = 1, delta_rerope_limit: int = 0) -> KvmConfig:
+               h2d_mode: int = 1, delta_rerope_limit: int = 0,
+               candidate_mode: int = 0) -> KvmConfig:
     """A kvm_config for a workload shape.  With a host-resident repository the
     GPU reads missed blocks from pinned host memory itself (h2d_mode 1) unless
-    h2d_mode=0 asks for copy-engine transfers."""
+    h2d_mode=0 asks for copy-engine transfers.  candidate_mode=1 leaves sink and
+    recent blocks out of the Eq. (10) softmax."""
     mb = max_blocks if max_blocks is not None else wl.n_blocks + wl.steps * wl.append_blocks
     mp = max_positions if max_positions is not None else max(mb, wl.view_blocks) * BLOCK_TOKENS
     il = index_location if index_location is not None else (
@@ -54,7 +56,8 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         max_positions=mp, tile_blocks=wl.tile_blocks,
         pool_pages=pool_pages if pool_pages is not None else wl.view_blocks + wl.append_blocks,
         index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
-        h2d_mode=h2d_mode, score_variant=score_variant, delta_rerope_limit=delta_rerope_limit)
+        h2d_mode=h2d_mode, score_variant=score_variant, delta_rerope_limit=delta_rerope_limit,
+        candidate_mode=candidate_mode)
 
 
 def _ptr(t) -> int | None:

@@ -30,7 +30,7 @@ class KvmConfig(ctypes.Structure):
         ("pool_pages", ctypes.c_int32), ("index_location", ctypes.c_int32),
         ("repo_location", ctypes.c_int32), ("h2d_batch_blocks", ctypes.c_int32),
         ("h2d_mode", ctypes.c_int32), ("score_variant", ctypes.c_int32),
-        ("delta_rerope_limit", ctypes.c_int32),
+        ("delta_rerope_limit", ctypes.c_int32), ("candidate_mode", ctypes.c_int32),
     ]
 
 

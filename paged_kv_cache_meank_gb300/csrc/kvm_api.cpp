@@ -85,6 +85,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->score_variant != 0 && c->score_variant != 1) return bad("score_variant must be 0 or 1");
     if (c->h2d_mode != 0 && c->h2d_mode != 1) return bad("h2d_mode must be 0 or 1");
     if (c->delta_rerope_limit < 0) return bad("delta_rerope_limit must be >= 0");
+    if (c->candidate_mode != 0 && c->candidate_mode != 1) return bad("candidate_mode must be 0 or 1");
     return true;
 }
 
@@ -299,19 +300,25 @@ kvm_status kvm_build_index(kvm_ctx *c, const void *k_pages, int64_t first_block,
     return KVM_OK;
 }
 
+// Blocks [c0, c1) are scored (the candidate set); the rest of [0, N) get 0.
 static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void *q,
-                               const void *index, int64_t N, float *scores, cudaStream_t s) {
-    const int nch = kvm::score_chunks(sh, N, kvm::kMaxChunks);
+                               const void *index, int64_t N, int64_t c0, int64_t c1,
+                               float *scores, cudaStream_t s) {
     cudaError_t e;
-    if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0, 0, N,
-                                     0, nch, c->scr, s)) != cudaSuccess)
-        return cuda_fail(e, "score pass 1");
-    if ((e = kvm::launch_score_combine(sh, nch, c->scr, s)) != cudaSuccess)
-        return cuda_fail(e, "score combine");
-    if ((e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0, 0, N,
-                                     nch, c->scr, c->cfg.max_blocks, s)) != cudaSuccess)
-        return cuda_fail(e, "score pass 2");
-    if ((e = kvm::launch_score_reduce(sh, N, c->scr, c->cfg.max_blocks, scores, s)) != cudaSuccess)
+    if (c1 > c0) {
+        const int nch = kvm::score_chunks(sh, c1 - c0, kvm::kMaxChunks);
+        if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0,
+                                         c0, c1, 0, nch, c->scr, s)) != cudaSuccess)
+            return cuda_fail(e, "score pass 1");
+        if ((e = kvm::launch_score_combine(sh, nch, c->scr, s)) != cudaSuccess)
+            return cuda_fail(e, "score combine");
+        if ((e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0,
+                                         c0, c1, nch, c->scr, c->cfg.max_blocks, s)) !=
+            cudaSuccess)
+            return cuda_fail(e, "score pass 2");
+    }
+    if ((e = kvm::launch_score_reduce(sh, N, c0, c1, c->scr, c->cfg.max_blocks, scores, s)) !=
+        cudaSuccess)
         return cuda_fail(e, "score reduce");
     return KVM_OK;
 }
@@ -321,7 +328,8 @@ static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void
 // records per-chunk (max, sum) and the combine folds every tile's chunks
 // before pass 2 re-streams the tiles (KVMem §5, tiled retrieval).
 static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q,
-                                   const void *index, int64_t N, float *scores, cudaStream_t s) {
+                                   const void *index, int64_t N, int64_t c0, int64_t c1,
+                                   float *scores, cudaStream_t s) {
     const int64_t tile = c->cfg.tile_blocks;
     const int64_t T = (N + tile - 1) / tile;
     const int cpt = std::max(1, std::min(kvm::score_chunks(sh, tile, kvm::kMaxChunks),
@@ -334,10 +342,14 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
     KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0));
     kvm::ScoreShape tsh = sh;
     tsh.index_cap = tile;
-    for (int pass = 1; pass <= 2; ++pass) {
+    for (int pass = 1; pass <= 2 && c1 > c0; ++pass) {
         for (int64_t t = 0; t < T; ++t) {
             const int buf = (int)(t & 1);
             const int64_t b0 = t * tile, nb = std::min(tile, N - b0);
+            // the tile's part of the candidate range; an empty part still runs
+            // pass 1 so that its chunks hold (-inf, 0) for the combine
+            const int64_t lo = std::min(std::max(b0, c0), b0 + nb);
+            const int64_t hi = std::max(std::min(b0 + nb, c1), lo);
             KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
             KVM_CUDA(cudaMemcpy2DAsync(c->stage[buf], tile * row,
                                        static_cast<const char *>(index) + b0 * row,
@@ -347,11 +359,11 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
             KVM_CUDA(cudaStreamWaitEvent(s, c->ev_ready[buf], 0));
             if (pass == 1)
                 e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
-                                            c->stage[buf], b0, b0, b0 + nb, (int)(t * cpt), cpt,
+                                            c->stage[buf], b0, lo, hi, (int)(t * cpt), cpt,
                                             c->scr, s);
             else
                 e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
-                                            c->stage[buf], b0, b0, b0 + nb, cpt, c->scr,
+                                            c->stage[buf], b0, lo, hi, cpt, c->scr,
                                             c->cfg.max_blocks, s);
             if (e != cudaSuccess) return cuda_fail(e, "tiled score pass");
             KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
@@ -359,7 +371,8 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
         if (pass == 1 && (e = kvm::launch_score_combine(sh, (int)(T * cpt), c->scr, s)) != cudaSuccess)
             return cuda_fail(e, "score combine");
     }
-    if ((e = kvm::launch_score_reduce(sh, N, c->scr, c->cfg.max_blocks, scores, s)) != cudaSuccess)
+    if ((e = kvm::launch_score_reduce(sh, N, c0, c1, c->scr, c->cfg.max_blocks, scores, s)) !=
+        cudaSuccess)
         return cuda_fail(e, "score reduce");
     return KVM_OK;
 }
@@ -378,9 +391,14 @@ kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const 
                     (long long)c->cfg.max_blocks);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const kvm::ScoreShape sh = shape_of(c, n_queries, c->cfg.max_blocks);
+    int64_t c0 = 0, c1 = n_blocks;
+    if (c->cfg.candidate_mode == 1) {
+        c0 = std::min<int64_t>(c->cfg.sink_blocks, n_blocks);
+        c1 = std::max<int64_t>(n_blocks - c->cfg.recent_blocks, c0);
+    }
     kvm_status st = c->cfg.index_location == KVM_DEVICE
-                        ? score_device(c, sh, q, index, n_blocks, scores_out, s)
-                        : score_host_tiled(c, sh, q, index, n_blocks, scores_out, s);
+                        ? score_device(c, sh, q, index, n_blocks, c0, c1, scores_out, s)
+                        : score_host_tiled(c, sh, q, index, n_blocks, c0, c1, scores_out, s);
     if (st != KVM_OK) return st;
     const cudaError_t e = kvm::launch_select(scores_out, n_blocks, c->cfg.sink_blocks,
                                              c->cfg.recent_blocks, c->cfg.view_blocks,

@@ -93,7 +93,8 @@ cudaError_t launch_score_pass2(int q_dtype, int index_dtype, const ScoreShape &s
                                int64_t b_begin, int64_t b_end, int n_chunks,
                                const ScoreScratch &scr, int64_t partial_stride,
                                cudaStream_t s);
-cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks,
+// Scores of [0, n_blocks): the partial sums over (l, g) for [c0, c1), 0 elsewhere.
+cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t c0, int64_t c1,
                                 const ScoreScratch &scr, int64_t partial_stride,
                                 float *scores_out, cudaStream_t s);
 // Number of chunks used for a range of n blocks.

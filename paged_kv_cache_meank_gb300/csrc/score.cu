@@ -262,23 +262,27 @@ cudaError_t launch_score_combine(const ScoreShape &sh, int n_chunks_total,
     return cudaGetLastError();
 }
 
-__global__ void score_reduce_kernel(int LG, float inv_lh, int64_t n_blocks,
-                                    const float *__restrict__ partial, int64_t stride,
-                                    float *__restrict__ out) {
+// R_b = (1 / (L H)) * sum over (l, g) of the pass-2 partials, for the scored
+// blocks [c0, c1); blocks outside the candidate set get 0.
+__global__ void score_reduce_kernel(int LG, float inv_lh, int64_t n_blocks, int64_t c0,
+                                    int64_t c1, const float *__restrict__ partial,
+                                    int64_t stride, float *__restrict__ out) {
     for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < n_blocks;
          b += (int64_t)gridDim.x * blockDim.x) {
         float s = 0.f;
-        for (int lg = 0; lg < LG; ++lg) s += partial[(size_t)lg * stride + b];
+        if (b >= c0 && b < c1)
+            for (int lg = 0; lg < LG; ++lg) s += partial[(size_t)lg * stride + b];
         out[b] = s * inv_lh;
     }
 }
 
-cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, const ScoreScratch &scr,
-                                int64_t partial_stride, float *scores_out, cudaStream_t s) {
+cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t c0, int64_t c1,
+                                const ScoreScratch &scr, int64_t partial_stride,
+                                float *scores_out, cudaStream_t s) {
     int64_t blocks = (n_blocks + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
     const float inv_lh = (float)(1.0 / ((double)sh.L * sh.H));
-    score_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(sh.L * sh.G, inv_lh, n_blocks,
+    score_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(sh.L * sh.G, inv_lh, n_blocks, c0, c1,
                                                          scr.partial, partial_stride,
                                                          scores_out);
     return cudaGetLastError();

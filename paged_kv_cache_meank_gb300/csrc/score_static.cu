@@ -86,6 +86,8 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     if (cfg->sink_blocks < 0 || cfg->recent_blocks < 0 ||
         cfg->view_blocks < cfg->sink_blocks + cfg->recent_blocks + 1)
         return bad(KVM_ERR_INVALID_ARG, "view_blocks must be >= sink + recent + 1");
+    if (cfg->candidate_mode != 0 && cfg->candidate_mode != 1)
+        return bad(KVM_ERR_INVALID_ARG, "candidate_mode must be 0 or 1");
     if (n_queries < 1 || n_blocks < 1) return bad(KVM_ERR_INVALID_ARG, "empty input");
     if (n_blocks > cfg->max_blocks)
         return bad(KVM_ERR_CAPACITY, "n_blocks beyond max_blocks (the index row stride)");
@@ -133,13 +135,20 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     scr.err = static_cast<int *>(base);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if ((e = kvm::launch_score_pass1(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, 0, n_blocks,
-                                     0, nch, scr, s)) != cudaSuccess ||
-        (e = kvm::launch_score_combine(sh, nch, scr, s)) != cudaSuccess ||
-        (e = kvm::launch_score_pass2(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, 0,
-                                     n_blocks, nch, scr, n_blocks, s)) != cudaSuccess ||
-        (e = kvm::launch_score_reduce(sh, n_blocks, scr, n_blocks, scores_out, s)) != cudaSuccess ||
+    int64_t c0 = 0, c1 = n_blocks;
+    if (cfg->candidate_mode == 1) {
+        c0 = cfg->sink_blocks < n_blocks ? cfg->sink_blocks : n_blocks;
+        c1 = n_blocks - cfg->recent_blocks > c0 ? n_blocks - cfg->recent_blocks : c0;
+    }
+    cudaError_t e = cudaSuccess;
+    if ((c1 > c0 &&
+         ((e = kvm::launch_score_pass1(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, c0, c1,
+                                       0, nch, scr, s)) != cudaSuccess ||
+          (e = kvm::launch_score_combine(sh, nch, scr, s)) != cudaSuccess ||
+          (e = kvm::launch_score_pass2(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, c0, c1,
+                                       nch, scr, n_blocks, s)) != cudaSuccess)) ||
+        (e = kvm::launch_score_reduce(sh, n_blocks, c0, c1, scr, n_blocks, scores_out, s)) !=
+            cudaSuccess ||
         (e = kvm::launch_select(scores_out, n_blocks, cfg->sink_blocks, cfg->recent_blocks,
                                 cfg->view_blocks, sel_ids_out, s)) != cudaSuccess) {
         kvm::set_last_error(std::string("launch: ") + cudaGetErrorString(e));

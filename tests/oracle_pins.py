@@ -257,6 +257,30 @@ def pin_eq10_tiled(o):
         assert np.allclose(o.block_relevance_tiled(q, idx, N, tile), R, rtol=1e-12)
 
 
+def pin_eq10_excluded(o):
+    """Candidate set without the reserved blocks: the softmax covers [S, N-W)
+    only, so those scores sum to M_q, the reserved scores are 0, the reserved
+    blocks' index rows cannot change anything, no reserved blocks give the
+    default reading, and a loop over the candidate blocks agrees."""
+    rng = np.random.default_rng(13)
+    L, M, H, G, d, N, S, W = 2, 3, 4, 2, 8, 14, 2, 3
+    q = rng.standard_normal((L, M, H, d))
+    idx = rng.standard_normal((L, G, N, d))
+    R = o.block_relevance_excl(q, idx, N, S, W)
+    assert abs(R[S:N - W].sum() - M) < 1e-12
+    assert np.all(R[:S] == 0) and np.all(R[N - W:] == 0) and np.all(R[S:N - W] > 0)
+    other = idx.copy()
+    other[:, :, :S] = 7.0 * rng.standard_normal((L, G, S, d))
+    other[:, :, N - W:] = -3.0
+    assert np.array_equal(o.block_relevance_excl(q, other, N, S, W), R)
+    assert np.allclose(o.block_relevance_excl(q, idx, N, 0, 0), o.block_relevance(q, idx, N),
+                       rtol=1e-14, atol=0)
+    Rb = brute.relevance(q.tolist(), idx[:, :, S:N - W].tolist(), H, G)
+    assert np.allclose(R[S:N - W], Rb, rtol=1e-12, atol=1e-15)
+    assert np.all(o.block_relevance_excl(q, idx, 5, 3, 2) == 0)     # nothing left to score
+    assert o.candidate_range(10, 4, 8) == (4, 4)
+
+
 # ---------------------------------------------------------------- selector
 
 def pin_select_golden(o):

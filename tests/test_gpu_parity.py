@@ -108,6 +108,38 @@ def test_score_select_fewer_queries_and_ragged(kvm, variant):
     check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
 
 
+@pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
+@pytest.mark.parametrize("loc", ["device", "host-tiled"])
+def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
+    """candidate_mode 1: the Eq. (10) softmax runs over the non-reserved blocks
+    only; sink and recent blocks score exactly 0 and are still selected.  The
+    host-tiled index puts the candidate range's ends inside 96-block tiles."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=1237, view_blocks=100)
+    ws = workload.make_index_direct(wl, seed=4)
+    kw = dict(score_variant=variant, candidate_mode=1)
+    index = ws.index.to("cuda")
+    if loc == "host-tiled":
+        kw["index_location"] = kvm.KVM_HOST_PINNED
+        index = ws.index.pin_memory()
+    cfg = kvm.config_for(wl, **kw)
+    if loc == "host-tiled":
+        cfg.tile_blocks = 96
+    ctx = kvm.Context(cfg)
+    N, S, W = wl.n_blocks, wl.sink_blocks, wl.recent_blocks
+    scores = torch.full((N,), 5.0, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.score_select(ws.q.cuda(), wl.n_queries, index, N, scores, sel)
+    ctx.sync()
+    got = scores.cpu().double().numpy()
+    R = ora.block_relevance_excl(ora.as_f64(to_np(ws.q, "bf16"), "bf16"),
+                                 ora.as_f64(to_np(ws.index, "bf16"), "bf16"), N, S, W)
+    assert np.all(got[:S] == 0) and np.all(got[N - W:] == 0)
+    assert_scores_close(got[S:N - W], R[S:N - W], "candidates only")
+    assert abs(got.sum() - wl.n_queries) < 1e-3 * wl.n_queries
+    check_selection(sel.cpu().numpy(), R, S, W, wl.view_blocks, "candidates only")
+
+
 @pytest.mark.parametrize("n_queries", [21, 32, 40, 42], ids=lambda n: f"rows{n * 6}")
 def test_score_select_query_row_tilings(kvm, n_queries):
     """Query rows per KV head across the tensor-core tilings: one M = 128 tile

@@ -153,7 +153,22 @@ def _delta_limit_inclusive(block_of_page, baked_pos, delta_count, sel, limit):
     return page, action, bop, bp, cnt
 
 
+def _excl_softmax_over_all(q, index, n_blocks, sink, recent):
+    R = ora.block_relevance(q, index, n_blocks)
+    c0, c1 = ora.candidate_range(n_blocks, sink, recent)
+    R[:c0] = 0.0
+    R[c1:] = 0.0
+    return R
+
+
+def _excl_range_off_by_one(n_blocks, sink, recent):
+    return min(sink, n_blocks), max(n_blocks - recent - 1, min(sink, n_blocks))
+
+
 MUTANTS = {
+    "excluded reading normalises over every block": ("block_relevance_excl",
+                                                     _excl_softmax_over_all),
+    "candidate range drops the last candidate": ("candidate_range", _excl_range_off_by_one),
     "delta rotation ignores the sign of delta": ("delta_rerope_k", _delta_sign_ignored),
     "delta limit off by one": ("residency_step_delta", _delta_limit_inclusive),
     "interleaved pairs": ("rotate_f64", _interleaved_rotate),
