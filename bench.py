@@ -452,7 +452,7 @@ def oracle_select_view_sample(wl, index, q, raw_h, layers):
 
 
 STEP_KIND = {"tiny-4k": Step, "q27-256k": Step, "q27-10m-score": ScoreStep,
-             "q27x16-1m": HostStep, "q27-512k-churn": ChurnStep,
+             "q27x16-1m": HostStep, "q27-512k-churn": ChurnStep, "q27-256k-fp8": Step,
              "q27x16-512k-churn": ChurnStep}
 
 
@@ -515,7 +515,7 @@ def bench_ours(args, wl, world, rank, local, dist):
     kern = {k: {"ms": parts[k], "gbs": ab[k] / (parts[k] * 1e-3) / 1e9,
                 "frac_hbm": ab[k] / (parts[k] * 1e-3) / 1e9 / peak} for k in parts}
     dom = max(parts, key=parts.get)
-    traffic = _traffic_from_profile(dom)
+    traffic = _traffic_from_profile(wl.name, dom)
     roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"], "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_hbm"],
             "traffic": traffic, "algorithmic_bytes": ab[dom]}
@@ -538,13 +538,15 @@ def bench_ours(args, wl, world, rank, local, dist):
         "value": job_throughput(world, wl.n_blocks, ms),
         "unit": "scored blocks/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.kv_dtype,
         "data": "synthetic (seeded N(0,1/128) raw K/V, 2% planted blocks, RoPE-free queries)",
         "config": {"workload": wl.name, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
                    "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "history_blocks": wl.n_blocks,
                    "history_tokens": wl.n_tokens, "queries": wl.n_queries,
                    "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
-                   "recent_blocks": wl.recent_blocks, "parallelism": f"replicas{world}",
+                   "recent_blocks": wl.recent_blocks, "kv_dtype": wl.kv_dtype,
+                   "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2, no flush"},
         "components": comps,
         "roofline": roof,
@@ -577,16 +579,16 @@ def h2d_peak(dev, stream, nbytes=256 << 20, reps=20):
     return nbytes / (ms * 1e-3) / 1e9
 
 
-def _traffic_from_profile(kernel):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    when one matches the current kernel build (else null)."""
+def _traffic_from_profile(workload_name, kernel):
+    """DRAM bytes per launch from the committed ncu summary of this workload and
+    kernel, when one matches the current kernel source (else null)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         import hashlib
         with open(p) as f:
-            d = json.load(f).get(kernel)
+            d = json.load(f).get(workload_name, {}).get(kernel)
         if not d:
             return None
         with open(os.path.join(ROOT, d["source"]), "rb") as f:

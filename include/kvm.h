@@ -52,7 +52,12 @@ typedef enum {
     KVM_ERR_DEVICE = -8                /* a device-side range check fired             */
 } kvm_status;
 
-enum { KVM_F32 = 0, KVM_BF16 = 1 };              /* element types            */
+/* Element types.  KVM_E4M3 is 8-bit floating point (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; no infinity, S.1111.111 is NaN; largest
+ * finite value 448), the FP8 KV cache of the [KVMem] §6.1 platforms.  It is
+ * for kv_dtype only, stored at unit scale; values written by the library are
+ * rounded to nearest even and saturate to +-448. */
+enum { KVM_F32 = 0, KVM_BF16 = 1, KVM_E4M3 = 2 };
 enum { KVM_DEVICE = 0, KVM_HOST_PINNED = 1 };    /* where a buffer lives     */
 
 /* Shapes and budgets of one workspace.  All fields are required. */
@@ -63,7 +68,7 @@ typedef struct {
     int32_t head_dim;        /* d: 64 or 128                                   */
     int32_t block_tokens;    /* must be 32 ([KVMem] §4.3 default block size)   */
     double  rope_theta;      /* RoPE base                                      */
-    int32_t kv_dtype;        /* K pages, raw K, V: KVM_F32 or KVM_BF16         */
+    int32_t kv_dtype;        /* K pages, raw K, V: KVM_F32, KVM_BF16, KVM_E4M3 */
     int32_t index_dtype;     /* Mean-K entries                                 */
     int32_t q_dtype;         /* queries                                        */
     int32_t sink_blocks;     /* S: always-kept leading blocks                  */

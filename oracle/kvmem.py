@@ -51,23 +51,69 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
     return r
 
 
+# FP8 E4M3 (the 8-bit KV cache of the pages' platforms, [KVMem] §6.1), in the
+# common OCP encoding: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+# bits.  Exponent field 0 holds the subnormals m * 2^-9; S.1111.111 is NaN and
+# there is no infinity, so the largest finite value is 1.75 * 2^8 = 448.
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f32(bits: np.ndarray) -> np.ndarray:
+    """E4M3 bit patterns (uint8) -> the float32 values they denote (exact)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return (sign * mag).astype(np.float32)
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round float32 to E4M3 with round-to-nearest-even; finite values beyond
+    the largest finite one saturate to +-448; NaN maps to NaN.  Returns uint8
+    bits.  Steps: the binade e of |x| (clamped below at the subnormal binade),
+    the scaled mantissa |x| / 2^(e-3) rounded half to even, a carry into the
+    next binade, saturation."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(x)
+    sign = np.where(np.signbit(x), 0x80, 0).astype(np.int64)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))   # a = f * 2^ex, f in [1/2, 1)
+    e = (ex - 1).astype(np.int64)
+    e = np.maximum(e, -6)                       # subnormals share the binade of 2^-6
+    q = a / np.exp2(e - 3.0)                    # in [8, 16) for normals, [0, 8) below
+    qr = np.round(q)                            # numpy rounds half to even
+    carry = qr >= 16
+    e = np.where(carry, e + 1, e)
+    qr = np.where(carry, qr / 2, qr)
+    normal = qr >= 8
+    field = np.where(normal, e + 7, 0)
+    mant = np.where(normal, qr - 8, qr).astype(np.int64)
+    code = (field.astype(np.int64) << 3) | mant
+    code = np.where(a >= E4M3_MAX, 0x7E, code)  # saturate (1.1111.110 = 448)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return (sign | code).astype(np.uint8)
+
+
 def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Stored values (uint16 bf16 bits or float32) as float64."""
-    if dtype == "bf16":
-        return bf16_to_f32(x).astype(np.float64)
-    return np.asarray(x, dtype=np.float32).astype(np.float64)
+    """Stored values (uint16 bf16 bits, uint8 e4m3 bits or float32) as float64."""
+    return as_f32(x, dtype).astype(np.float64)
 
 
 def as_f32(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return bf16_to_f32(x)
+    if dtype == "e4m3":
+        return e4m3_to_f32(x)
     return np.asarray(x, dtype=np.float32)
 
 
 def round_to(x32: np.ndarray, dtype: str) -> np.ndarray:
-    """float32 values rounded once to the storage dtype (RNE)."""
+    """float32 values rounded once to the storage dtype (RNE; e4m3 saturates)."""
     if dtype == "bf16":
         return f32_to_bf16(x32)
+    if dtype == "e4m3":
+        return f32_to_e4m3(x32)
     return np.asarray(x32, dtype=np.float32)
 
 

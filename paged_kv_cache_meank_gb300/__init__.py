@@ -20,15 +20,16 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (KVM_BF16, KVM_DEVICE, KVM_F32, KVM_HOST_PINNED, KvmBuffers, KvmConfig,
-                   KvmError, KvmStepStats, check, load)
+from ._abi import (KVM_BF16, KVM_DEVICE, KVM_E4M3, KVM_F32, KVM_HOST_PINNED, KvmBuffers,
+                   KvmConfig, KvmError, KvmStepStats, check, load)
 from .configs import BLOCK_TOKENS, Workload
 
-__all__ = ["Context", "KvmError", "config_for", "load", "KVM_F32", "KVM_BF16", "KVM_DEVICE",
-           "KVM_HOST_PINNED"]
+__all__ = ["Context", "KvmError", "config_for", "load", "KVM_F32", "KVM_BF16", "KVM_E4M3",
+           "KVM_DEVICE", "KVM_HOST_PINNED"]
 
-_DT = {"f32": KVM_F32, "bf16": KVM_BF16}
-_TDT = {KVM_F32: torch.float32, KVM_BF16: torch.bfloat16}
+_DT = {"f32": KVM_F32, "bf16": KVM_BF16, "e4m3": KVM_E4M3}
+# e4m3 elements travel as their bit patterns in uint8 tensors
+_TDT = {KVM_F32: torch.float32, KVM_BF16: torch.bfloat16, KVM_E4M3: torch.uint8}
 
 
 def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: int | None = None,

@@ -7,7 +7,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libkvm.so")
 
-KVM_F32, KVM_BF16 = 0, 1
+KVM_F32, KVM_BF16, KVM_E4M3 = 0, 1, 2
 KVM_DEVICE, KVM_HOST_PINNED = 0, 1
 
 STATUS = {

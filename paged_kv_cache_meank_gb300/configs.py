@@ -23,7 +23,7 @@ class Workload:
     n_q_heads: int
     head_dim: int
     rope_theta: float
-    kv_dtype: str          # "f32" or "bf16": K pages, raw K, V
+    kv_dtype: str          # "f32", "bf16" or "e4m3": K pages, raw K, V
     index_dtype: str       # Mean-K entries
     q_dtype: str           # RoPE-free current-step queries
     n_blocks: int          # complete historical blocks N
@@ -62,7 +62,7 @@ class Workload:
         return self.view_blocks * BLOCK_TOKENS
 
     def elem_bytes(self, which: str) -> int:
-        return {"f32": 4, "bf16": 2}[getattr(self, which)]
+        return {"f32": 4, "bf16": 2, "e4m3": 1}[getattr(self, which)]
 
     @property
     def block_bytes(self) -> int:
@@ -114,4 +114,8 @@ W10M = Workload(name="q27-10m-score", n_blocks=312500, view_blocks=2048,
 # not fit pinned in the 199 GB of host memory next to the rest of the process.
 CHURN512K_16 = CHURN512K.with_(name="q27x16-512k-churn", n_layers=16)
 
-ALL = {w.name: w for w in (TINY, W256K, W1M, CHURN512K, CHURN512K_16, W10M)}
+# The 256K step with 8-bit (e4m3) K / V pages, as the FP8 KV cache of the
+# pages' evaluation platforms ([KVMem] §6.1); the index and queries stay bf16.
+W256K_FP8 = W256K.with_(name="q27-256k-fp8", kv_dtype="e4m3")
+
+ALL = {w.name: w for w in (TINY, W256K, W1M, CHURN512K, CHURN512K_16, W10M, W256K_FP8)}

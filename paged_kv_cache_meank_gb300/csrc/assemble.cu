@@ -59,15 +59,16 @@ struct SlotWork {
         }
         const size_t row = (size_t)tok * D + (size_t)c * PPT;
         const bool do_v = (src_v != nullptr) && (dst_v != nullptr);
+        using V = typename VecTraits<T>::V;
 #pragma unroll 2
         for (int lg = lg0; lg < lg1; ++lg) {
             const size_t off = (size_t)lg * kBlockTokens * D + row;
-            const uint4 vx = ld_stream(src_k + off);
-            const uint4 vy = ld_stream(src_k + off + HD);
-            uint4 wx = make_uint4(0, 0, 0, 0), wy = wx;
+            V vx, vy, wx{}, wy{};
+            ld_stream_v(src_k + off, vx);
+            ld_stream_v(src_k + off + HD, vy);
             if (do_v) {
-                wx = ld_stream(src_v + off);
-                wy = ld_stream(src_v + off + HD);
+                ld_stream_v(src_v + off, wx);
+                ld_stream_v(src_v + off + HD, wy);
             }
             float x[PPT], y[PPT], ox[PPT], oy[PPT];
             VecTraits<T>::unpack(vx, x);
@@ -78,15 +79,15 @@ struct SlotWork {
                 ox[i] = __fsub_rn(__fmul_rn(x[i], cs[i]), __fmul_rn(y[i], sn[i]));
                 oy[i] = __fadd_rn(__fmul_rn(x[i], sn[i]), __fmul_rn(y[i], cs[i]));
             }
-            st_stream(dst_k + off, VecTraits<T>::pack(ox));
-            st_stream(dst_k + off + HD, VecTraits<T>::pack(oy));
+            st_stream_v(dst_k + off, VecTraits<T>::pack(ox));
+            st_stream_v(dst_k + off + HD, VecTraits<T>::pack(oy));
             if (dst_raw != nullptr) {
-                st_stream(dst_raw + off, vx);
-                st_stream(dst_raw + off + HD, vy);
+                st_stream_v(dst_raw + off, vx);
+                st_stream_v(dst_raw + off + HD, vy);
             }
             if (do_v) {
-                st_stream(dst_v + off, wx);
-                st_stream(dst_v + off + HD, wy);
+                st_stream_v(dst_v + off, wx);
+                st_stream_v(dst_v + off + HD, wy);
             }
         }
     }
@@ -181,6 +182,12 @@ cudaError_t launch_assemble_ids(int kv_dtype, int d, const int32_t *sel_ids,
     if (kv_dtype == F32 && d == 64)
         return ids_t<float, 64>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo, v_repo,
                                 k_pages, v_pages, LG, table, err, s);
+    if (kv_dtype == E4M3 && d == 128)
+        return ids_t<e4m3, 128>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo, v_repo,
+                                k_pages, v_pages, LG, table, err, s);
+    if (kv_dtype == E4M3 && d == 64)
+        return ids_t<e4m3, 64>(sel_ids, page_ids, n_sel, max_blocks, raw_k_repo, v_repo,
+                               k_pages, v_pages, LG, table, err, s);
     return cudaErrorInvalidValue;
 }
 
@@ -196,6 +203,10 @@ cudaError_t launch_assemble_desc(int kv_dtype, int d, const SlotDesc *desc, int 
         return desc_t<float, 128>(desc, n_desc, LG, table, max_pos, err, s);
     if (kv_dtype == F32 && d == 64)
         return desc_t<float, 64>(desc, n_desc, LG, table, max_pos, err, s);
+    if (kv_dtype == E4M3 && d == 128)
+        return desc_t<e4m3, 128>(desc, n_desc, LG, table, max_pos, err, s);
+    if (kv_dtype == E4M3 && d == 64)
+        return desc_t<e4m3, 64>(desc, n_desc, LG, table, max_pos, err, s);
     return cudaErrorInvalidValue;
 }
 

@@ -47,7 +47,7 @@ kvm_status cuda_fail(cudaError_t e, const char *what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t elt_bytes(int dt) { return dt == KVM_BF16 ? 2 : 4; }
+size_t elt_bytes(int dt) { return dt == KVM_E4M3 ? 1 : dt == KVM_BF16 ? 2 : 4; }
 
 struct Layout {
     size_t table, part_m, part_z, row_m, row_invz, partial, stage0, stage1, desc, err, total;
@@ -63,8 +63,11 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
     if (c->block_tokens != 32) return bad("block_tokens must be 32");
     if (!(c->rope_theta > 1.0)) return bad("rope_theta must be > 1");
-    for (int dt : {c->kv_dtype, c->index_dtype, c->q_dtype})
-        if (dt != KVM_F32 && dt != KVM_BF16) return bad("dtype must be KVM_F32 or KVM_BF16");
+    if (c->kv_dtype != KVM_F32 && c->kv_dtype != KVM_BF16 && c->kv_dtype != KVM_E4M3)
+        return bad("kv_dtype must be KVM_F32, KVM_BF16 or KVM_E4M3");
+    for (int dt : {c->index_dtype, c->q_dtype})
+        if (dt != KVM_F32 && dt != KVM_BF16)
+            return bad("index_dtype and q_dtype must be KVM_F32 or KVM_BF16");
     if (c->sink_blocks < 0 || c->recent_blocks < 0) return bad("sink/recent must be >= 0");
     if (c->view_blocks < c->sink_blocks + c->recent_blocks + 1)
         return bad("view_blocks must be >= sink + recent + 1");

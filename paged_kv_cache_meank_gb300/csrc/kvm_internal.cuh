@@ -18,7 +18,7 @@ constexpr int kMaxHalfDim = 64;       // head_dim <= 128
 constexpr int kMaxRows = 256;         // query rows per KV head (M_q * H/G)
 constexpr int kMaxChunks = 64;        // block chunks per (layer, kv head) in scoring
 
-enum DType { F32 = 0, BF16 = 1 };
+enum DType { F32 = 0, BF16 = 1, E4M3 = 2 };
 
 struct Omega {
     double w[kMaxHalfDim];            // theta^(-2i/d), double precision

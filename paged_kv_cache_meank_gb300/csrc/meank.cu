@@ -32,7 +32,11 @@ meank_kernel(const T *__restrict__ k_pages, T *__restrict__ raw_out, TI *__restr
     constexpr int TPT = HD / PPT;            // lanes per token row
     constexpr int TOK = 32 / TPT;            // tokens per warp-wide sweep
     constexpr int ITERS = 32 / TOK;          // sweeps over the block's 32 tokens
-    constexpr int GROUP = ITERS < 4 ? ITERS : 4;   // sweeps with loads in flight together
+    // sweeps with loads in flight together: 128 bytes per lane
+    constexpr int GROUP = ITERS < 128 / (2 * (int)sizeof(typename VecTraits<T>::V))
+                              ? ITERS
+                              : 128 / (2 * (int)sizeof(typename VecTraits<T>::V));
+    using V = typename VecTraits<T>::V;
     // cos/sin of (token, column slice): PPT pairs padded by 2 so that the eight
     // lanes of one shared-memory phase hit distinct banks
     constexpr int ROW = PPT + 2;
@@ -60,13 +64,13 @@ meank_kernel(const T *__restrict__ k_pages, T *__restrict__ raw_out, TI *__restr
         for (int k = 0; k < PPT; ++k) ax[k] = ay[k] = 0.f;
 #pragma unroll
         for (int g0 = 0; g0 < ITERS; g0 += GROUP) {
-            uint4 vx[GROUP], vy[GROUP];
+            V vx[GROUP], vy[GROUP];
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
                 const int t = t0 + (g0 + i) * TOK;
                 const size_t off = (size_t)t * D + (size_t)c * PPT;
-                vx[i] = ld_stream(src + off);
-                vy[i] = ld_stream(src + off + HD);
+                ld_stream_v(src + off, vx[i]);
+                ld_stream_v(src + off + HD, vy[i]);
             }
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
@@ -93,8 +97,8 @@ meank_kernel(const T *__restrict__ k_pages, T *__restrict__ raw_out, TI *__restr
                 }
                 if (raw_out != nullptr) {
                     const size_t off = base + (size_t)t * D + (size_t)c * PPT;
-                    st_stream(raw_out + off, VecTraits<T>::pack(rx));
-                    st_stream(raw_out + off + HD, VecTraits<T>::pack(ry));
+                    st_stream_v(raw_out + off, VecTraits<T>::pack(rx));
+                    st_stream_v(raw_out + off + HD, VecTraits<T>::pack(ry));
                 }
             }
         }
@@ -157,6 +161,12 @@ cudaError_t launch_meank(int kv_dtype, int index_dtype, int d, const void *k_pag
     } else if (kv_dtype == F32 && index_dtype == BF16) {
         if (d == 128) KVM_MEANK(float, __nv_bfloat16, 128);
         if (d == 64) KVM_MEANK(float, __nv_bfloat16, 64);
+    } else if (kv_dtype == E4M3 && index_dtype == BF16) {
+        if (d == 128) KVM_MEANK(e4m3, __nv_bfloat16, 128);
+        if (d == 64) KVM_MEANK(e4m3, __nv_bfloat16, 64);
+    } else if (kv_dtype == E4M3 && index_dtype == F32) {
+        if (d == 128) KVM_MEANK(e4m3, float, 128);
+        if (d == 64) KVM_MEANK(e4m3, float, 64);
     }
 #undef KVM_MEANK
     return cudaErrorInvalidValue;

@@ -20,7 +20,7 @@ order listed):
    topic ``A_t[m mod topics_per_step]``).
 
 Values are drawn in fp32 and rounded once to the storage dtype (bf16 RNE via
-``Tensor.to``).  The workspaces of KVMem (Virtualizing Million-Token Agent
+``Tensor.to``; e4m3 through torch's float8_e4m3fn, kept as uint8 bit patterns).  The workspaces of KVMem (Virtualizing Million-Token Agent
 Workspaces on a Consumer GPU, §6) are real agent traces that are not available
 here; these draws stand in for them with the same shapes.
 """
@@ -32,7 +32,20 @@ import torch
 
 from .configs import BLOCK_TOKENS, Workload
 
-_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+
+
+def _to_storage(x: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
+    """float32 values as the storage dtype (uint8 holds e4m3 bit patterns)."""
+    if dtype == torch.uint8:
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+    return x.to(dtype)
+
+
+def _from_storage(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype == torch.uint8:
+        return x.view(torch.float8_e4m3fn).float()
+    return x.float()
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -55,7 +68,7 @@ def _randn(shape, gen, device, chunk_elems=1 << 28, out_dtype=torch.float32, sca
         tmp = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
         if scale != 1.0:
             tmp.mul_(scale)
-        flat[s:e].copy_(tmp)
+        flat[s:e].copy_(_to_storage(tmp, out_dtype))
     return out
 
 
@@ -110,8 +123,8 @@ def make_workspace(wl: Workload, seed: int = 0, device="cpu", n_blocks: int | No
                 shift = shift[:, None, None, None, :]
             else:
                 shift = (wl.k_shift * wl.k_std) * u
-            sel = raw[planted].float() + shift
-            raw[planted] = sel.to(raw.dtype)
+            sel = _from_storage(raw[planted]) + shift
+            raw[planted] = _to_storage(sel, raw.dtype)
         ws.raw_k = raw
         ws.v = _randn(shape, gen, device, scale=wl.k_std, out_dtype=kvd)
     if with_q:

@@ -28,7 +28,10 @@ MIXED = configs.Workload(
     rope_theta=1e6, kv_dtype="f32", index_dtype="f32", q_dtype="bf16", n_blocks=150,
     n_queries=8, sink_blocks=1, recent_blocks=2, view_blocks=20, planted_frac=0.05)
 
-SMALL = [configs.TINY, MID, MID64, MIXED]
+# 8-bit (e4m3) K / V pages with a bf16 index, d = 128
+FP8 = MID.with_(name="mid-e4m3-d128", kv_dtype="e4m3", n_blocks=211)
+
+SMALL = [configs.TINY, MID, MID64, MIXED, FP8]
 
 REL_SCORE = 1e-4   # relative tolerance on R_b
 
@@ -37,6 +40,8 @@ def to_np(t: torch.Tensor, dtype: str) -> np.ndarray:
     t = t.detach().cpu().contiguous()
     if dtype == "bf16":
         return t.view(torch.int16).numpy().view(np.uint16).copy()
+    if dtype == "e4m3":
+        return t.view(torch.uint8).numpy().copy()
     return t.float().numpy().copy()
 
 
@@ -44,6 +49,8 @@ def from_np(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
     if dtype == "bf16":
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
             torch.bfloat16).to(device)
+    if dtype == "e4m3":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(device)
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
 
 
@@ -53,15 +60,22 @@ def bf16_ordered(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, 0x8000 - (b & 0x7FFF) - 1, b + 0x8000 - 1 + 1)
 
 
+def e4m3_ordered(bits: np.ndarray) -> np.ndarray:
+    """Monotone integer image of e4m3 bit patterns (+0 and -0 both map to 0)."""
+    b = bits.astype(np.int32)
+    return np.where(b & 0x80, -(b & 0x7F), b)
+
+
 def assert_storage_close(gpu: np.ndarray, ref: np.ndarray, dtype: str, what: str,
                          f32_pair_ulps: float = 2.0):
-    """K-type outputs: bf16 within 1 ulp of the reference rounding; float32 within
-    ``f32_pair_ulps`` ulps of the rotate-half pair's magnitude."""
+    """K-type outputs: bf16 and e4m3 within 1 ulp of the reference rounding;
+    float32 within ``f32_pair_ulps`` ulps of the rotate-half pair's magnitude."""
     assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
-    if dtype == "bf16":
-        d = np.abs(bf16_ordered(gpu) - bf16_ordered(ref))
+    if dtype in ("bf16", "e4m3"):
+        order = bf16_ordered if dtype == "bf16" else e4m3_ordered
+        d = np.abs(order(gpu) - order(ref))
         bad = int((d > 1).sum())
-        assert bad == 0, f"{what}: {bad} elements beyond 1 bf16 ulp (max {d.max()})"
+        assert bad == 0, f"{what}: {bad} elements beyond 1 {dtype} ulp (max {d.max()})"
         return float((d == 0).mean())
     h = ref.shape[-1] // 2
     mag = np.maximum(np.abs(ref[..., :h]), np.abs(ref[..., h:]))

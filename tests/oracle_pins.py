@@ -62,6 +62,34 @@ def pin_bf16_rounding(o):
 
 # ---------------------------------------------------------------- RoPE
 
+def pin_e4m3(o):
+    """FP8 E4M3: every finite code survives decode -> encode; the encoder picks
+    the nearest finite code by exhaustive search, ties to the even mantissa,
+    saturating beyond 448; fixed points of the format."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = o.e4m3_to_f32(codes)
+    fin = ~np.isnan(vals)
+    assert sorted(codes[~fin].tolist()) == [0x7F, 0xFF]
+    assert np.array_equal(o.f32_to_e4m3(vals[fin]), codes[fin])
+    assert float(np.nanmax(vals)) == 448.0 and vals[1] == 2.0 ** -9 and vals[8] == 2.0 ** -6
+    assert vals[0x38] == 1.0 and vals[0xB8] == -1.0 and vals[0x7E] == 448.0
+    pos_codes = np.arange(0x7F)                 # +0 .. 448, ascending
+    pos_vals = vals[pos_codes].astype(np.float64)
+    rng = np.random.default_rng(14)
+    mids = (pos_vals[:-1] + pos_vals[1:]) / 2
+    xs = np.concatenate([rng.standard_normal(4000) * 0.1, rng.standard_normal(1000) * 100,
+                         mids, -mids, [0.0, -0.0, 447.0, 448.0, 463.9, 464.0, 500.0, 1e6, -1e6]])
+    xs = xs.astype(np.float32).astype(np.float64)
+    got = o.f32_to_e4m3(xs.astype(np.float32))
+    for x, g in zip(xs, got):
+        dist = np.abs(pos_vals - min(abs(x), 448.0))
+        best = np.flatnonzero(dist == dist.min())
+        if len(best) > 1:                           # a tie: the even mantissa wins
+            best = [b for b in best if pos_codes[b] % 2 == 0]
+        want = int(pos_codes[best[0]]) | (0x80 if np.signbit(x) else 0)
+        assert int(g) == want, (x, int(g), want)
+
+
 def pin_rope_closed_form(o):
     """d = 4: pair 0 turns at omega_0 = 1, pair 1 at omega_1 = theta^-1/2."""
     theta = 1e4

@@ -16,12 +16,16 @@ def to_np(t: torch.Tensor, dtype: str) -> np.ndarray:
     t = t.detach().cpu().contiguous()
     if dtype == "bf16":
         return t.view(torch.int16).numpy().view(np.uint16).copy()
+    if dtype == "e4m3":
+        return t.view(torch.uint8).numpy().copy()
     return t.float().numpy().copy()
 
 
 def from_np(a: np.ndarray, dtype: str) -> torch.Tensor:
     if dtype == "bf16":
         return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+    if dtype == "e4m3":
+        return torch.from_numpy(np.asarray(a, dtype=np.uint8).copy())
     return torch.from_numpy(np.asarray(a, dtype=np.float32).copy())
 
 

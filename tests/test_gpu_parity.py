@@ -211,20 +211,21 @@ def test_assemble_view(kvm, wl):
     assert torch.equal(kp2, kp[torch.from_numpy(pages).long().cuda()])
 
 
-def test_assemble_roundtrip_at_original_positions(kvm):
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_assemble_roundtrip_at_original_positions(kvm, kv_dtype):
     """Every block selected in order lands at its original positions: the view
     K equals the prefill K (KVMem §4.4; InferScale Theorem 6)."""
     from paged_kv_cache_meank_gb300 import workload
-    wl = MID.with_(n_blocks=40, view_blocks=40)
+    wl = MID.with_(n_blocks=40, view_blocks=40, kv_dtype=kv_dtype)
     ws = workload.make_workspace(wl, seed=6, with_q=False)
-    raw = to_np(ws.raw_k, "bf16")
-    kp_ref = prefill_k_pages(raw, "bf16", wl.rope_theta)
+    raw = to_np(ws.raw_k, kv_dtype)
+    kp_ref = prefill_k_pages(raw, kv_dtype, wl.rope_theta)
     ctx = _ctx(kvm, wl)
-    out = torch.empty(ctx.block_shape(40), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(ctx.block_shape(40), dtype=ctx.kv_dtype, device="cuda")
     ids = torch.arange(40, dtype=torch.int32, device="cuda")
     ctx.assemble_view(ids, None, 40, ws.raw_k.cuda(), None, out, None)
     ctx.sync()
-    assert np.array_equal(to_np(out, "bf16"), kp_ref)
+    assert np.array_equal(to_np(out, kv_dtype), kp_ref)
 
 
 def test_device_range_checks(kvm):

@@ -91,7 +91,7 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
         assert st["hits"] == sum(hit) and st["misses"] == len(hit) - sum(hit)
         assert st["reroped"] == sum(rope)
         blk = ctx.block_shape(1)
-        nbytes = int(np.prod(blk)) * (2 if wl.kv_dtype == "bf16" else 4)
+        nbytes = int(np.prod(blk)) * {"f32": 4, "bf16": 2, "e4m3": 1}[wl.kv_dtype]
         if repo_host:
             assert st["h2d_bytes"] == 2 * nbytes * st["misses"]
         # the view: K at compact positions from the oracle's raw K, V unchanged
@@ -120,6 +120,22 @@ def test_step_sequence(kvm, repo_host, h2d_mode):
     assert hist[0]["misses"] == wl.view_blocks and hist[0]["hits"] == 0
     # same queries, same history: every block is a hit and nothing moves
     assert hist[2]["misses"] == 0 and hist[2]["reroped"] == 0
+
+
+@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 1)],
+                         ids=["repo-device", "repo-host-gpu-pull"])
+def test_step_sequence_fp8_pages(kvm, repo_host, h2d_mode):
+    """The same working-set sequence with 8-bit (e4m3) K / V pages: Mean-K from
+    e4m3 prefill K, view K re-RoPE'd and rounded to e4m3, V bytes moved."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(kv_dtype="e4m3", name="mid-e4m3")
+    g = torch.Generator().manual_seed(23)
+    u = workload.unit_vectors(2, wl.head_dim, g, "cpu")
+    qa = workload.make_queries(wl, g, "cpu", u[0])
+    qb = workload.make_queries(wl, g, "cpu", u[1])
+    hist = _run_steps(kvm, wl, repo_host, False, [qa, qb, qa], [270, 290, 300],
+                      h2d_mode=h2d_mode)
+    assert hist[0]["misses"] == wl.view_blocks
 
 
 def test_step_host_index_tiled(kvm):

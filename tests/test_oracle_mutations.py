@@ -165,7 +165,33 @@ def _excl_range_off_by_one(n_blocks, sink, recent):
     return min(sink, n_blocks), max(n_blocks - recent - 1, min(sink, n_blocks))
 
 
+def _e4m3_ties_away(x):
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex - 1, -6)
+    q = np.floor(a / np.exp2(e - 3.0) + 0.5)
+    carry = q >= 16
+    e = np.where(carry, e + 1, e)
+    q = np.where(carry, q / 2, q)
+    normal = q >= 8
+    code = (np.where(normal, e + 7, 0).astype(np.int64) << 3) | np.where(normal, q - 8, q).astype(np.int64)
+    code = np.where(a >= 448, 0x7E, code)
+    return (np.where(np.signbit(x), 0x80, 0) | code).astype(np.uint8)
+
+
+def _e4m3_no_saturation(x):
+    c = _ORIG_E4M3(x)
+    big = np.abs(np.asarray(x, dtype=np.float32)) >= 464
+    return np.where(big, c | 0x7F, c).astype(np.uint8)
+
+
+_ORIG_E4M3 = ora.f32_to_e4m3
+
+
 MUTANTS = {
+    "e4m3 ties away from zero": ("f32_to_e4m3", _e4m3_ties_away),
+    "e4m3 overflows to NaN instead of saturating": ("f32_to_e4m3", _e4m3_no_saturation),
     "excluded reading normalises over every block": ("block_relevance_excl",
                                                      _excl_softmax_over_all),
     "candidate range drops the last candidate": ("candidate_range", _excl_range_off_by_one),
