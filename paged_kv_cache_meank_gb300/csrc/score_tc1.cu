@@ -3,22 +3,26 @@
 // l, kv head g) the maximum and the partition sum of its scaled scores over a
 // chunk of Mean-K blocks, for bf16 queries and a bf16 index.
 //
-// The contraction is D[query row][block] = Q_g . Kbar^T (M = 128 query rows
-// per row tile, N = 128 blocks), both operands in 128-byte-swizzled shared
-// memory.  (Keeping Q in TMEM as the A operand was measured slower: it needs
-// tiles of at most 96 blocks to fit two accumulators, and the tensor pipe runs
-// N = 96 instructions at a lower fraction of its peak than N = 128.)
+// The contraction is D[query row][block] = Q_g . Kbar^T, M = 128 query rows
+// per row tile and N = 256 blocks per index tile, both operands in
+// 128-byte-swizzled shared memory.  The tensor pipe runs N = 256 instructions
+// near its peak rate where N = 128 ran at about 72% of it.  Work is a sequence
+// of slots, one per (index tile, row tile); slot j accumulates into TMEM
+// buffer j mod 2 (256 columns each), so the epilogue of one slot overlaps the
+// MMAs of the next.  (Keeping Q in TMEM as the A operand was measured slower:
+// it needs tiles of at most 96 blocks to fit.)
 //
 // CTA = 18 warps, one SM:
-//   warp 0       TMA producer: 128-block index tiles into a 4-stage ring (one
-//                copy per 128-byte K atom)
-//   warp 1       MMA issuer: one thread, two TMEM accumulators of 256 columns
+//   warp 0       TMA producer: each tile's 128-byte K atoms (256 rows, 32 KB
+//                each) into a 4-entry ring
+//   warp 1       MMA issuer: one thread, per slot 4 * (d / 64) MMAs into one of
+//                two TMEM accumulators
 //   warps 2..17  epilogue, four warps per TMEM lane quadrant; each thread owns
 //                a query row (and, in the second row tile, half of one) and
 //                keeps a reference m and the partition sum z relative to it
 // For 128 < rows <= 192 the second row tile holds rows 128..191 twice (lanes
-// 0-63 and 64-127): quadrants 0-1 take its block columns 0-63, quadrants 2-3
-// columns 64-127, and the two halves of a row are merged at the end.  Every
+// 0-63 and 64-127): quadrants 0-1 take its block columns 0-127, quadrants 2-3
+// columns 128-255, and the two halves of a row are merged at the end.  Every
 // mbarrier wait is bounded; on timeout the kernel raises the device error flag
 // (bit 4) and winds down, freeing its TMEM.
 #include <cuda.h>
@@ -32,22 +36,21 @@ namespace kvm {
 
 namespace {
 
-constexpr int TB = 128;             // index blocks per tile
+constexpr int TB = 256;             // index blocks per tile
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 2 * TB;   // one accumulator: two row tiles
+constexpr uint32_t kAccCols = TB;   // one accumulator: one row tile x one index tile
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kQRows = 256;         // query rows padded to two row tiles
 
 template <int D>
 struct Lay1 {
     static constexpr int KA = D / 64;              // 128-byte K atoms per row
-    static constexpr int ATOM_TILE = TB * 128;
-    static constexpr int TILE = KA * ATOM_TILE;
+    static constexpr int ATOM_TILE = TB * 128;     // one ring entry: one atom of a tile
     static constexpr int STAGES = 4;
     static constexpr int Q_ATOM = kQRows * 128;
-    static constexpr int OFF_Q = STAGES * TILE;
+    static constexpr int OFF_Q = STAGES * ATOM_TILE;
     static constexpr int OFF_X = OFF_Q + KA * Q_ATOM;      // 1536 floats
     static constexpr int OFF_D = OFF_X + 1536 * 4;         // 2 x 32 x 2 floats
     static constexpr int OFF_BAR = OFF_D + 2 * 32 * 2 * 4;
@@ -200,19 +203,26 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // ring entry of atom a of tile i: (stage, phase parity)
+    auto ring = [](int i, int a) {
+        const int e = i * LY::KA + a;
+        return make_int2(e % LY::STAGES, (e / LY::STAGES) & 1);
+    };
+    const int n_slots = n_tiles * qtiles;
+
     if (warp == 0) {
         if (lane == 0) {
             for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % LY::STAGES;
-                const uint32_t ph = (i / LY::STAGES) & 1;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
-                tc::mbar_expect_tx(&full[s], LY::TILE);
                 const int32_t y =
                     (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
-#pragma unroll
-                for (int a = 0; a < LY::KA; ++a)
-                    tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
-                                    a * 64, y);
+                bool ok = true;
+                for (int a = 0; a < LY::KA && ok; ++a) {
+                    const int2 e = ring(i, a);
+                    if (!tc::mbar_wait(&empty[e.x], e.y ^ 1, kWaitLimit)) { ok = false; break; }
+                    tc::mbar_expect_tx(&full[e.x], LY::ATOM_TILE);
+                    tc::tma_load_2d(tiles + e.x * LY::ATOM_TILE, &tmap, &full[e.x], a * 64, y);
+                }
+                if (!ok) { atomicOr(err, 4); break; }
             }
         }
     } else if (warp == 1) {
@@ -220,31 +230,35 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
             const uint32_t qbase = tc::smem_u32(qs);
             const uint32_t tbase = tc::smem_u32(tiles);
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, TB);
-            for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % LY::STAGES;
-                const uint32_t ph = (i / LY::STAGES) & 1;
-                const int buf = i & 1;
-                const uint32_t bph = (i >> 1) & 1;
-                if (!tc::mbar_wait(&full[s], ph, kWaitLimit)) { atomicOr(err, 4); break; }
-                if (!tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
+            bool ok = true;
+            for (int j = 0; j < n_slots && ok; ++j) {
+                const int i = j / qtiles, t = j - i * qtiles;
+                const int buf = j & 1;
+                const uint32_t bph = (j >> 1) & 1;
+                if (t == 0)
+                    for (int a = 0; a < LY::KA && ok; ++a) {
+                        const int2 e = ring(i, a);
+                        ok = tc::mbar_wait(&full[e.x], e.y, kWaitLimit);
+                    }
+                if (!ok || !tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitLimit)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t d = tmem + buf * kAccCols;
-                const uint32_t tile = tbase + s * LY::TILE;
-                for (int t = 0; t < qtiles; ++t) {
 #pragma unroll
-                    for (int a = 0; a < LY::KA; ++a) {
+                for (int a = 0; a < LY::KA; ++a) {
+                    const uint32_t atom = tbase + ring(i, a).x * LY::ATOM_TILE;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = tc::sdesc_sw128(
-                                qbase + a * LY::Q_ATOM + t * 128 * 128 + kk * 32);
-                            const uint64_t bd = tc::sdesc_sw128(tile + a * LY::ATOM_TILE + kk * 32);
-                            tc::mma_bf16(d + t * TB, ad, bd, idesc, (a | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad =
+                            tc::sdesc_sw128(qbase + a * LY::Q_ATOM + t * 128 * 128 + kk * 32);
+                        const uint64_t bd = tc::sdesc_sw128(atom + kk * 32);
+                        tc::mma_bf16(d, ad, bd, idesc, (a | kk) != 0);
                     }
                 }
-                tc::mma_commit(&empty[s]);
                 tc::mma_commit(&tfull[buf]);
+                if (t == qtiles - 1)
+                    for (int a = 0; a < LY::KA; ++a) tc::mma_commit(&empty[ring(i, a).x]);
             }
+            if (!ok) atomicOr(err, 4);
         }
     } else {
         const int ew = warp - 2;                    // 0..15
@@ -252,43 +266,41 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
         const int sub = ew >> 2;                    // which quarter of the columns
         const int lrow = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int my_c0 = sub * 32;                 // first row tile: 32 block columns
-        // second row tile, duplicated: quadrants 0-1 take columns 0-63, 2-3
-        // columns 64-127, sixteen per warp
-        const int c1 = (quad >= 2 ? 64 : 0) + sub * 16;
+        const int my_c0 = sub * 64;                 // a full row tile: 64 block columns
+        // second row tile, duplicated: quadrants 0-1 take columns 0-127, 2-3
+        // columns 128-255, thirty-two per warp
+        const int c1 = (quad >= 2 ? 128 : 0) + sub * 32;
         float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
-        for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            const uint32_t bph = (i >> 1) & 1;
+        for (int j = 0; j < n_slots; ++j) {
+            const int i = j / qtiles, t = j - i * qtiles;
+            const int buf = j & 1;
+            const uint32_t bph = (j >> 1) & 1;
             if (!tc::mbar_wait(&tfull[buf], bph, kWaitLimit)) { atomicOr(err, 4); break; }
             tc::tc_fence_after();
             const int64_t gb0 = cb0 + (int64_t)i * TB;
             const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
             const uint32_t taddr = tmem + lane_base + buf * kAccCols;
+            const bool half = t == 1 && dup;
+            const int c0 = half ? c1 : my_c0;
             uint32_t r[64];
-            tc::tmem_ld32_async(taddr + my_c0, r);
-            if (qtiles > 1) {
-                if (dup) tc::tmem_ld16_async(taddr + TB + c1, r + 32);
-                else tc::tmem_ld32_async(taddr + TB + my_c0, r + 32);
-            }
+            tc::tmem_ld32_async(taddr + c0, r);
+            if (!half) tc::tmem_ld32_async(taddr + c0 + 32, r + 32);
             tc::tmem_wait_ld(r);
             tc::tmem_wait_ld(r + 16);
-            if (qtiles > 1) {
+            if (!half) {
                 tc::tmem_wait_ld(r + 32);
-                if (!dup) tc::tmem_wait_ld(r + 48);
+                tc::tmem_wait_ld(r + 48);
             }
             // the accumulator is in registers: hand the buffer back to the MMA warp
             tc::tc_fence_before();
             tc::mbar_arrive(&tempty[buf]);
-            const int nv = min(32, max(0, nvalid - my_c0));
-            row_update<32>(r, nv, scale_log2, m_run[0], z_run[0]);
-            if (qtiles > 1) {
-                if (dup)
-                    row_update<16>(r + 32, min(16, max(0, nvalid - c1)), scale_log2, m_run[1],
-                                   z_run[1]);
-                else
-                    row_update<32>(r + 32, nv, scale_log2, m_run[1], z_run[1]);
-            }
+            // explicit branches keep both rows' statistics in registers
+            if (half)
+                row_update<32>(r, min(32, max(0, nvalid - c0)), scale_log2, m_run[1], z_run[1]);
+            else if (t == 0)
+                row_update<64>(r, min(64, max(0, nvalid - c0)), scale_log2, m_run[0], z_run[0]);
+            else
+                row_update<64>(r, min(64, max(0, nvalid - c0)), scale_log2, m_run[1], z_run[1]);
         }
         // the quadrant's four warps merge their (m, z) in a fixed order:
         // [t][quad][sub-1][lane] pairs
