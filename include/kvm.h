@@ -105,6 +105,11 @@ typedef struct {
                                 1 = only the blocks the selector may still choose,
                                 [sink_blocks, N - recent_blocks): the softmax covers
                                 those, and sink / recent blocks score 0. */
+    int64_t host_tier_blocks;/* 0 = off; else kvm_step keeps a host-tier policy
+                                (see kvm_tier_step) over at most this many
+                                blocks, >= view_blocks, fed with every step's
+                                selection, and reports its hits / misses */
+    double  host_tier_lambda;/* the policy's decay, in [0, 1]              */
 } kvm_config;
 
 typedef struct kvm_ctx kvm_ctx;
@@ -235,6 +240,9 @@ typedef struct {
     int32_t h2d_copies;   /* host-to-device copies issued              */
     int64_t h2d_bytes;    /* bytes moved host to device               */
     int32_t delta_reroped;/* hits rotated in place by their position change */
+    int32_t host_hits;    /* with host_tier_blocks: selected blocks in the host tier */
+    int32_t host_misses;  /* ... and not in it (reads from the next tier)           */
+    int32_t host_demoted; /* ... blocks the host tier demoted in this step          */
 } kvm_step_stats;
 
 /*
@@ -255,6 +263,47 @@ typedef struct {
  */
 kvm_status kvm_step(kvm_ctx *ctx, const void *q, int32_t n_queries, int64_t n_blocks,
                     kvm_step_stats *stats, kvm_stream stream);
+
+/*
+ * Host-tier admission and eviction of repository blocks ([KVMem] §4.4,
+ * retrieval-aware hierarchical reuse).  Host memory keeps at most
+ * capacity_blocks blocks.  Admission and eviction weigh both recent and
+ * cumulative retrieval.  The pages give no formula; the policy is LRFU (Lee et
+ * al., IEEE Transactions on Computers 50(12), 2001):
+ *
+ *     CRF_t(b) = sum over b's references t_i of 2^(-lambda * (t - t_i))
+ *
+ * with lambda in [0, 1] (0 = reference counts, 1 = most recent use).
+ *
+ * Each kvm_tier_step is one agent step:
+ * - first, blocks [previous n_blocks, n_blocks) are created: their K / V reach
+ *   host memory by stage-out, so they become resident with one reference;
+ * - then the `ids` (distinct, the step's selected blocks) count one reference
+ *   each; a selected block that is not resident is a host miss (in a full
+ *   system, a read from the next tier) and becomes resident;
+ * - while more than capacity_blocks blocks are resident, the resident
+ *   unselected block with the smallest CRF_t is demoted (ties: the lower id
+ *   first).
+ *
+ * demoted_out (nullable, host, room for n_blocks ids) receives the demoted ids
+ * in demotion order.  Host-only bookkeeping: no device memory, no stream.  The
+ * next tier itself (NVMe) is not part of this library.
+ * Errors: KVM_ERR_INVALID_ARG for a bad capacity or lambda, ids out of range or
+ * repeated, or a shrinking history.  On error the tier is unchanged.
+ */
+typedef struct kvm_tier kvm_tier;
+typedef struct {
+    int32_t hits;       /* selected blocks already host-resident         */
+    int32_t misses;     /* selected blocks that were not                 */
+    int32_t demoted;    /* blocks demoted in this step                   */
+    int64_t resident;   /* host-resident blocks after the step           */
+} kvm_tier_stats;
+kvm_status kvm_tier_create(int64_t capacity_blocks, double lambda, kvm_tier **out);
+kvm_status kvm_tier_step(kvm_tier *tier, const int32_t *ids, int32_t n_ids, int64_t n_blocks,
+                         int32_t *demoted_out, kvm_tier_stats *stats);
+/* flags[b] = 1 if block b is host-resident, for b < n (host buffer). */
+kvm_status kvm_tier_resident(const kvm_tier *tier, uint8_t *flags, int64_t n);
+kvm_status kvm_tier_destroy(kvm_tier *tier);
 
 /*
  * kvm_score_select without any device allocation: the paper has no

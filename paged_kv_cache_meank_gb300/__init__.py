@@ -21,11 +21,11 @@ import torch
 
 from . import _abi
 from ._abi import (KVM_BF16, KVM_DEVICE, KVM_E4M3, KVM_F32, KVM_HOST_PINNED, KvmBuffers,
-                   KvmConfig, KvmError, KvmStepStats, check, load)
+                   KvmConfig, KvmError, KvmStepStats, KvmTierStats, check, load)
 from .configs import BLOCK_TOKENS, Workload
 
-__all__ = ["Context", "KvmError", "config_for", "load", "KVM_F32", "KVM_BF16", "KVM_E4M3",
-           "KVM_DEVICE", "KVM_HOST_PINNED"]
+__all__ = ["Context", "HostTier", "KvmError", "config_for", "load", "KVM_F32", "KVM_BF16",
+           "KVM_E4M3", "KVM_DEVICE", "KVM_HOST_PINNED"]
 
 _DT = {"f32": KVM_F32, "bf16": KVM_BF16, "e4m3": KVM_E4M3}
 # e4m3 elements travel as their bit patterns in uint8 tensors
@@ -37,11 +37,13 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
                repo_location: int | None = None, h2d_batch_blocks: int = 64,
                max_queries: int | None = None, score_variant: int = 0,
                h2d_mode: int = 1, delta_rerope_limit: int = 0,
-               candidate_mode: int = 0) -> KvmConfig:
+               candidate_mode: int = 0, host_tier_blocks: int = 0,
+               host_tier_lambda: float = 0.5) -> KvmConfig:
     """A kvm_config for a workload shape.  With a host-resident repository the
     GPU reads missed blocks from pinned host memory itself (h2d_mode 1) unless
     h2d_mode=0 asks for copy-engine transfers.  candidate_mode=1 leaves sink and
-    recent blocks out of the Eq. (10) softmax."""
+    recent blocks out of the Eq. (10) softmax.  host_tier_blocks > 0 runs the
+    host-tier policy (kvm_tier_step) over every step's selection."""
     mb = max_blocks if max_blocks is not None else wl.n_blocks + wl.steps * wl.append_blocks
     mp = max_positions if max_positions is not None else max(mb, wl.view_blocks) * BLOCK_TOKENS
     il = index_location if index_location is not None else (
@@ -58,7 +60,8 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         pool_pages=pool_pages if pool_pages is not None else wl.view_blocks + wl.append_blocks,
         index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
         h2d_mode=h2d_mode, score_variant=score_variant, delta_rerope_limit=delta_rerope_limit,
-        candidate_mode=candidate_mode)
+        candidate_mode=candidate_mode, host_tier_blocks=host_tier_blocks,
+        host_tier_lambda=host_tier_lambda)
 
 
 def _ptr(t) -> int | None:
@@ -88,6 +91,47 @@ def score_select_static(cfg: KvmConfig, q, n_queries: int, index, n_blocks: int,
                                       ctypes.byref(n_sel), _stream(stream)),
           "kvm_score_select_static")
     return n_sel.value
+
+
+class HostTier:
+    """kvm_tier: host-tier admission and eviction (LRFU over retrievals) of the
+    block repository.  Host-only; needs no GPU."""
+
+    def __init__(self, capacity_blocks: int, lam: float):
+        self.lib = load()
+        h = ctypes.c_void_p()
+        check(self.lib.kvm_tier_create(int(capacity_blocks), float(lam), ctypes.byref(h)),
+              "kvm_tier_create")
+        self.handle = h
+
+    def step(self, ids, n_blocks: int):
+        """One step: returns (hits, misses, demoted ids in demotion order)."""
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        dem = np.empty(max(int(n_blocks), 1), dtype=np.int32)
+        st = KvmTierStats()
+        check(self.lib.kvm_tier_step(self.handle, arr.ctypes.data if arr.size else None,
+                                     int(arr.size), int(n_blocks), dem.ctypes.data,
+                                     ctypes.byref(st)), "kvm_tier_step")
+        return st.hits, st.misses, dem[:st.demoted].tolist()
+
+    def resident(self, n: int):
+        import numpy as np
+        flags = np.zeros(max(int(n), 1), dtype=np.uint8)
+        check(self.lib.kvm_tier_resident(self.handle, flags.ctypes.data, int(n)),
+              "kvm_tier_resident")
+        return flags[:n]
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.kvm_tier_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Context:

@@ -31,6 +31,7 @@ class KvmConfig(ctypes.Structure):
         ("repo_location", ctypes.c_int32), ("h2d_batch_blocks", ctypes.c_int32),
         ("h2d_mode", ctypes.c_int32), ("score_variant", ctypes.c_int32),
         ("delta_rerope_limit", ctypes.c_int32), ("candidate_mode", ctypes.c_int32),
+        ("host_tier_blocks", ctypes.c_int64), ("host_tier_lambda", ctypes.c_double),
     ]
 
 
@@ -48,7 +49,15 @@ class KvmStepStats(ctypes.Structure):
         ("n_blocks", ctypes.c_int64), ("n_sel", ctypes.c_int32), ("hits", ctypes.c_int32),
         ("misses", ctypes.c_int32), ("reroped", ctypes.c_int32), ("evicted", ctypes.c_int32),
         ("h2d_copies", ctypes.c_int32), ("h2d_bytes", ctypes.c_int64),
-        ("delta_reroped", ctypes.c_int32),
+        ("delta_reroped", ctypes.c_int32), ("host_hits", ctypes.c_int32),
+        ("host_misses", ctypes.c_int32), ("host_demoted", ctypes.c_int32),
+    ]
+
+
+class KvmTierStats(ctypes.Structure):
+    _fields_ = [
+        ("hits", ctypes.c_int32), ("misses", ctypes.c_int32), ("demoted", ctypes.c_int32),
+        ("resident", ctypes.c_int64),
     ]
 
 
@@ -78,6 +87,13 @@ SIGNATURES = {
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                                ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    "kvm_tier_create": (ctypes.c_int, [ctypes.c_int64, ctypes.c_double,
+                                       ctypes.POINTER(ctypes.c_void_p)]),
+    "kvm_tier_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                     ctypes.c_int64, ctypes.c_void_p,
+                                     ctypes.POINTER(KvmTierStats)]),
+    "kvm_tier_resident": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]),
+    "kvm_tier_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "kvm_sync": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "kvm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvm_last_error": (ctypes.c_char_p, []),

@@ -31,6 +31,7 @@ SOURCES = [
     "assemble.cu",
     "score_static.cu",
     "kvm_api.cpp",
+    "host_tier.cpp",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

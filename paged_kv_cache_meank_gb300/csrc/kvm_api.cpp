@@ -89,6 +89,10 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->h2d_mode != 0 && c->h2d_mode != 1) return bad("h2d_mode must be 0 or 1");
     if (c->delta_rerope_limit < 0) return bad("delta_rerope_limit must be >= 0");
     if (c->candidate_mode != 0 && c->candidate_mode != 1) return bad("candidate_mode must be 0 or 1");
+    if (c->host_tier_blocks < 0 || (c->host_tier_blocks > 0 && c->host_tier_blocks < c->view_blocks))
+        return bad("host_tier_blocks must be 0 or >= view_blocks");
+    if (c->host_tier_blocks > 0 && !(c->host_tier_lambda >= 0.0 && c->host_tier_lambda <= 1.0))
+        return bad("host_tier_lambda must be in [0, 1]");
     return true;
 }
 
@@ -150,6 +154,7 @@ struct kvm_ctx {
     std::vector<int32_t> delta_count;    // delta rotations since the page's K was rebuilt
     std::vector<int32_t> page_of_block;
     std::vector<uint8_t> mark;
+    kvm_tier *tier = nullptr;            // host-tier policy (host_tier_blocks > 0)
     // fault injection
     int inject_what = 0;
     int64_t inject_nth = 0, inject_seen = 0;
@@ -256,6 +261,10 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     for (auto &ev : c->ev_batch)
         if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
             return cleanup(cuda_fail(e, "cudaEventCreate"));
+    if (cfg->host_tier_blocks > 0) {
+        const kvm_status ts = kvm_tier_create(cfg->host_tier_blocks, cfg->host_tier_lambda, &c->tier);
+        if (ts != KVM_OK) return cleanup(ts);
+    }
 
     kvm::Omega om{};
     const int hd = cfg->head_dim / 2;
@@ -278,6 +287,7 @@ kvm_status kvm_destroy(kvm_ctx *c) {
     for (auto ev : c->ev_batch)
         if (ev) cudaEventDestroy(ev);
     if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    if (c->tier) kvm_tier_destroy(c->tier);
     delete c;
     return KVM_OK;
 }
@@ -702,7 +712,13 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
     for (int j = 0; j < n_sel; ++j) c->baked_pos[page_of_slot[j]] = (int64_t)j * 32;
     c->delta_count.swap(new_count);
 
+    kvm_tier_stats ts{};
+    if (c->tier && kvm_tier_step(c->tier, sel.data(), n_sel, n_blocks, nullptr, &ts) != KVM_OK)
+        return KVM_ERR_INVALID_ARG;
     if (stats) {
+        stats->host_hits = ts.hits;
+        stats->host_misses = ts.misses;
+        stats->host_demoted = ts.demoted;
         stats->n_blocks = n_blocks;
         stats->n_sel = n_sel;
         stats->misses = (int32_t)miss_slots.size();

@@ -84,3 +84,35 @@ def test_layout_sizes_follow_the_workloads():
     # KV bytes per block 2 * L * c * h * d * b (InferScale §4 storage cost) for c = 32
     w = configs.W256K
     assert 2 * w.block_bytes == 2 * w.n_layers * 32 * w.n_kv_heads * w.head_dim * 2
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of kvm_config, kvm_buffers, kvm_step_stats and
+    kvm_tier_stats have the header's sizes and field offsets (a C program
+    compiled against include/kvm.h prints them)."""
+    import os
+    import shutil
+    import subprocess
+    from paged_kv_cache_meank_gb300 import _abi
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"kvm_config": _abi.KvmConfig, "kvm_buffers": _abi.KvmBuffers,
+               "kvm_step_stats": _abi.KvmStepStats, "kvm_tier_stats": _abi.KvmTierStats}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "kvm.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([cc, "-std=c99", "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle.kvmem as ora
+import oracle.tier as oracle_tier
 from gpu_helpers import (MID, assert_meank_close, assert_scores_close, assert_storage_close,
                          check_selection, from_np, to_np)
 from recall_ref import prefill_k_pages
@@ -23,7 +24,7 @@ def kvm():
 
 
 def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_step,
-               pool_extra=6, batch=7, h2d_mode=0):
+               pool_extra=6, batch=7, h2d_mode=0, host_tier=None):
     from paged_kv_cache_meank_gb300 import workload
     N_max = max(n_blocks_per_step)
     ws = workload.make_workspace(wl, seed=11, n_blocks=N_max, with_q=False)
@@ -34,8 +35,11 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
         wl, max_blocks=N_max, pool_pages=wl.view_blocks + pool_extra,
         repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
         index_location=kvm.KVM_HOST_PINNED if index_host else kvm.KVM_DEVICE,
-        h2d_batch_blocks=batch, h2d_mode=h2d_mode)
+        h2d_batch_blocks=batch, h2d_mode=h2d_mode,
+        host_tier_blocks=host_tier[0] if host_tier else 0,
+        host_tier_lambda=host_tier[1] if host_tier else 0.5)
     cfg.tile_blocks = 64
+    tier_ref = oracle_tier.HostTier(*host_tier) if host_tier else None
     ctx = kvm.Context(cfg)
     # (a) the GPU builds the index and raw K from the prefill K pages
     index_d = torch.zeros(ctx.index_shape(), dtype=ctx.index_dtype, device="cuda")
@@ -90,6 +94,9 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
         assert page_table[:len(g_sel)].cpu().tolist() == page, f"step {step} page table"
         assert st["hits"] == sum(hit) and st["misses"] == len(hit) - sum(hit)
         assert st["reroped"] == sum(rope)
+        if tier_ref is not None:   # the host-tier policy fed with this step's selection
+            h, m, dem = tier_ref.step(g_sel.tolist(), N)
+            assert (st["host_hits"], st["host_misses"], st["host_demoted"]) == (h, m, len(dem))
         blk = ctx.block_shape(1)
         nbytes = int(np.prod(blk)) * {"f32": 4, "bf16": 2, "e4m3": 1}[wl.kv_dtype]
         if repo_host:
@@ -136,6 +143,20 @@ def test_step_sequence_fp8_pages(kvm, repo_host, h2d_mode):
     hist = _run_steps(kvm, wl, repo_host, False, [qa, qb, qa], [270, 290, 300],
                       h2d_mode=h2d_mode)
     assert hist[0]["misses"] == wl.view_blocks
+
+
+def test_step_host_tier_policy(kvm):
+    """kvm_step with host_tier_blocks: every step's selection feeds the LRFU
+    host-tier policy; its hits, misses and demotions match the oracle's."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    g = torch.Generator().manual_seed(24)
+    u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
+    qs = [workload.make_queries(wl, g, "cpu", u[k % 3]) for k in range(6)]
+    hist = _run_steps(kvm, wl, True, False, qs, [240, 250, 260, 270, 285, 300], h2d_mode=1,
+                      host_tier=(wl.view_blocks + 20, 0.3))
+    assert hist[0]["host_misses"] == 0          # all blocks are created resident
+    assert sum(h["host_demoted"] for h in hist) > 0
 
 
 def test_step_host_index_tiled(kvm):
