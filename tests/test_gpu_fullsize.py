@@ -49,17 +49,26 @@ def _oracle_R(q, index, wl, n_blocks):
                                           wl.index_dtype), n_blocks)
 
 
-def test_256k_build_sampled(kvm):
-    """Mean-K and raw K over the full 8192-block, 64-layer history; sampled
-    blocks against the oracle."""
-    wl = configs.W256K
+def _draw_pages(shape, dtype, std, g):
+    """K pages as a prefill leaves them, drawn directly in the storage dtype
+    (e4m3 as uint8 bit patterns)."""
+    out = torch.empty(shape, dtype=torch.uint8 if dtype == "e4m3" else torch.bfloat16,
+                      device="cuda")
+    for i in range(0, shape[0], 1024):
+        x = torch.randn(out[i:i + 1024].shape, generator=g, device="cuda") * std
+        out[i:i + 1024] = (x.to(torch.float8_e4m3fn).view(torch.uint8) if dtype == "e4m3"
+                           else x.to(torch.bfloat16))
+    return out
+
+
+@pytest.mark.parametrize("wl", [configs.W256K, configs.W256K_FP8], ids=lambda w: w.kv_dtype)
+def test_256k_build_sampled(kvm, wl):
+    """Mean-K and raw K over the full 8192-block, 64-layer history (bf16 or
+    e4m3 pages); sampled blocks against the oracle."""
     g = torch.Generator(device="cuda").manual_seed(101)
-    N = wl.n_blocks
+    N, kd = wl.n_blocks, wl.kv_dtype
     ctx = kvm.Context(kvm.config_for(wl))
-    kp = torch.empty(ctx.block_shape(N), dtype=torch.bfloat16, device="cuda")
-    for i in range(0, N, 1024):     # K as a prefill leaves it, drawn directly
-        kp[i:i + 1024] = (torch.randn(kp[i:i + 1024].shape, generator=g, device="cuda")
-                          * wl.k_std).to(torch.bfloat16)
+    kp = _draw_pages(ctx.block_shape(N), kd, wl.k_std, g)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
     raw = torch.empty_like(kp)
     ctx.build_index(kp, 0, N, index, raw)
@@ -67,13 +76,13 @@ def test_256k_build_sampled(kvm):
     rng = np.random.default_rng(7)
     ids = np.unique(np.concatenate([[0, 1, N - 1], rng.choice(N, 29, replace=False)]))
     for b in ids:
-        kpb = to_np(kp[b:b + 1], "bf16")
-        ref = ora.meank(kpb, "bf16", int(b), wl.rope_theta)
+        kpb = to_np(kp[b:b + 1], kd)
+        ref = ora.meank(kpb, kd, int(b), wl.rope_theta)
         got = to_np(index[:, :, b:b + 1], "bf16")
-        kmax = float(np.abs(ora.as_f64(kpb, "bf16")).max()) * 2 ** 0.5
+        kmax = float(np.abs(ora.as_f64(kpb, kd)).max()) * 2 ** 0.5
         assert_meank_close(got, ref, "bf16", wl.k_std, f"block {b}", kmax)
-        exact = assert_storage_close(to_np(raw[b:b + 1], "bf16"),
-                                     ora.raw_k(kpb, "bf16", int(b), wl.rope_theta), "bf16",
+        exact = assert_storage_close(to_np(raw[b:b + 1], kd),
+                                     ora.raw_k(kpb, kd, int(b), wl.rope_theta), kd,
                                      f"raw K block {b}")
         assert exact > 0.999
 
@@ -95,26 +104,27 @@ def test_256k_score_select_all_blocks(kvm):
     assert set(ws.planted.tolist()) <= set(sel.cpu().tolist())
 
 
-def test_256k_assemble_sampled(kvm):
-    """The full 1024-slot view over the 64-layer history; sampled slots against
-    the oracle's view, every V byte compared."""
-    wl = configs.W256K
+@pytest.mark.parametrize("wl", [configs.W256K, configs.W256K_FP8], ids=lambda w: w.kv_dtype)
+def test_256k_assemble_sampled(kvm, wl):
+    """The full 1024-slot view over the 64-layer history (bf16 or e4m3 pages);
+    sampled slots against the oracle's view, every V byte compared."""
+    kd = wl.kv_dtype
     ws = workload.make_workspace(wl, seed=103, device="cuda", with_q=False)
     ctx = kvm.Context(kvm.config_for(wl))
     N, V = wl.n_blocks, wl.view_blocks
     rng = np.random.default_rng(8)
     ids = np.sort(rng.choice(N, V, replace=False)).astype(np.int32)
-    kp = torch.empty(ctx.block_shape(V), dtype=torch.bfloat16, device="cuda")
+    kp = torch.empty(ctx.block_shape(V), dtype=ctx.kv_dtype, device="cuda")
     vp = torch.empty_like(kp)
     ctx.assemble_view(torch.from_numpy(ids).cuda(), None, V, ws.raw_k, ws.v, kp, vp)
     ctx.sync()
     assert torch.equal(vp, ws.v[torch.from_numpy(ids).long().cuda()])
     for j in np.unique(np.concatenate([[0, V - 1], rng.choice(V, 14, replace=False)])):
         b = int(ids[j])
-        raw = to_np(ws.raw_k[b:b + 1], "bf16")
+        raw = to_np(ws.raw_k[b:b + 1], kd)
         c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
-        ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
-        assert_storage_close(to_np(kp[j:j + 1], "bf16"), ref, "bf16", f"slot {j}")
+        ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, kd), c, s), kd)
+        assert_storage_close(to_np(kp[j:j + 1], kd), ref, kd, f"slot {j}")
 
 
 def test_10m_scoring_properties(kvm):
