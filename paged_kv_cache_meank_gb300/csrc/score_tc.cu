@@ -15,12 +15,13 @@
 //                128-byte-swizzled shared memory (one copy per 64-element K atom)
 //   warp 1       MMA issuer: one thread issues tcgen05.mma into one of two TMEM
 //                accumulators and commits to mbarriers
-//   warps 2..17  epilogue, four warps per TMEM lane quadrant, each taking a
-//                quarter of the accumulator's columns; each thread owns one
-//                block and sums its quarter of the rows in registers, and the
-//                four quarters combine in a fixed order through shared memory.
-//                An accumulator goes back to the MMA warp as soon as it has
-//                been read into registers, before the exponentials.
+//   warps 2..17  epilogue in two groups of eight that take alternate tiles
+//                (group g owns TMEM accumulator g); in a group, two warps per
+//                TMEM lane quadrant each take half of the accumulator's
+//                columns.  Each thread owns one block and sums its half of the
+//                rows in registers, and the two halves combine in a fixed order
+//                through shared memory.  An accumulator goes back to the MMA
+//                warp once its last columns are in registers.
 // Every mbarrier wait is bounded; on timeout the kernel raises the device
 // error flag (bit 4) and winds down, freeing its TMEM.
 #include <cuda.h>
@@ -54,7 +55,7 @@ struct Lay {
     static constexpr int OFF_O = OFF_Q + QB;       // float[kQRows]
     static constexpr int OFF_X = OFF_O + kQRows * 4;   // warp exchange, 1536 floats
     static constexpr int OFF_BAR = OFF_X + 1536 * 4;
-    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
 };
 
 // Sum of 2^(v*c + no) over n loaded columns (n a multiple of 16, at most 64;
@@ -106,7 +107,7 @@ __device__ __forceinline__ float exp_sum_n(const uint32_t *r, const float *no, f
 
 }  // namespace
 
-// NC: columns per epilogue warp when fixed at compile time (48 for 192 query
+// NC: columns per epilogue warp when fixed at compile time (96 for 192 query
 // rows), 0 for any row count.
 template <int D, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,8 +127,8 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
-    uint64_t *xfull = tempty + 2;        // [4][4]: warps 1..3 of a quadrant wrote their partials
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + 16);
+    uint64_t *xfull = tempty + 2;        // [2][4][4]: a warp's partner wrote its partial
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lg = blockIdx.y;
@@ -146,9 +147,9 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
-            tc::mbar_init(&tempty[b], kEpiWarps * 32);
+            tc::mbar_init(&tempty[b], (kEpiWarps / 2) * 32);
         }
-        for (int k = 0; k < 16; ++k) tc::mbar_init(&xfull[k], 96);
+        for (int k = 0; k < 32; ++k) tc::mbar_init(&xfull[k], 32);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -242,82 +243,101 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
             }
         }
     } else {
+        // Two groups of eight warps take alternate tiles: group gr owns TMEM
+        // buffer gr and the tiles i = gr, gr + 2, ..., so that one group's
+        // waits and TMEM loads overlap the other group's exponentials.  In a
+        // group two warps share a lane quadrant, each taking half of the n2
+        // columns in chunks; the buffer goes back to the MMA warp once its
+        // last chunk is in registers.
         const int ew = warp - 2;                    // 0..15
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
-        const int sub = ew >> 2;                    // which quarter of the columns
+        const int gr = ew >> 3;                     // group
+        const int hf = (ew >> 2) & 1;               // which half of the columns
         const int lrow = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        // the n2 columns in 16-column units, split into four near-equal runs
+        // the n2 columns in 16-column units, split into two near-equal runs
         const int nu = n2 >> 4;
-        const int u0 = (sub * nu) >> 2, u1 = ((sub + 1) * nu) >> 2;
+        const int u0 = (hf * nu) >> 1, u1 = ((hf + 1) * nu) >> 1;
         const int my_c0 = u0 * 16;
         const int my_nc = (u1 - u0) * 16;
-        // warp 0 of a quadrant combines tile i - 1 while on tile i, when the
-        // other three warps' partials of tile i - 1 are long written
+        // warp hf = 0 of a quadrant adds its partner's partial of the group's
+        // tile jj - 1 while on tile jj, when that partial is long written
         float pend = 0.f;
-        auto combine = [&](int j, float own) -> bool {
-            const int xs = j & 3;
-            if (!tc::mbar_wait(&xfull[xs * 4 + quad], (j >> 2) & 1, kWaitLimit)) return false;
-            const float *slot = xch + ((xs * 4 + quad) * 3) * 32 + lane;
-            const float sum = ((own + slot[0]) + slot[32]) + slot[64];
-            const int64_t gb0 = cb0 + (int64_t)j * TB;
+        auto combine = [&](int jj, float own) -> bool {
+            const int bar = (gr * 4 + (jj & 3)) * 4 + quad;
+            if (!tc::mbar_wait(&xfull[bar], (jj >> 2) & 1, kWaitLimit)) return false;
+            const float sum = own + xch[bar * 32 + lane];
+            const int64_t gb0 = cb0 + (int64_t)(2 * jj + gr) * TB;
             if (lrow < min((int64_t)TB, cb1 - gb0))
                 scr.partial[(size_t)lg * partial_stride + gb0 + lrow] = sum;
             return true;
         };
         bool ok = true;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            const uint32_t bph = (i >> 1) & 1;
-            if (!tc::mbar_wait(&tfull[buf], bph, kWaitLimit)) {
+        int jj = 0;
+        for (int i = gr; i < n_tiles; i += 2, ++jj) {
+            if (!tc::mbar_wait(&tfull[gr], jj & 1, kWaitLimit)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            const uint32_t taddr = tmem + lane_base + buf * 256;
-            uint32_t r[64];
+            const uint32_t taddr = tmem + lane_base + gr * 256;
+            uint32_t r[48];
             float sum;
-            if (NC == 48) {   // 192 query rows: 48 columns per warp
+            if (NC == 96) {   // 192 query rows: 96 columns per warp, two chunks of 48
                 tc::tmem_ld32_async(taddr + my_c0, r);
                 tc::tmem_ld16_async(taddr + my_c0 + 32, r + 32);
                 tc::tmem_wait_ld(r);
                 tc::tmem_wait_ld(r + 16);
                 tc::tmem_wait_ld(r + 32);
-                tc::tc_fence_before();
-                tc::mbar_arrive(&tempty[buf]);
                 sum = exp_sum_n<48>(r, o_r + my_c0, scale_log2);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    if (k * 32 + 32 <= my_nc)
-                        tc::tmem_ld32_async(taddr + my_c0 + k * 32, r + k * 32);
-                    else if (k * 32 + 16 <= my_nc)
-                        tc::tmem_ld16_async(taddr + my_c0 + k * 32, r + k * 32);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (k * 16 < my_nc) tc::tmem_wait_ld(r + k * 16);
+                tc::tmem_ld32_async(taddr + my_c0 + 48, r);
+                tc::tmem_ld16_async(taddr + my_c0 + 80, r + 32);
+                tc::tmem_wait_ld(r);
+                tc::tmem_wait_ld(r + 16);
+                tc::tmem_wait_ld(r + 32);
                 tc::tc_fence_before();
-                tc::mbar_arrive(&tempty[buf]);
-                sum = exp_sum(r, o_r + my_c0, my_nc, scale_log2);
-            }
-            // the quadrant's four warps combine in a fixed order through a
-            // four-deep ring of shared-memory slots.  A slot is not rewritten
-            // before warp 0 of the quadrant read it: tile i + 3 needs that
-            // warp's arrival on tempty for tile i + 1, which follows its read
-            // of tile i's slots.
-            if (sub) {
-                xch[(((i & 3) * 4 + quad) * 3 + sub - 1) * 32 + lane] = sum;
-                tc::mbar_arrive(&xfull[(i & 3) * 4 + quad]);
+                tc::mbar_arrive(&tempty[gr]);
+                sum += exp_sum_n<48>(r, o_r + my_c0 + 48, scale_log2);
             } else {
-                if (i > 0 && !combine(i - 1, pend)) {
+                sum = 0.f;
+                if (my_nc == 0) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&tempty[gr]);
+                }
+                for (int c = 0; c < my_nc; c += 32) {
+                    const int n = min(32, my_nc - c);    // 16 or 32
+                    if (n == 32) {
+                        tc::tmem_ld32_async(taddr + my_c0 + c, r);
+                        tc::tmem_wait_ld(r);
+                        tc::tmem_wait_ld(r + 16);
+                    } else {
+                        tc::tmem_ld16_async(taddr + my_c0 + c, r);
+                        tc::tmem_wait_ld(r);
+                    }
+                    if (c + 32 >= my_nc) {
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(&tempty[gr]);
+                    }
+                    sum += exp_sum(r, o_r + my_c0 + c, n, scale_log2);
+                }
+            }
+            // the partner's partial goes through a four-deep ring of slots per
+            // group.  A slot is not rewritten before warp hf = 0 read it: the
+            // group's tile jj + 4 needs that warp's arrival on tempty for tile
+            // jj + 3, which follows its read of tile jj's slot.
+            const int bar = (gr * 4 + (jj & 3)) * 4 + quad;
+            if (hf) {
+                xch[bar * 32 + lane] = sum;
+                tc::mbar_arrive(&xfull[bar]);
+            } else {
+                if (jj > 0 && !combine(jj - 1, pend)) {
                     ok = false;
                     break;
                 }
                 pend = sum;
             }
         }
-        if (sub == 0 && n_tiles > 0 && ok && !combine(n_tiles - 1, pend)) ok = false;
+        if (hf == 0 && jj > 0 && ok && !combine(jj - 1, pend)) ok = false;
         if (!ok) atomicOr(err, 4);
     }
     tc::tc_fence_before();
@@ -389,16 +409,16 @@ cudaError_t launch_score_pass2_tc(const ScoreShape &sh, const void *q, const voi
                                   int64_t b_index0, int64_t b_begin, int64_t b_end, int n_chunks,
                                   const ScoreScratch &scr, int64_t partial_stride, int *err,
                                   cudaStream_t s) {
-    const bool n48 = ((sh.rows + 15) & ~15) == 192;
+    const bool n192 = ((sh.rows + 15) & ~15) == 192;
     if (sh.d == 128)
-        return n48 ? pass2_t<128, 48>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
-                                      partial_stride, err, s)
-                   : pass2_t<128, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
-                                     partial_stride, err, s);
-    return n48 ? pass2_t<64, 48>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
-                                 partial_stride, err, s)
-               : pass2_t<64, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
-                                partial_stride, err, s);
+        return n192 ? pass2_t<128, 96>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
+                                       partial_stride, err, s)
+                    : pass2_t<128, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
+                                      partial_stride, err, s);
+    return n192 ? pass2_t<64, 96>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
+                                  partial_stride, err, s)
+                : pass2_t<64, 0>(sh, q, index, b_index0, b_begin, b_end, n_chunks, scr,
+                                 partial_stride, err, s);
 }
 
 }  // namespace kvm
