@@ -5,10 +5,16 @@
  *   [KVMem] "KVMem: Virtualizing Million-Token Agent Workspaces on a Consumer GPU"
  *   [InfS]  "InferScale: GPU-Native KV Injection for Personalized LLM Serving"
  *
- * One process, one GPU (sm_103a).  Every buffer is allocated by the caller
- * (device memory, or pinned host memory where stated) and must outlive the
- * calls that use it; the library never allocates or frees device memory and
- * never frees caller memory.  All work is enqueued on the caller's stream;
+ * One process, one GPU (sm_103a).  Every buffer is allocated by the caller and
+ * must outlive the calls that use it; the library never allocates or frees
+ * device memory and never frees caller memory.  A buffer that a call's kernels
+ * read or write may be device memory or pinned (page-locked) host memory; the
+ * kernels then access pinned host memory directly over the host link, moving
+ * only the bytes they touch.  Pageable host memory is rejected
+ * (KVM_ERR_INVALID_ARG).  The one exception is the Mean-K index read by
+ * kvm_score_select: with index_location KVM_DEVICE it must be device memory
+ * (TMA streams it), and with KVM_HOST_PINNED it is pinned host memory staged
+ * in tiles.  All work is enqueued on the caller's stream;
  * functions return after enqueueing unless stated otherwise.  No C++
  * exception crosses this boundary: every function returns a kvm_status.
  * Argument errors are detected on the host before anything is enqueued and

@@ -201,6 +201,40 @@ void reset_pool(kvm_ctx *c) {
 
 }  // namespace
 
+// The address a kernel uses for a caller buffer: device (or managed) memory as
+// is; pinned host memory through its device alias, so that kernels read or
+// write it over the host link without a staging copy.  Pageable host memory is
+// rejected.  NULL stays NULL.
+static kvm_status kernel_ptr(const void *p, const void **out, const char *what) {
+    *out = nullptr;
+    if (!p) return KVM_OK;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(KVM_ERR_INVALID_ARG, "%s: not an address the GPU can use", what);
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return KVM_OK;
+    }
+    if (a.type == cudaMemoryTypeHost) {
+        void *d = nullptr;
+        const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void *>(p), 0);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+        *out = d;
+        return KVM_OK;
+    }
+    return fail(KVM_ERR_INVALID_ARG,
+                "%s: pageable host memory; use device memory or pinned host memory", what);
+}
+template <typename T>
+static kvm_status kernel_ptr(T *p, T **out, const char *what) {
+    const void *q = nullptr;
+    const kvm_status st = kernel_ptr(static_cast<const void *>(p), &q, what);
+    *out = static_cast<T *>(const_cast<void *>(q));
+    return st;
+}
+
 extern "C" {
 
 size_t kvm_workspace_bytes(const kvm_config *cfg) {
@@ -305,6 +339,11 @@ kvm_status kvm_build_index(kvm_ctx *c, const void *k_pages, int64_t first_block,
         return fail(KVM_ERR_CAPACITY, "positions up to %lld beyond max_positions %lld",
                     (long long)((first_block + n_blocks) * 32), (long long)c->cfg.max_positions);
     if (n_blocks == 0) return KVM_OK;
+    kvm_status st;
+    if ((st = kernel_ptr(k_pages, &k_pages, "k_pages")) != KVM_OK ||
+        (st = kernel_ptr(index, &index, "index")) != KVM_OK ||
+        (st = kernel_ptr(raw_k_out, &raw_k_out, "raw_k_out")) != KVM_OK)
+        return st;
     const cudaError_t e = kvm::launch_meank(
         c->cfg.kv_dtype, c->cfg.index_dtype, c->cfg.head_dim, k_pages, raw_k_out, index,
         c->cfg.max_blocks, first_block, n_blocks, c->cfg.n_layers * c->cfg.n_kv_heads,
@@ -402,6 +441,20 @@ kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const 
     if (n_blocks > c->cfg.max_blocks)
         return fail(KVM_ERR_CAPACITY, "n_blocks %lld > max_blocks %lld", (long long)n_blocks,
                     (long long)c->cfg.max_blocks);
+    kvm_status st;
+    if ((st = kernel_ptr(q, &q, "q")) != KVM_OK ||
+        (st = kernel_ptr(scores_out, &scores_out, "scores_out")) != KVM_OK ||
+        (st = kernel_ptr(sel_ids_out, &sel_ids_out, "sel_ids_out")) != KVM_OK)
+        return st;
+    if (c->cfg.index_location == KVM_DEVICE) {
+        // the scoring kernels stream the index with TMA from device memory
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, index) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            return fail(KVM_ERR_INVALID_ARG,
+                        "index: device memory required (KVM_HOST_PINNED for a host index)");
+        }
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const kvm::ScoreShape sh = shape_of(c, n_queries, c->cfg.max_blocks);
     int64_t c0 = 0, c1 = n_blocks;
@@ -409,9 +462,9 @@ kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const 
         c0 = std::min<int64_t>(c->cfg.sink_blocks, n_blocks);
         c1 = std::max<int64_t>(n_blocks - c->cfg.recent_blocks, c0);
     }
-    kvm_status st = c->cfg.index_location == KVM_DEVICE
-                        ? score_device(c, sh, q, index, n_blocks, c0, c1, scores_out, s)
-                        : score_host_tiled(c, sh, q, index, n_blocks, c0, c1, scores_out, s);
+    st = c->cfg.index_location == KVM_DEVICE
+             ? score_device(c, sh, q, index, n_blocks, c0, c1, scores_out, s)
+             : score_host_tiled(c, sh, q, index, n_blocks, c0, c1, scores_out, s);
     if (st != KVM_OK) return st;
     const cudaError_t e = kvm::launch_select(scores_out, n_blocks, c->cfg.sink_blocks,
                                              c->cfg.recent_blocks, c->cfg.view_blocks,
@@ -433,6 +486,14 @@ kvm_status kvm_assemble_view(kvm_ctx *c, const int32_t *sel_ids, const int32_t *
     if ((int64_t)n_sel * 32 > c->cfg.max_positions)
         return fail(KVM_ERR_CAPACITY, "view of %d slots beyond max_positions", n_sel);
     if (n_sel == 0) return KVM_OK;
+    kvm_status st;
+    if ((st = kernel_ptr(sel_ids, &sel_ids, "sel_ids")) != KVM_OK ||
+        (st = kernel_ptr(page_ids, &page_ids, "page_ids")) != KVM_OK ||
+        (st = kernel_ptr(raw_k_repo, &raw_k_repo, "raw_k_repo")) != KVM_OK ||
+        (st = kernel_ptr(v_repo, &v_repo, "v_repo")) != KVM_OK ||
+        (st = kernel_ptr(k_pages, &k_pages, "k_pages")) != KVM_OK ||
+        (st = kernel_ptr(v_pages, &v_pages, "v_pages")) != KVM_OK)
+        return st;
     const cudaError_t e = kvm::launch_assemble_ids(
         c->cfg.kv_dtype, c->cfg.head_dim, sel_ids, page_ids, n_sel, c->cfg.max_blocks,
         raw_k_repo, v_repo, k_pages, v_pages, c->cfg.n_layers * c->cfg.n_kv_heads, c->table,

@@ -228,6 +228,43 @@ def test_assemble_roundtrip_at_original_positions(kvm, kv_dtype):
     assert np.array_equal(to_np(out, kv_dtype), kp_ref)
 
 
+def test_pinned_host_buffers(kvm):
+    """Every call accepts pinned host buffers, which the kernels read over the
+    host link; the results are bit-identical to the same calls on device
+    buffers.  Pageable host memory and a host index on the device path are
+    rejected."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=120, view_blocks=40)
+    ws = workload.make_workspace(wl, seed=31)
+    ctx = _ctx(kvm, wl)
+    N, V = wl.n_blocks, wl.view_blocks
+    kp = from_np(prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta), "bf16")
+
+    def run(kp_in, v_in, q_in):
+        index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+        raw = torch.empty(ctx.block_shape(N), dtype=torch.bfloat16, device="cuda")
+        ctx.build_index(kp_in, 0, N, index, raw)
+        scores = torch.empty(N, device="cuda")
+        sel = torch.empty(V, dtype=torch.int32, device="cuda")
+        ctx.score_select(q_in, wl.n_queries, index, N, scores, sel)
+        k_out = torch.empty(ctx.block_shape(V), dtype=torch.bfloat16, device="cuda")
+        v_out = torch.empty_like(k_out)
+        ctx.assemble_view(sel, None, V, raw, v_in, k_out, v_out)
+        ctx.sync()
+        return index, raw, scores, sel, k_out, v_out
+
+    dev = run(kp, ws.v.cuda(), ws.q.cuda())
+    host = run(kp.cpu().pin_memory(), ws.v.pin_memory(), ws.q.pin_memory())
+    for a, b in zip(dev, host):
+        assert torch.equal(a, b)
+    with pytest.raises(kvm.KvmError) as ei:                  # pageable memory
+        ctx.build_index(kp.cpu(), 0, N, dev[0], None)
+    assert ei.value.name == "KVM_ERR_INVALID_ARG"
+    with pytest.raises(kvm.KvmError):                        # index on the TMA path
+        ctx.score_select(ws.q.cuda(), wl.n_queries, dev[0].cpu().pin_memory(), N, dev[2],
+                         dev[3])
+
+
 def test_device_range_checks(kvm):
     """Out-of-range ids are skipped and reported by kvm_sync, and the context
     stays usable."""
