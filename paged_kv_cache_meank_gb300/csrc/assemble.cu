@@ -28,6 +28,11 @@ struct SlotWork {
     // Rotate one block's K to positions pos0 + t for pairs [lg0, lg1) and copy V.
     // src_k and dst_k may be the same block (an in-place delta rotation), so
     // they carry no __restrict__
+    // U: (layer, kv head) pairs whose loads are issued before any of them is
+    // stored.  Batching pays for sources in device memory; for blocks read
+    // from pinned host memory over the host link, one pair at a time was
+    // measured faster.
+    template <int U>
     __device__ static void run(const T *src_k, const T *__restrict__ src_v,
                                T *dst_k, T *__restrict__ dst_v, int64_t pos0,
                                int lg0, int lg1, const float2 *__restrict__ table,
@@ -60,34 +65,49 @@ struct SlotWork {
         const size_t row = (size_t)tok * D + (size_t)c * PPT;
         const bool do_v = (src_v != nullptr) && (dst_v != nullptr);
         using V = typename VecTraits<T>::V;
-#pragma unroll 2
-        for (int lg = lg0; lg < lg1; ++lg) {
-            const size_t off = (size_t)lg * kBlockTokens * D + row;
-            V vx, vy, wx{}, wy{};
-            ld_stream_v(src_k + off, vx);
-            ld_stream_v(src_k + off + HD, vy);
-            if (do_v) {
-                ld_stream_v(src_v + off, wx);
-                ld_stream_v(src_v + off + HD, wy);
-            }
-            float x[PPT], y[PPT], ox[PPT], oy[PPT];
-            VecTraits<T>::unpack(vx, x);
-            VecTraits<T>::unpack(vy, y);
+        // The loads of U pairs are issued explicitly ahead of their stores
+        // because src_k and dst_k may alias (in-place delta rotation);
+        // different pairs never overlap, and each element is still read before
+        // it is written.
+        constexpr int kOuterUnroll = U == 1 ? 2 : 1;
+#pragma unroll kOuterUnroll
+        for (int lg = lg0; lg < lg1; lg += U) {
+            V vx[U], vy[U], wx[U], wy[U];
 #pragma unroll
-            for (int i = 0; i < PPT; ++i) {
-                // R_p: (x cos - y sin, x sin + y cos), each product rounded
-                ox[i] = __fsub_rn(__fmul_rn(x[i], cs[i]), __fmul_rn(y[i], sn[i]));
-                oy[i] = __fadd_rn(__fmul_rn(x[i], sn[i]), __fmul_rn(y[i], cs[i]));
+            for (int u = 0; u < U; ++u) {
+                if (lg + u < lg1) {
+                    const size_t off = (size_t)(lg + u) * kBlockTokens * D + row;
+                    ld_stream_v(src_k + off, vx[u]);
+                    ld_stream_v(src_k + off + HD, vy[u]);
+                    if (do_v) {
+                        ld_stream_v(src_v + off, wx[u]);
+                        ld_stream_v(src_v + off + HD, wy[u]);
+                    }
+                }
             }
-            st_stream_v(dst_k + off, VecTraits<T>::pack(ox));
-            st_stream_v(dst_k + off + HD, VecTraits<T>::pack(oy));
-            if (dst_raw != nullptr) {
-                st_stream_v(dst_raw + off, vx);
-                st_stream_v(dst_raw + off + HD, vy);
-            }
-            if (do_v) {
-                st_stream_v(dst_v + off, wx);
-                st_stream_v(dst_v + off + HD, wy);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (lg + u >= lg1) break;
+                const size_t off = (size_t)(lg + u) * kBlockTokens * D + row;
+                float x[PPT], y[PPT], ox[PPT], oy[PPT];
+                VecTraits<T>::unpack(vx[u], x);
+                VecTraits<T>::unpack(vy[u], y);
+#pragma unroll
+                for (int i = 0; i < PPT; ++i) {
+                    // R_p: (x cos - y sin, x sin + y cos), each product rounded
+                    ox[i] = __fsub_rn(__fmul_rn(x[i], cs[i]), __fmul_rn(y[i], sn[i]));
+                    oy[i] = __fadd_rn(__fmul_rn(x[i], sn[i]), __fmul_rn(y[i], cs[i]));
+                }
+                st_stream_v(dst_k + off, VecTraits<T>::pack(ox));
+                st_stream_v(dst_k + off + HD, VecTraits<T>::pack(oy));
+                if (dst_raw != nullptr) {
+                    st_stream_v(dst_raw + off, vx[u]);
+                    st_stream_v(dst_raw + off + HD, vy[u]);
+                }
+                if (do_v) {
+                    st_stream_v(dst_v + off, wx[u]);
+                    st_stream_v(dst_v + off + HD, wy[u]);
+                }
             }
         }
     }
@@ -109,7 +129,9 @@ assemble_ids_kernel(const int32_t *__restrict__ sel_ids, const int32_t *__restri
     }
     const size_t blk = (size_t)LG * kBlockTokens * D;
     const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
-    SlotWork<T, D>::run(raw_k_repo + b * blk, v_repo ? v_repo + b * blk : nullptr,
+    // 128 bytes of loads in flight per thread whatever the element size
+    constexpr int U = 128 / (4 * (int)sizeof(typename VecTraits<T>::V));
+    SlotWork<T, D>::template run<U>(raw_k_repo + b * blk, v_repo ? v_repo + b * blk : nullptr,
                         k_pages + p * blk, v_pages ? v_pages + p * blk : nullptr,
                         (int64_t)j * kBlockTokens, lg0, lg1, table, tab);
 }
@@ -130,7 +152,8 @@ assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
     // a delta rotation runs in place (src_k == dst_k): every thread reads its
     // 16-byte pieces before it writes the same addresses
     const int lg0 = blockIdx.y * lg_per_cta, lg1 = min(LG, lg0 + lg_per_cta);
-    SlotWork<T, D>::run(static_cast<const T *>(sd.src_k), static_cast<const T *>(sd.src_v),
+    SlotWork<T, D>::template run<1>(static_cast<const T *>(sd.src_k),
+                                    static_cast<const T *>(sd.src_v),
                         static_cast<T *>(sd.dst_k), static_cast<T *>(sd.dst_v), sd.pos0, lg0,
                         lg1, table, tab, static_cast<T *>(sd.dst_raw), delta);
 }
