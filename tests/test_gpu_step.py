@@ -129,8 +129,8 @@ def test_step_sequence(kvm, repo_host, h2d_mode):
     assert hist[2]["misses"] == 0 and hist[2]["reroped"] == 0
 
 
-@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 1)],
-                         ids=["repo-device", "repo-host-gpu-pull"])
+@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 0), (True, 1)],
+                         ids=["repo-device", "repo-host-copy-engine", "repo-host-gpu-pull"])
 def test_step_sequence_fp8_pages(kvm, repo_host, h2d_mode):
     """The same working-set sequence with 8-bit (e4m3) K / V pages: Mean-K from
     e4m3 prefill K, view K re-RoPE'd and rounded to e4m3, V bytes moved."""
