@@ -125,14 +125,17 @@ template <typename T, typename TI, int D>
 static cudaError_t launch_meank_t(const void *k_pages, void *raw_out, void *index,
                                   int64_t index_cap, int64_t first_block, int64_t n_blocks,
                                   int LG, const float2 *table, cudaStream_t s) {
-    // long runs of (layer, kv head) pairs per CTA amortise the table stage; short
-    // ones keep the machine full when few blocks are built
+    // long runs of (layer, kv head) pairs per CTA amortise the table stage (16 KB
+    // per CTA at d = 128); short ones keep the machine full when few blocks are
+    // built.  The cap was measured on the 256K build: 128 pairs for 2- and
+    // 4-byte elements, 256 for e4m3, whose pairs carry half the bytes.
     int lg_per_cta = LG;
     const int64_t want_ctas = 152 * 16;
     while (lg_per_cta > kMeanKWarps &&
            n_blocks * ((LG + lg_per_cta - 1) / lg_per_cta) < want_ctas)
         lg_per_cta = (lg_per_cta + 1) / 2;
-    if (lg_per_cta > 8 * kMeanKWarps) lg_per_cta = 8 * kMeanKWarps;
+    constexpr int kCap = (sizeof(T) == 1 ? 64 : 32) * kMeanKWarps;
+    if (lg_per_cta > kCap) lg_per_cta = kCap;
     dim3 grid((unsigned)n_blocks, (unsigned)((LG + lg_per_cta - 1) / lg_per_cta));
     meank_kernel<T, TI, D><<<grid, kMeanKWarps * 32, 0, s>>>(
         static_cast<const T *>(k_pages), static_cast<T *>(raw_out), static_cast<TI *>(index),
