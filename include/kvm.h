@@ -353,9 +353,14 @@ const char *kvm_status_string(kvm_status s);
 /* Detail of the last error raised on the calling thread ("" if none). */
 const char *kvm_last_error(void);
 
-/* Host-side fault injection for tests: make the n-th (1-based) next host
- * copy submission (what = 1) or kernel launch (what = 2) of kvm_step fail
- * with KVM_ERR_INJECTED.  what = 0 clears.  The context stays usable. */
+/* Fault injection for tests.  what = 1 / 2: make the n-th (1-based) next host
+ * copy submission / kernel launch of kvm_step fail with KVM_ERR_INJECTED.
+ * what = 3: the n-th next tensor-core scoring pass (kvm_score_select or
+ * kvm_step; passes 1 and 2 both count) runs with its TMA producer idle, so
+ * its bounded device waits run out after about a second each; the call
+ * itself returns KVM_OK and the next kvm_sync returns KVM_ERR_TIMEOUT.  Its
+ * scores and selection are then meaningless (ids stay in range).  what = 0
+ * clears.  The context stays usable in every case. */
 kvm_status kvm_debug_inject(kvm_ctx *ctx, int32_t what, int64_t nth);
 
 #ifdef __cplusplus

@@ -352,6 +352,14 @@ kvm_status kvm_build_index(kvm_ctx *c, const void *k_pages, int64_t first_block,
     return KVM_OK;
 }
 
+// The shape for one scoring pass launch: a pending injection of kind 3 makes
+// the n-th tensor-core pass run with an idle TMA producer.
+static kvm::ScoreShape pass_shape(kvm_ctx *c, kvm::ScoreShape sh) {
+    if (kvm::score_uses_tc(c->cfg.q_dtype, c->cfg.index_dtype, sh))
+        sh.idle_producer = injected(c, 3) ? 1 : 0;
+    return sh;
+}
+
 // Blocks [c0, c1) are scored (the candidate set); the rest of [0, N) get 0.
 static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void *q,
                                const void *index, int64_t N, int64_t c0, int64_t c1,
@@ -359,14 +367,14 @@ static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void
     cudaError_t e;
     if (c1 > c0) {
         const int nch = kvm::score_chunks(sh, c1 - c0, kvm::kMaxChunks);
-        if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0,
-                                         c0, c1, 0, nch, c->scr, s)) != cudaSuccess)
+        if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, pass_shape(c, sh),
+                                         q, index, 0, c0, c1, 0, nch, c->scr, s)) != cudaSuccess)
             return cuda_fail(e, "score pass 1");
         if ((e = kvm::launch_score_combine(sh, nch, c->scr, s)) != cudaSuccess)
             return cuda_fail(e, "score combine");
-        if ((e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, sh, q, index, 0,
-                                         c0, c1, nch, c->scr, c->cfg.max_blocks, s)) !=
-            cudaSuccess)
+        if ((e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, pass_shape(c, sh),
+                                         q, index, 0, c0, c1, nch, c->scr, c->cfg.max_blocks,
+                                         s)) != cudaSuccess)
             return cuda_fail(e, "score pass 2");
     }
     if ((e = kvm::launch_score_reduce(sh, N, c0, c1, c->scr, c->cfg.max_blocks, scores, s)) !=
@@ -410,11 +418,13 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
             KVM_CUDA(cudaEventRecord(c->ev_ready[buf], c->copy_stream));
             KVM_CUDA(cudaStreamWaitEvent(s, c->ev_ready[buf], 0));
             if (pass == 1)
-                e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
+                e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype,
+                                            pass_shape(c, tsh), q,
                                             c->stage[buf], b0, lo, hi, (int)(t * cpt), cpt,
                                             c->scr, s);
             else
-                e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype, tsh, q,
+                e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype,
+                                            pass_shape(c, tsh), q,
                                             c->stage[buf], b0, lo, hi, cpt, c->scr,
                                             c->cfg.max_blocks, s);
             if (e != cudaSuccess) return cuda_fail(e, "tiled score pass");
@@ -827,8 +837,8 @@ const char *kvm_last_error(void) { return g_last_error.c_str(); }
 
 kvm_status kvm_debug_inject(kvm_ctx *c, int32_t what, int64_t nth) {
     if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
-    if (what < 0 || what > 2 || (what != 0 && nth < 1))
-        return fail(KVM_ERR_INVALID_ARG, "what must be 0..2 and nth >= 1");
+    if (what < 0 || what > 3 || (what != 0 && nth < 1))
+        return fail(KVM_ERR_INVALID_ARG, "what must be 0..3 and nth >= 1");
     c->inject_what = what;
     c->inject_nth = nth;
     c->inject_seen = 0;

@@ -45,6 +45,8 @@ struct ScoreShape {
     int64_t index_cap;  // row stride (in blocks) of the index buffer being read
     int chunk_cap;      // chunk stride of the (max, sum) scratch per (layer, kv head)
     int variant;        // 0: tensor cores where supported, 1: CUDA cores
+    int idle_producer;  // 1: a tensor-core pass's TMA producer issues nothing, so
+                        // that its bounded waits run out (failure-detection tests)
 };
 
 // ---- rope_table.cu
@@ -82,6 +84,8 @@ struct ScoreScratch {
 
 // Pass 1 over blocks [b_begin, b_end) of the index (rows of `index` addressed
 // relative to b_index0), writing chunks [chunk0, chunk0 + n_chunks).
+// True where the passes of a call run on the tensor-core kernels.
+bool score_uses_tc(int q_dtype, int index_dtype, const ScoreShape &sh);
 cudaError_t launch_score_pass1(int q_dtype, int index_dtype, const ScoreShape &sh,
                                const void *q, const void *index, int64_t b_index0,
                                int64_t b_begin, int64_t b_end, int chunk0, int n_chunks,

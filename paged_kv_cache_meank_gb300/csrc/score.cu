@@ -14,7 +14,8 @@
 // This file holds the CUDA-core ("SIMT") variant: one thread per query row
 // with the row in shared memory, eight Mean-K vectors per step broadcast from
 // shared memory, and warp-shuffle reductions across rows for pass 2.  It reads
-// any element type.  The tensor-core variant for bf16 lives in score_mma.cu.
+// any element type.  The tensor-core variant for bf16 lives in score_tc1.cu (pass 1)
+// and score_tc.cu (pass 2).
 #include <math.h>
 
 #include <algorithm>

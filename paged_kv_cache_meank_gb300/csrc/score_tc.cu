@@ -22,8 +22,10 @@
 //                rows in registers, and the two halves combine in a fixed order
 //                through shared memory.  An accumulator goes back to the MMA
 //                warp once its last columns are in registers.
-// Every mbarrier wait is bounded; on timeout the kernel raises the device
-// error flag (bit 4) and winds down, freeing its TMEM.
+// Every mbarrier wait is bounded (one second of global time); on timeout the
+// kernel raises the device error flag (bit 4) and winds down: the producer
+// waits for the copies it issued, the MMA warp for its last commit, and then
+// the TMEM is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,7 +43,7 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitNs = 1000000000u;   // 1 s
 constexpr int kQRows = 256;         // largest N (query rows per kv head)
 
 template <int D>
@@ -201,10 +203,13 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int i = 0; i < n_tiles; ++i) {
+            // an idle producer (a test of the bounded waits) issues nothing
+            const int n_load = sh.idle_producer ? 0 : n_tiles;
+            int issued = 0;
+            for (int i = 0; i < n_load; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
+                if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitNs)) { atomicOr(err, 4); break; }
                 tc::mbar_expect_tx(&full[s], LY::TILE);
                 const int32_t y =
                     (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
@@ -212,20 +217,29 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
                 for (int a = 0; a < LY::KA; ++a)
                     tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
                                     a * 64, y);
+                ++issued;
             }
+            // every issued copy lands before the CTA ends: wait for the last
+            // use of each ring stage (at once in a run without errors)
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                if (!tc::mbar_wait(&full[i % kStages], (i / kStages) & 1, kWaitNs)) {
+                    atomicOr(err, 4);
+                    break;
+                }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t qbase = tc::smem_u32(qs);
             const uint32_t tbase = tc::smem_u32(tiles);
             const uint32_t idesc = tc::idesc_bf16_f32(128, n2);
+            int last = -1;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
                 const int buf = i & 1;
                 const uint32_t bph = (i >> 1) & 1;
-                if (!tc::mbar_wait(&full[s], ph, kWaitLimit)) { atomicOr(err, 4); break; }
-                if (!tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitLimit)) { atomicOr(err, 4); break; }
+                if (!tc::mbar_wait(&full[s], ph, kWaitNs)) { atomicOr(err, 4); break; }
+                if (!tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitNs)) { atomicOr(err, 4); break; }
                 tc::tc_fence_after();
                 const uint32_t d = tmem + buf * 256;
                 const uint32_t tile = tbase + s * LY::TILE;
@@ -240,7 +254,12 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
                 }
                 tc::mma_commit(&empty[s]);
                 tc::mma_commit(&tfull[buf]);
+                last = i;
             }
+            // the last commit covers every MMA issued: they are done before
+            // the TMEM is freed
+            if (last >= 0 && !tc::mbar_wait(&tfull[last & 1], (last >> 1) & 1, kWaitNs))
+                atomicOr(err, 4);
         }
     } else {
         // Two groups of eight warps take alternate tiles: group gr owns TMEM
@@ -265,7 +284,7 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
         float pend = 0.f;
         auto combine = [&](int jj, float own) -> bool {
             const int bar = (gr * 4 + (jj & 3)) * 4 + quad;
-            if (!tc::mbar_wait(&xfull[bar], (jj >> 2) & 1, kWaitLimit)) return false;
+            if (!tc::mbar_wait(&xfull[bar], (jj >> 2) & 1, kWaitNs)) return false;
             const float sum = own + xch[bar * 32 + lane];
             const int64_t gb0 = cb0 + (int64_t)(2 * jj + gr) * TB;
             if (lrow < min((int64_t)TB, cb1 - gb0))
@@ -275,7 +294,7 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
         bool ok = true;
         int jj = 0;
         for (int i = gr; i < n_tiles; i += 2, ++jj) {
-            if (!tc::mbar_wait(&tfull[gr], jj & 1, kWaitLimit)) {
+            if (!tc::mbar_wait(&tfull[gr], jj & 1, kWaitNs)) {
                 ok = false;
                 break;
             }

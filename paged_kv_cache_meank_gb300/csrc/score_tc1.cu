@@ -23,8 +23,10 @@
 // For 128 < rows <= 192 the second row tile holds rows 128..191 twice (lanes
 // 0-63 and 64-127): quadrants 0-1 take its block columns 0-127, quadrants 2-3
 // columns 128-255, and the two halves of a row are merged at the end.  Every
-// mbarrier wait is bounded; on timeout the kernel raises the device error flag
-// (bit 4) and winds down, freeing its TMEM.
+// mbarrier wait is bounded (one second of global time); on timeout the kernel
+// raises the device error flag (bit 4) and winds down: the producer waits for
+// the copies it issued, the MMA warp for its last commit, and then the TMEM is
+// freed.
 #include <cuda.h>
 #include <math.h>
 
@@ -41,7 +43,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = TB;   // one accumulator: one row tile x one index tile
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitNs = 1000000000u;   // 1 s
 constexpr int kQRows = 256;         // query rows padded to two row tiles
 
 template <int D>
@@ -212,18 +214,29 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int i = 0; i < n_tiles; ++i) {
+            // an idle producer (a test of the bounded waits) issues nothing
+            const int n_load = sh.idle_producer ? 0 : n_tiles;
+            int issued = 0;                         // ring entries
+            for (int i = 0; i < n_load; ++i) {
                 const int32_t y =
                     (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
                 bool ok = true;
                 for (int a = 0; a < LY::KA && ok; ++a) {
                     const int2 e = ring(i, a);
-                    if (!tc::mbar_wait(&empty[e.x], e.y ^ 1, kWaitLimit)) { ok = false; break; }
+                    if (!tc::mbar_wait(&empty[e.x], e.y ^ 1, kWaitNs)) { ok = false; break; }
                     tc::mbar_expect_tx(&full[e.x], LY::ATOM_TILE);
                     tc::tma_load_2d(tiles + e.x * LY::ATOM_TILE, &tmap, &full[e.x], a * 64, y);
+                    ++issued;
                 }
                 if (!ok) { atomicOr(err, 4); break; }
             }
+            // every issued copy lands before the CTA ends: wait for the last
+            // use of each ring stage (at once in a run without errors)
+            for (int e = max(0, issued - LY::STAGES); e < issued; ++e)
+                if (!tc::mbar_wait(&full[e % LY::STAGES], (e / LY::STAGES) & 1, kWaitNs)) {
+                    atomicOr(err, 4);
+                    break;
+                }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -231,6 +244,7 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
             const uint32_t tbase = tc::smem_u32(tiles);
             constexpr uint32_t idesc = tc::idesc_bf16_f32(128, TB);
             bool ok = true;
+            int last = -1;
             for (int j = 0; j < n_slots && ok; ++j) {
                 const int i = j / qtiles, t = j - i * qtiles;
                 const int buf = j & 1;
@@ -238,9 +252,9 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
                 if (t == 0)
                     for (int a = 0; a < LY::KA && ok; ++a) {
                         const int2 e = ring(i, a);
-                        ok = tc::mbar_wait(&full[e.x], e.y, kWaitLimit);
+                        ok = tc::mbar_wait(&full[e.x], e.y, kWaitNs);
                     }
-                if (!ok || !tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitLimit)) { ok = false; break; }
+                if (!ok || !tc::mbar_wait(&tempty[buf], bph ^ 1, kWaitNs)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t d = tmem + buf * kAccCols;
 #pragma unroll
@@ -257,7 +271,12 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
                 tc::mma_commit(&tfull[buf]);
                 if (t == qtiles - 1)
                     for (int a = 0; a < LY::KA; ++a) tc::mma_commit(&empty[ring(i, a).x]);
+                last = j;
             }
+            // the last commit covers every MMA issued: they are done before
+            // the TMEM is freed
+            if (last >= 0 && !tc::mbar_wait(&tfull[last & 1], (last >> 1) & 1, kWaitNs))
+                ok = false;
             if (!ok) atomicOr(err, 4);
         }
     } else {
@@ -275,7 +294,7 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
             const int i = j / qtiles, t = j - i * qtiles;
             const int buf = j & 1;
             const uint32_t bph = (j >> 1) & 1;
-            if (!tc::mbar_wait(&tfull[buf], bph, kWaitLimit)) { atomicOr(err, 4); break; }
+            if (!tc::mbar_wait(&tfull[buf], bph, kWaitNs)) { atomicOr(err, 4); break; }
             tc::tc_fence_after();
             const int64_t gb0 = cb0 + (int64_t)i * TB;
             const int nvalid = (int)min((int64_t)TB, cb1 - gb0);
@@ -311,7 +330,7 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
                 slot[(t * 12 + sub - 1) * 64 + 1] = z_run[t];
             }
             tc::mbar_arrive(&xfin[quad]);
-        } else if (!tc::mbar_wait(&xfin[quad], 0, kWaitLimit)) {
+        } else if (!tc::mbar_wait(&xfin[quad], 0, kWaitNs)) {
             atomicOr(err, 4);
         } else {
             float M[2], Z[2];
@@ -342,7 +361,7 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
                     xdup[((quad - 2) * 32 + lane) * 2] = M[1];
                     xdup[((quad - 2) * 32 + lane) * 2 + 1] = Z[1];
                     tc::mbar_arrive(&xdbar[quad - 2]);
-                } else if (!tc::mbar_wait(&xdbar[quad], 0, kWaitLimit)) {
+                } else if (!tc::mbar_wait(&xdbar[quad], 0, kWaitNs)) {
                     atomicOr(err, 4);
                 } else {
                     const float m2 = xdup[(quad * 32 + lane) * 2];

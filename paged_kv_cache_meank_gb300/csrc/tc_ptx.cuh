@@ -38,11 +38,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: returns false (and the caller raises an error flag) if the
-// phase did not complete within `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
+// Low 32 bits of the GPU's global timer, in nanoseconds (wraps every 4.29 s).
+__device__ __forceinline__ uint32_t global_ns_lo() {
+    uint32_t t;
+    asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
+    return t;
+}
+// Bounded wait for the phase of the given parity: false (the caller then
+// raises its error flag) once limit_ns (below 2^31) of global time have passed,
+// or 2^30 polls, whichever comes first.  A wait that ends within its first 64
+// polls never reads the timer.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit_ns) {
+    uint32_t t0 = 0;
+    for (uint32_t n = 0; n < (1u << 30); ++n) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 63) {
+            const uint32_t t = global_ns_lo();
+            if (n == 63)
+                t0 = t;
+            else if (t - t0 > limit_ns)
+                return false;
+        }
+    }
     return false;
 }
 

@@ -140,6 +140,49 @@ def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
     check_selection(sel.cpu().numpy(), R, S, W, wl.view_blocks, "candidates only")
 
 
+@pytest.mark.parametrize("loc", ["device", "host-tiled"])
+@pytest.mark.parametrize("nth", [1, 2], ids=["pass1", "pass2"])
+def test_bounded_wait_runs_out_and_context_recovers(kvm, nth, loc):
+    """A tensor-core pass whose TMA producer stays idle (a barrier that nothing
+    completes): its bounded waits run out after about a second, the kernel
+    winds down and frees its TMEM, kvm_sync reports KVM_ERR_TIMEOUT, and the
+    next call on the same context matches the oracle."""
+    import time
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    ws = workload.make_index_direct(wl, seed=6)
+    kw = {}
+    index = ws.index.to("cuda")
+    if loc == "host-tiled":
+        kw["index_location"] = kvm.KVM_HOST_PINNED
+        index = ws.index.pin_memory()
+    cfg = kvm.config_for(wl, **kw)
+    if loc == "host-tiled":
+        cfg.tile_blocks = 128
+    ctx = kvm.Context(cfg)
+    N = wl.n_blocks
+    q = ws.q.cuda()
+    scores = torch.empty(N, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    # launches of the host-tiled path: pass 1 over the 3 tiles, then pass 2
+    ctx.debug_inject(3, nth if loc == "device" else 1 + 3 * (nth - 1))
+    t0 = time.monotonic()
+    ctx.score_select(q, wl.n_queries, index, N, scores, sel)
+    with pytest.raises(kvm.KvmError) as ei:
+        ctx.sync()
+    assert ei.value.name == "KVM_ERR_TIMEOUT"
+    assert time.monotonic() - t0 < 30.0
+    s = sel.cpu().numpy()
+    assert np.all((s >= 0) & (s < N))
+    # the same context, the next call: parity
+    ctx.score_select(q, wl.n_queries, index, N, scores, sel)
+    ctx.sync()
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q, "bf16"), "bf16"),
+                            ora.as_f64(to_np(ws.index, "bf16"), "bf16"), N)
+    assert_scores_close(scores.cpu().numpy(), R, "after a timed-out pass")
+    check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+
+
 @pytest.mark.parametrize("n_queries", [21, 32, 40, 42], ids=lambda n: f"rows{n * 6}")
 def test_score_select_query_row_tilings(kvm, n_queries):
     """Query rows per KV head across the tensor-core tilings: one M = 128 tile
