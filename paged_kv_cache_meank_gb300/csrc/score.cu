@@ -9,7 +9,7 @@
 //   pass 1   per (l, g, chunk): running max and rescaled partition sum per row
 //   combine  per (l, g, row): fold the chunks in chunk order -> M, 1/Z
 //   pass 2   per (l, g, chunk): for each block, sum over rows of 2^(t - M)/Z
-//   reduce   per block: sum over (l, g) in order, times 1/(L*H)
+//   reduce   per block: sum over (l, g) in a fixed order, times 1/(L*H)
 //
 // This file holds the CUDA-core ("SIMT") variant: one thread per query row
 // with the row in shared memory, eight Mean-K vectors per step broadcast from
@@ -264,15 +264,38 @@ cudaError_t launch_score_combine(const ScoreShape &sh, int n_chunks_total,
 }
 
 // R_b = (1 / (L H)) * sum over (l, g) of the pass-2 partials, for the scored
-// blocks [c0, c1); blocks outside the candidate set get 0.
-__global__ void score_reduce_kernel(int LG, float inv_lh, int64_t n_blocks, int64_t c0,
-                                    int64_t c1, const float *__restrict__ partial,
-                                    int64_t stride, float *__restrict__ out) {
-    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < n_blocks;
-         b += (int64_t)gridDim.x * blockDim.x) {
+// blocks [c0, c1); blocks outside the candidate set get 0.  A CTA takes 32
+// blocks, one per lane.  Each of its 16 warps sums a contiguous run of the
+// (l, g) pairs into four interleaved accumulators, and the runs are added in
+// warp order, so the order of the additions is fixed.
+constexpr int kRedWarps = 16;
+
+__global__ void __launch_bounds__(kRedWarps * 32)
+score_reduce_kernel(int LG, float inv_lh, int64_t n_blocks, int64_t c0, int64_t c1,
+                    const float *__restrict__ partial, int64_t stride, float *__restrict__ out) {
+    __shared__ float part[kRedWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b = (int64_t)blockIdx.x * 32 + lane;
+    const bool scored = b < n_blocks && b >= c0 && b < c1;
+    const int lg0 = (int)((int64_t)LG * warp / kRedWarps);
+    const int lg1 = (int)((int64_t)LG * (warp + 1) / kRedWarps);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (scored) {
+        const float *p = partial + (size_t)lg0 * stride + b;
+        int lg = lg0;
+        for (; lg + 4 <= lg1; lg += 4, p += 4 * stride) {
+            a0 += p[0];
+            a1 += p[stride];
+            a2 += p[2 * stride];
+            a3 += p[3 * stride];
+        }
+        for (; lg < lg1; ++lg, p += stride) a0 += p[0];
+    }
+    part[warp][lane] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (warp == 0 && b < n_blocks) {
         float s = 0.f;
-        if (b >= c0 && b < c1)
-            for (int lg = 0; lg < LG; ++lg) s += partial[(size_t)lg * stride + b];
+        for (int w = 0; w < kRedWarps; ++w) s += part[w][lane];
         out[b] = s * inv_lh;
     }
 }
@@ -280,12 +303,11 @@ __global__ void score_reduce_kernel(int LG, float inv_lh, int64_t n_blocks, int6
 cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t c0, int64_t c1,
                                 const ScoreScratch &scr, int64_t partial_stride,
                                 float *scores_out, cudaStream_t s) {
-    int64_t blocks = (n_blocks + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (n_blocks <= 0) return cudaSuccess;
+    const int64_t blocks = (n_blocks + 31) / 32;
     const float inv_lh = (float)(1.0 / ((double)sh.L * sh.H));
-    score_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(sh.L * sh.G, inv_lh, n_blocks, c0, c1,
-                                                         scr.partial, partial_stride,
-                                                         scores_out);
+    score_reduce_kernel<<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(
+        sh.L * sh.G, inv_lh, n_blocks, c0, c1, scr.partial, partial_stride, scores_out);
     return cudaGetLastError();
 }
 
