@@ -138,7 +138,6 @@ class Step:
     """The full step on a device-resident workspace: Mean-K build, scoring and
     selection, view assembly."""
     parts = ["build", "score_select", "assemble"]
-    launches_per_step = 1 + 5 + 1
     zero_copy_inputs = True
 
     def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
@@ -204,7 +203,6 @@ class ScoreStep:
     """Scoring + selection only, over a Mean-K index drawn directly in HBM (the
     10M-token index-scaling workload)."""
     parts = ["score_select"]
-    launches_per_step = 5
 
     def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
@@ -293,7 +291,6 @@ class HostStep:
     re-RoPE.  Every timed step starts from an empty page pool, so all selected
     blocks are misses."""
     parts = ["step"]
-    launches_per_step = 0   # counted from the step statistics
 
     def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
         import paged_kv_cache_meank_gb300 as kvm
@@ -318,8 +315,6 @@ class HostStep:
                       pool_v=self.pool_v, pool_raw_k=self.pool_raw, page_table=self.page_table,
                       scores=self.scores, sel_ids=self.sel)
         self.stats = []
-        nt = (wl.n_blocks + wl.tile_blocks - 1) // wl.tile_blocks
-        self.score_launches = (2 * nt + 3) if wl.index_loc == "host" else 5
 
     def inputs(self):
         return {"q": self.q}
@@ -337,9 +332,6 @@ class HostStep:
         if ev:
             ev[1].record(s)
         self.stats.append(st)
-        b = self.ctx.cfg.h2d_batch_blocks
-        self.launches_per_step = self.score_launches + (st["misses"] + b - 1) // b + \
-            (1 if st["reroped"] > st["misses"] else 0)
 
     def link_bytes(self):
         """Host-to-device bytes of one step: the index tiles (streamed twice, once
@@ -362,7 +354,6 @@ class ChurnStep:
     runs kvm_step with the raw K / V in pinned host memory; blocks already in the
     page pool are reused, only misses go H2D."""
     parts = ["append_build", "step"]
-    launches_per_step = 0
     per_step_inputs = True
 
     def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
@@ -422,8 +413,6 @@ class ChurnStep:
             ev[2].record(s)
         self.stats.append(dict(st, t=t))
         self.t += 1
-        self.launches_per_step = 1 + 5 + (st["misses"] + 255) // 256 + \
-            (1 if st["reroped"] > st["misses"] else 0)
 
     def link_bytes(self):
         """Host-to-device bytes of one step: the missed blocks' raw K and V."""
@@ -473,6 +462,7 @@ def algorithmic_bytes(wl):
 
 
 def bench_ours(args, wl, world, rank, local, dist):
+    import paged_kv_cache_meank_gb300 as kvm_lib
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -493,10 +483,12 @@ def bench_ours(args, wl, world, rank, local, dist):
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    n_launch0 = kvm_lib.launch_count()
     t0.record(stream)
     for i in range(K):
         step.run(evs[i])
     t1.record(stream)
+    n_launches = kvm_lib.launch_count() - n_launch0   # this library's kernels, timed region
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
@@ -552,7 +544,7 @@ def bench_ours(args, wl, world, rank, local, dist):
                    "l2": "inputs larger than L2, no flush"},
         "components": comps,
         "roofline": roof,
-        "gpu_launches": step.launches_per_step * K,
+        "gpu_launches": n_launches,
         "clocks": clk,
     }
     if not args.no_e2e:

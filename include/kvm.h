@@ -353,6 +353,12 @@ const char *kvm_status_string(kvm_status s);
 /* Detail of the last error raised on the calling thread ("" if none). */
 const char *kvm_last_error(void);
 
+/* Kernels this library has launched in the process so far, over every
+ * context and entry point (a running total, for benchmarks and tests: the
+ * difference across a region is the number of kernels it launched).  Copies
+ * and memsets are not kernels and are not counted. */
+int64_t kvm_launch_count(void);
+
 /* Fault injection for tests.  what = 1 / 2: make the n-th (1-based) next host
  * copy submission / kernel launch of kvm_step fail with KVM_ERR_INJECTED.
  * what = 3: the n-th next tensor-core scoring pass (kvm_score_select or

@@ -24,8 +24,8 @@ from ._abi import (KVM_BF16, KVM_DEVICE, KVM_E4M3, KVM_F32, KVM_HOST_PINNED, Kvm
                    KvmConfig, KvmError, KvmStepStats, KvmTierStats, check, load)
 from .configs import BLOCK_TOKENS, Workload
 
-__all__ = ["Context", "HostTier", "KvmError", "config_for", "load", "KVM_F32", "KVM_BF16",
-           "KVM_E4M3", "KVM_DEVICE", "KVM_HOST_PINNED"]
+__all__ = ["Context", "HostTier", "KvmError", "config_for", "launch_count", "load", "KVM_F32",
+           "KVM_BF16", "KVM_E4M3", "KVM_DEVICE", "KVM_HOST_PINNED"]
 
 _DT = {"f32": KVM_F32, "bf16": KVM_BF16, "e4m3": KVM_E4M3}
 # e4m3 elements travel as their bit patterns in uint8 tensors
@@ -91,6 +91,12 @@ def score_select_static(cfg: KvmConfig, q, n_queries: int, index, n_blocks: int,
                                       ctypes.byref(n_sel), _stream(stream)),
           "kvm_score_select_static")
     return n_sel.value
+
+
+def launch_count() -> int:
+    """kvm_launch_count: kernels the library has launched in this process so
+    far (the difference across a region counts the kernels it launched)."""
+    return int(load().kvm_launch_count())
 
 
 class HostTier:

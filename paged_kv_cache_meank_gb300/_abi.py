@@ -98,6 +98,7 @@ SIGNATURES = {
     "kvm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvm_last_error": (ctypes.c_char_p, []),
     "kvm_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]),
+    "kvm_launch_count": (ctypes.c_int64, []),
 }
 
 _lib = None

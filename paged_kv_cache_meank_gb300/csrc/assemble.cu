@@ -173,6 +173,7 @@ static cudaError_t ids_t(const int32_t *sel_ids, const int32_t *page_ids, int n_
     assemble_ids_kernel<T, D><<<grid, SlotWork<T, D>::NT, 0, s>>>(
         sel_ids, page_ids, max_blocks, static_cast<const T *>(rk), static_cast<const T *>(v),
         static_cast<T *>(kp), static_cast<T *>(vp), LG, lpc, table, err);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -183,6 +184,7 @@ static cudaError_t desc_t(const SlotDesc *desc, int n_desc, int LG, const float2
     dim3 grid((unsigned)n_desc, (unsigned)((LG + lpc - 1) / lpc));
     assemble_desc_kernel<T, D><<<grid, SlotWork<T, D>::NT, 0, s>>>(desc, LG, lpc, table,
                                                                      max_pos, err);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@
 // with CUDA events, Figure 3) and §5 (block record: chronological id, tier,
 // baked position).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -50,7 +51,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t elt_bytes(int dt) { return dt == KVM_E4M3 ? 1 : dt == KVM_BF16 ? 2 : 4; }
 
 struct Layout {
-    size_t table, part_m, part_z, row_m, row_invz, partial, stage0, stage1, desc, err, total;
+    size_t table, part_m, part_z, row_m, row_invz, partial, stage0, stage1, desc, sel, err, total;
     size_t stage_bytes;
     int rows_max, chunk_cap;
 };
@@ -119,6 +120,7 @@ Layout layout_of(const kvm_config *c) {
     lo.stage0 = take(lo.stage_bytes);
     lo.stage1 = take(lo.stage_bytes);
     lo.desc = take((size_t)(c->pool_pages + c->view_blocks) * sizeof(kvm::SlotDesc));
+    lo.sel = take(kvm::select_scratch_bytes());
     lo.err = take(256);
     lo.total = off;
     return lo;
@@ -128,6 +130,11 @@ Layout layout_of(const kvm_config *c) {
 
 void kvm::set_last_error(const std::string &msg) { g_last_error = msg; }
 
+namespace {
+std::atomic<int64_t> g_launches{0};
+}
+void kvm::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 struct kvm_ctx {
     kvm_config cfg{};
     Layout lo{};
@@ -136,6 +143,7 @@ struct kvm_ctx {
     kvm::ScoreScratch scr{};
     void *stage[2] = {nullptr, nullptr};
     kvm::SlotDesc *desc_dev = nullptr;
+    int *sel_scratch = nullptr;        // selection histograms and segment counts
     int *err_dev = nullptr;
     cudaStream_t copy_stream = nullptr;
     cudaEvent_t ev_ready[2] = {nullptr, nullptr};
@@ -268,6 +276,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->stage[0] = c->ws + lo.stage0;
     c->stage[1] = c->ws + lo.stage1;
     c->desc_dev = reinterpret_cast<kvm::SlotDesc *>(c->ws + lo.desc);
+    c->sel_scratch = reinterpret_cast<int *>(c->ws + lo.sel);
     c->err_dev = reinterpret_cast<int *>(c->ws + lo.err);
     c->scr.err = c->err_dev;
     c->block_of_page.assign(cfg->pool_pages, -1);
@@ -478,7 +487,7 @@ kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const 
     if (st != KVM_OK) return st;
     const cudaError_t e = kvm::launch_select(scores_out, n_blocks, c->cfg.sink_blocks,
                                              c->cfg.recent_blocks, c->cfg.view_blocks,
-                                             sel_ids_out, s);
+                                             sel_ids_out, c->sel_scratch, s);
     if (e != cudaSuccess) return cuda_fail(e, "select launch");
     if (n_sel_out) *n_sel_out = (int32_t)std::min<int64_t>(n_blocks, c->cfg.view_blocks);
     return KVM_OK;
@@ -834,6 +843,8 @@ const char *kvm_status_string(kvm_status s) {
 }
 
 const char *kvm_last_error(void) { return g_last_error.c_str(); }
+
+int64_t kvm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 kvm_status kvm_debug_inject(kvm_ctx *c, int32_t what, int64_t nth) {
     if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");

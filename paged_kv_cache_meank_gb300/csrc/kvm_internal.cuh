@@ -13,6 +13,9 @@ namespace kvm {
 // Sets the message kvm_last_error() returns on the calling thread.
 void set_last_error(const std::string &msg);
 
+// Counts one kernel launch of this library (read by kvm_launch_count).
+void note_launch();
+
 constexpr int kBlockTokens = 32;
 constexpr int kMaxHalfDim = 64;       // head_dim <= 128
 constexpr int kMaxRows = 256;         // query rows per KV head (M_q * H/G)
@@ -105,7 +108,14 @@ cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t 
 int score_chunks(const ScoreShape &sh, int64_t n_blocks, int max_chunks);
 
 // ---- select.cu
+// Device scratch of one selection (histograms and segment counts); fixed size.
+size_t select_scratch_bytes();
+// sel_ids <- the selection over scores [0, n_blocks); `scratch` is device
+// memory of select_scratch_bytes(), used by long histories only.
 cudaError_t launch_select(const float *scores, int64_t n_blocks, int sink, int recent,
-                          int view_blocks, int32_t *sel_ids, cudaStream_t s);
+                          int view_blocks, int32_t *sel_ids, int *scratch, cudaStream_t s);
+
+// Multiprocessors of the current device (152 where it cannot be read).
+int sm_count();
 
 }  // namespace kvm

@@ -140,6 +140,7 @@ static cudaError_t launch_meank_t(const void *k_pages, void *raw_out, void *inde
     meank_kernel<T, TI, D><<<grid, kMeanKWarps * 32, 0, s>>>(
         static_cast<const T *>(k_pages), static_cast<T *>(raw_out), static_cast<TI *>(index),
         index_cap, first_block, LG, lg_per_cta, table);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -138,7 +138,7 @@ __global__ void score_simt_kernel(const TQ *__restrict__ q, const TI *__restrict
     }
 }
 
-static int sm_count() {
+int sm_count() {
     static int n = 0;
     if (n <= 0) {
         int dev = 0, v = 0;
@@ -193,6 +193,7 @@ static cudaError_t simt_t(const ScoreShape &sh, const void *q, const void *index
     kern<<<grid, threads, smem, s>>>(static_cast<const TQ *>(q), static_cast<const TI *>(index),
                                      sh, b_index0, b_begin, b_end, chunk0, chunk_blocks, scr,
                                      partial_stride, scale_log2);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -260,6 +261,7 @@ cudaError_t launch_score_combine(const ScoreShape &sh, int n_chunks_total,
                                  const ScoreScratch &scr, cudaStream_t s) {
     const int n = sh.L * sh.G * sh.rows;
     score_combine_kernel<<<(n + 255) / 256, 256, 0, s>>>(sh, n_chunks_total, scr);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -308,6 +310,7 @@ cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t 
     const float inv_lh = (float)(1.0 / ((double)sh.L * sh.H));
     score_reduce_kernel<<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(
         sh.L * sh.G, inv_lh, n_blocks, c0, c1, scr.partial, partial_stride, scores_out);
+    note_launch();
     return cudaGetLastError();
 }
 

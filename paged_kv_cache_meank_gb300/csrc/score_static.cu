@@ -112,7 +112,8 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     const size_t part = up256(LG * nch * sh.rows * sizeof(float));
     const size_t rowb = up256(LG * sh.rows * sizeof(float));
     const size_t partial = up256(LG * (size_t)n_blocks * sizeof(float));
-    const size_t need = 256 + 2 * part + 2 * rowb + partial;
+    const size_t selb = up256(kvm::select_scratch_bytes());
+    const size_t need = 256 + 2 * part + 2 * rowb + partial + selb;
     if (need > SCRATCH_BYTES) {
         char msg[200];
         snprintf(msg, sizeof msg,
@@ -132,6 +133,7 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     scr.row_m = reinterpret_cast<float *>(b + 2 * part);
     scr.row_invz = reinterpret_cast<float *>(b + 2 * part + rowb);
     scr.partial = reinterpret_cast<float *>(b + 2 * part + 2 * rowb);
+    int *sel_scratch = reinterpret_cast<int *>(b + 2 * part + 2 * rowb + partial);
     scr.err = static_cast<int *>(base);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -150,7 +152,7 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
         (e = kvm::launch_score_reduce(sh, n_blocks, c0, c1, scr, n_blocks, scores_out, s)) !=
             cudaSuccess ||
         (e = kvm::launch_select(scores_out, n_blocks, cfg->sink_blocks, cfg->recent_blocks,
-                                cfg->view_blocks, sel_ids_out, s)) != cudaSuccess) {
+                                cfg->view_blocks, sel_ids_out, sel_scratch, s)) != cudaSuccess) {
         kvm::set_last_error(std::string("launch: ") + cudaGetErrorString(e));
         return KVM_ERR_CUDA;
     }

@@ -421,6 +421,7 @@ static cudaError_t pass2_t(const ScoreShape &sh, const void *q, const void *inde
     kern<<<grid, kThreads, Lay<D>::SMEM, s>>>(map, static_cast<const __nv_bfloat16 *>(q), sh,
                                               b_index0, b_begin, b_end, chunk_blocks, scr,
                                               partial_stride, scale_log2, err);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -402,6 +402,7 @@ static cudaError_t pass1_t(const ScoreShape &sh, const void *q, const void *inde
     kern<<<grid, kThreads, Lay1<D>::SMEM, s>>>(map, static_cast<const __nv_bfloat16 *>(q), sh,
                                                b_index0, b_begin, b_end, chunk0, chunk_blocks, scr,
                                                scale_log2, err);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -69,11 +69,13 @@ def test_create_rejects_small_or_misaligned_workspace(lib):
 
 
 def test_calls_reject_null_context(lib):
+    n0 = lib.kvm_launch_count()
     assert lib.kvm_build_index(None, None, 0, 0, None, None, None) == -1
     assert lib.kvm_score_select(None, None, 1, None, 1, None, None, None, None) == -1
     assert lib.kvm_assemble_view(None, None, None, 0, None, None, None, None, None) == -1
     assert lib.kvm_step(None, None, 1, 1, None, None) == -1
     assert lib.kvm_destroy(None) == 0
+    assert lib.kvm_launch_count() == n0     # rejected on the host: no kernel launched
 
 
 def test_layout_sizes_follow_the_workloads():

@@ -223,6 +223,113 @@ def test_select_ties_and_small_histories(kvm):
         assert torch.allclose(scores, torch.full_like(scores, wl.n_queries / N), rtol=1e-5)
 
 
+@pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
+def test_empty_and_degenerate_inputs(kvm, variant):
+    """Empty calls are no-ops or rejected on the host; an empty candidate set
+    (every block reserved) scores 0 everywhere and selects every block."""
+    wl = MID
+    ctx = _ctx(kvm, wl, score_variant=variant)
+    q = torch.randn(wl.n_layers, wl.n_queries, wl.n_q_heads, wl.head_dim,
+                    device="cuda").to(torch.bfloat16)
+    index = torch.full(ctx.index_shape(), 0.5, dtype=torch.bfloat16, device="cuda")
+    before = index.clone()
+    kp = torch.ones(ctx.block_shape(1), dtype=torch.bfloat16, device="cuda")
+    ctx.build_index(kp, 3, 0, index)                     # zero blocks: nothing written
+    pages = torch.full(ctx.block_shape(2), 7.0, dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ctx.assemble_view(ids, None, 0, kp, None, pages, None)   # empty view: nothing written
+    ctx.sync()
+    assert torch.equal(index, before)
+    assert bool((pages == 7.0).all())
+    scores = torch.empty(wl.n_blocks, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    for nq, nb in ((wl.n_queries, 0), (0, wl.n_blocks)):
+        with pytest.raises(kvm.KvmError) as ei:
+            ctx.score_select(q, nq, index, nb, scores, sel)
+        assert ei.value.name == "KVM_ERR_INVALID_ARG"
+    S, W = wl.sink_blocks, wl.recent_blocks
+    cx = _ctx(kvm, wl, score_variant=variant, candidate_mode=1)
+    for N in (1, S + W - 1, S + W):
+        scores.fill_(3.0)
+        sel.fill_(-1)
+        n_sel = cx.score_select(q, wl.n_queries, index, N, scores, sel)
+        cx.sync()
+        assert n_sel == N
+        assert bool((scores[:N] == 0).all()), N
+        assert np.array_equal(sel[:N].cpu().numpy(), np.arange(N)), N
+    ctx.sync()
+
+
+@pytest.mark.parametrize("pattern", ["random", "uniform", "classes"])
+@pytest.mark.parametrize("N", [16384, 40000, 100003])
+def test_select_long_histories_exact(kvm, N, pattern):
+    """Histories of 16384 blocks and more take the many-CTA select.  Its ids
+    must equal the oracle's selection over the GPU's own scores, bit for bit,
+    with large tie groups that cross segment boundaries: all blocks equal
+    ("uniform"), or three exact score levels with the cut inside a tie group
+    ("classes": every 20th block high, the next one middle)."""
+    wl = MID.with_(n_blocks=N, view_blocks=3000)
+    ctx = _ctx(kvm, wl, max_positions=wl.view_blocks * 32)
+    L, nq, H, d = wl.n_layers, wl.n_queries, wl.n_q_heads, wl.head_dim
+    g = torch.Generator(device="cuda").manual_seed(N)
+    u = torch.randn(d, device="cuda", generator=g)
+    u = u / u.norm()
+    if pattern == "random":
+        q = torch.randn(L, nq, H, d, device="cuda", generator=g).to(torch.bfloat16)
+        index = (torch.randn(ctx.index_shape(), device="cuda", generator=g) * 0.3).to(
+            torch.bfloat16)
+    else:
+        q = (u * 4.0).expand(L, nq, H, d).contiguous().to(torch.bfloat16)
+        index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+        if pattern == "uniform":
+            index[:, :, :N] = (u * 0.5).to(torch.bfloat16)
+        else:
+            b = torch.arange(N, device="cuda")
+            level = torch.where(b % 20 == 0, 1.0, torch.where(b % 20 == 1, 0.5, 0.0))
+            index[:, :, :N] = (level[:, None] * u[None, :]).to(torch.bfloat16)
+    scores = torch.empty(N, device="cuda")
+    sel = torch.full((wl.view_blocks,), -1, dtype=torch.int32, device="cuda")
+    n_sel = ctx.score_select(q, nq, index, N, scores, sel)
+    ctx.sync()
+    assert n_sel == wl.view_blocks
+    s_np = scores.cpu().numpy().astype(np.float64)
+    want = ora.select_blocks(s_np, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+    assert np.array_equal(sel.cpu().numpy(), want), pattern
+    if pattern != "random":
+        levels = np.unique(s_np)
+        assert len(levels) == (1 if pattern == "uniform" else 3), levels
+    if pattern == "random" and N == 40000:
+        R = ora.block_relevance(ora.as_f64(to_np(q.cpu(), "bf16"), "bf16"),
+                                ora.as_f64(to_np(index.cpu(), "bf16"), "bf16"), N)
+        assert_scores_close(s_np, R, "long history")
+
+
+def test_launch_count(kvm):
+    """kvm_launch_count counts this library's kernels: one per Mean-K build and
+    per view assembly; scoring is pass 1, combine, pass 2 and reduce, and the
+    selection one kernel for short histories, six for long ones."""
+    wl = MID
+    for N, n_score in ((wl.n_blocks, 5), (20000, 10)):
+        w = wl.with_(n_blocks=N, view_blocks=100)
+        ctx = _ctx(kvm, w, max_positions=w.view_blocks * 32)
+        q = torch.randn(w.n_layers, w.n_queries, w.n_q_heads, w.head_dim,
+                        device="cuda").to(torch.bfloat16)
+        index = torch.randn(ctx.index_shape(), device="cuda").to(torch.bfloat16)
+        scores = torch.empty(N, device="cuda")
+        sel = torch.empty(w.view_blocks, dtype=torch.int32, device="cuda")
+        n0 = kvm.launch_count()
+        ctx.score_select(q, w.n_queries, index, N, scores, sel)
+        assert kvm.launch_count() - n0 == n_score, N
+        ctx.sync()
+    kp = torch.zeros(ctx.block_shape(2), dtype=torch.bfloat16, device="cuda")
+    n0 = kvm.launch_count()
+    ctx.build_index(kp, 0, 2, index)
+    ids = torch.tensor([0, 1], dtype=torch.int32, device="cuda")   # blocks of kp
+    ctx.assemble_view(ids, None, 2, kp, None, torch.empty_like(kp), None)
+    assert kvm.launch_count() - n0 == 2
+    ctx.sync()
+
+
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
 def test_assemble_view(kvm, wl):
     from paged_kv_cache_meank_gb300 import workload
