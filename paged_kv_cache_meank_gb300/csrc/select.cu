@@ -62,9 +62,13 @@ __device__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
     return base + x - v;
 }
 
+// One CTA, for histories shorter than kSelManyMin blocks: the keys of all N
+// blocks are staged in shared memory once (at most 64 KB), and every pass
+// reads them there.
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
               int32_t *__restrict__ sel) {
+    extern __shared__ uint32_t keys[];     // [N] when N > V
     __shared__ int hist[256];
     __shared__ int warp_sums[32];
     __shared__ uint32_t s_prefix;
@@ -75,6 +79,21 @@ select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
         for (int64_t b = tid; b < N; b += blockDim.x) sel[b] = (int32_t)b;
         return;
     }
+    // all loads of a thread in flight before its first store
+    for (int64_t base = 0; base < N; base += 4 * kSelThreads) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t b = base + tid + j * kSelThreads;
+            v[j] = b < N ? R[b] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t b = base + tid + j * kSelThreads;
+            if (b < N) keys[b] = order_key(v[j]);
+        }
+    }
+    __syncthreads();
     const int64_t c0 = S, c1 = N - W;          // candidate range
     const int k = V - S - W;
     uint32_t prefix = 0, mask = 0;
@@ -83,18 +102,22 @@ select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
         for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
         for (int64_t b = c0 + tid; b < c1; b += blockDim.x) {
-            const uint32_t key = order_key(R[b]);
+            const uint32_t key = keys[b];
             if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
         }
         __syncthreads();
-        if (tid == 0) {
-            int acc = 0, dsel = 0;
-            for (int dgt = 255; dgt >= 0; --dgt) {
-                if (acc + hist[dgt] >= remaining) { dsel = dgt; break; }
-                acc += hist[dgt];
+        // the largest digit whose count, with the counts of all larger digits,
+        // reaches the remaining rank: thread t < 256 holds digit 255 - t, and
+        // a scan gives each the count of the digits above it
+        {
+            const int r = 255 - tid;
+            const int h = tid < 256 ? hist[r] : 0;
+            int total;
+            const int above = block_exclusive_scan(h, warp_sums, &total);
+            if (tid < 256 && above < remaining && (above + h >= remaining || r == 0)) {
+                s_prefix = prefix | ((uint32_t)r << shift);
+                s_remaining = remaining - (above + h >= remaining ? above : above + h);
             }
-            s_prefix = prefix | ((uint32_t)dsel << shift);
-            s_remaining = remaining - acc;
         }
         __syncthreads();
         prefix = s_prefix;
@@ -110,7 +133,7 @@ select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
     const int64_t s0 = min(N, (int64_t)tid * seg), s1 = min(N, s0 + seg);
     int n_eq = 0;
     for (int64_t b = s0; b < s1; ++b)
-        if (b >= c0 && b < c1 && order_key(R[b]) == T) ++n_eq;
+        if (b >= c0 && b < c1 && keys[b] == T) ++n_eq;
     int total;
     int eq_rank = block_exclusive_scan(n_eq, warp_sums, &total);
     int n_take = 0;
@@ -118,7 +141,7 @@ select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
         int r = eq_rank;
         for (int64_t b = s0; b < s1; ++b) {
             if (b < c0 || b >= c1) { ++n_take; continue; }
-            const uint32_t key = order_key(R[b]);
+            const uint32_t key = keys[b];
             if (key > T) ++n_take;
             else if (key == T) { if (r < need_eq) ++n_take; ++r; }
         }
@@ -130,7 +153,7 @@ select_kernel(const float *__restrict__ R, int64_t N, int S, int W, int V,
             bool take;
             if (b < c0 || b >= c1) take = true;
             else {
-                const uint32_t key = order_key(R[b]);
+                const uint32_t key = keys[b];
                 if (key > T) take = true;
                 else if (key == T) { take = r < need_eq; ++r; }
                 else take = false;
@@ -317,8 +340,13 @@ size_t select_scratch_bytes() { return (4 * 256 + 2 * kMaxSegs) * sizeof(int); }
 cudaError_t launch_select(const float *scores, int64_t n_blocks, int sink, int recent,
                           int view_blocks, int32_t *sel_ids, int *scratch, cudaStream_t s) {
     if (n_blocks <= view_blocks || n_blocks < kSelManyMin) {
-        select_kernel<<<1, kSelThreads, 0, s>>>(scores, n_blocks, sink, recent, view_blocks,
-                                                sel_ids);
+        const cudaError_t e = cudaFuncSetAttribute(    // per device: set on every call
+            select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (int)(kSelManyMin * sizeof(uint32_t)));
+        if (e != cudaSuccess) return e;
+        const size_t smem = n_blocks > view_blocks ? (size_t)n_blocks * sizeof(uint32_t) : 0;
+        select_kernel<<<1, kSelThreads, smem, s>>>(scores, n_blocks, sink, recent, view_blocks,
+                                                   sel_ids);
         note_launch();
         return cudaGetLastError();
     }
