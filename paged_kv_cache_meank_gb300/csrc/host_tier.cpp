@@ -79,18 +79,24 @@ kvm_status kvm_tier_step(kvm_tier *t, const int32_t *ids, int32_t n_ids, int64_t
             kvm::set_last_error("tier step: block id out of range");
             return KVM_ERR_INVALID_ARG;
         }
-    {
+    // every allocation comes before the first change of state, and none
+    // throws across the C ABI
+    std::vector<uint8_t> prot;
+    std::vector<std::pair<double, int64_t>> cand;
+    try {
         std::vector<int32_t> sorted(ids, ids + n_ids);
         std::sort(sorted.begin(), sorted.end());
         if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) {
             kvm::set_last_error("tier step: block ids must be distinct");
             return KVM_ERR_INVALID_ARG;
         }
-    }
-    try {
         t->crf.resize(n_blocks, 0.0);
         t->last.resize(n_blocks, -1);
         t->resident.resize(n_blocks, 0);
+        prot.assign((size_t)n_blocks, 0);
+        // at most every block resident after this step's creations and hits
+        cand.reserve((size_t)std::min<int64_t>(n_blocks,
+                                               t->n_resident + (n_blocks - t->n_blocks) + n_ids));
     } catch (...) {
         kvm::set_last_error("out of host memory");
         return KVM_ERR_CAPACITY;
@@ -109,10 +115,7 @@ kvm_status kvm_tier_step(kvm_tier *t, const int32_t *ids, int32_t n_ids, int64_t
     if (need > 0) {
         // candidates: resident and not referenced by the step's selection
         // blocks the step selected are protected; blocks only created are not
-        std::vector<uint8_t> prot((size_t)n_blocks, 0);
         for (int32_t i = 0; i < n_ids; ++i) prot[ids[i]] = 1;
-        std::vector<std::pair<double, int64_t>> cand;
-        cand.reserve((size_t)t->n_resident);
         for (int64_t b = 0; b < n_blocks; ++b)
             if (t->resident[b] && !prot[b]) cand.emplace_back(t->value(b), b);
         const size_t k = (size_t)std::min<int64_t>(need, (int64_t)cand.size());

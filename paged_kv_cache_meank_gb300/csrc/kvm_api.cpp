@@ -263,7 +263,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     if (workspace_bytes < lo.total)
         return fail(KVM_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lo.total);
     auto *c = new (std::nothrow) kvm_ctx();
-    if (!c) return fail(KVM_ERR_INVALID_ARG, "out of host memory");
+    if (!c) return fail(KVM_ERR_CAPACITY, "out of host memory");
     c->cfg = *cfg;
     c->lo = lo;
     c->ws = static_cast<char *>(workspace);
@@ -279,11 +279,18 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->sel_scratch = reinterpret_cast<int *>(c->ws + lo.sel);
     c->err_dev = reinterpret_cast<int *>(c->ws + lo.err);
     c->scr.err = c->err_dev;
-    c->block_of_page.assign(cfg->pool_pages, -1);
-    c->baked_pos.assign(cfg->pool_pages, -1);
-    c->delta_count.assign(cfg->pool_pages, 0);
-    c->page_of_block.assign((size_t)cfg->max_blocks, -1);
-    c->mark.assign((size_t)cfg->max_blocks, 0);
+    try {   // no exception crosses the C ABI
+        c->block_of_page.assign(cfg->pool_pages, -1);
+        c->baked_pos.assign(cfg->pool_pages, -1);
+        c->delta_count.assign(cfg->pool_pages, 0);
+        c->page_of_block.assign((size_t)cfg->max_blocks, -1);
+        c->mark.assign((size_t)cfg->max_blocks, 0);
+        c->ev_batch.assign((cfg->pool_pages + cfg->h2d_batch_blocks - 1) / cfg->h2d_batch_blocks + 1,
+                           nullptr);
+    } catch (...) {
+        delete c;
+        return fail(KVM_ERR_CAPACITY, "out of host memory");
+    }
 
     auto cleanup = [&](kvm_status s) { kvm_destroy(c); return s; };
     cudaError_t e = cudaGetDevice(&c->device);
@@ -298,9 +305,6 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     if ((e = cudaEventCreateWithFlags(&c->ev_main, cudaEventDisableTiming)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&c->ev_stage, cudaEventDisableTiming)) != cudaSuccess)
         return cleanup(cuda_fail(e, "cudaEventCreate"));
-    const int n_batches =
-        (cfg->pool_pages + cfg->h2d_batch_blocks - 1) / cfg->h2d_batch_blocks + 1;
-    c->ev_batch.assign(n_batches, nullptr);
     for (auto &ev : c->ev_batch)
         if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
             return cleanup(cuda_fail(e, "cudaEventCreate"));
@@ -582,10 +586,8 @@ kvm_status kvm_reset_pool(kvm_ctx *c) {
     return KVM_OK;
 }
 
-kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
-                    kvm_step_stats *stats, kvm_stream stream) {
-    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
-    if (!c->bound) return fail(KVM_ERR_NOT_BOUND, "kvm_step before kvm_bind");
+static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
+                            kvm_step_stats *stats, kvm_stream stream) {
     const kvm_config &cfg = c->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int32_t n_sel = 0;
@@ -604,9 +606,11 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
     const int P = cfg.pool_pages;
     std::vector<int32_t> page_of_slot(n_sel, -1);
     std::vector<uint8_t> is_hit(n_sel, 0);
+    for (int j = 0; j < n_sel; ++j)
+        if (sel[j] < 0 || sel[j] >= cfg.max_blocks)
+            return fail(KVM_ERR_DEVICE, "selected id %d out of range", sel[j]);
     for (int j = 0; j < n_sel; ++j) {
         const int32_t b = sel[j];
-        if (b < 0 || b >= cfg.max_blocks) return fail(KVM_ERR_DEVICE, "selected id %d out of range", b);
         c->mark[b] = 1;
         if (c->page_of_block[b] >= 0) {
             page_of_slot[j] = c->page_of_block[b];
@@ -793,8 +797,10 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
     c->delta_count.swap(new_count);
 
     kvm_tier_stats ts{};
-    if (c->tier && kvm_tier_step(c->tier, sel.data(), n_sel, n_blocks, nullptr, &ts) != KVM_OK)
-        return KVM_ERR_INVALID_ARG;
+    if (c->tier) {
+        const kvm_status tst = kvm_tier_step(c->tier, sel.data(), n_sel, n_blocks, nullptr, &ts);
+        if (tst != KVM_OK) return tst;
+    }
     if (stats) {
         stats->host_hits = ts.hits;
         stats->host_misses = ts.misses;
@@ -811,6 +817,20 @@ kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_bloc
         stats->h2d_bytes = pull ? 2 * (int64_t)miss_slots.size() * (int64_t)blk : h2d_bytes;
     }
     return KVM_OK;
+}
+
+kvm_status kvm_step(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
+                    kvm_step_stats *stats, kvm_stream stream) {
+    if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+    if (!c->bound) return fail(KVM_ERR_NOT_BOUND, "kvm_step before kvm_bind");
+    try {   // no exception crosses the C ABI
+        return step_body(c, q, n_queries, n_blocks, stats, stream);
+    } catch (...) {
+        // out of host memory part-way: forget the pool, as a failed step does
+        std::fill(c->mark.begin(), c->mark.end(), 0);
+        reset_pool(c);
+        return fail(KVM_ERR_CAPACITY, "out of host memory");
+    }
 }
 
 kvm_status kvm_sync(kvm_ctx *c, kvm_stream stream) {
