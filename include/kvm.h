@@ -335,8 +335,10 @@ kvm_status kvm_tier_destroy(kvm_tier *tier);
  *          call before any stream capture.
  * Sharing: every call on a device uses the same array.  Calls that overlap on
  *          the GPU (unordered streams or threads) race on it; order them.
- *          Leftover contents of earlier calls are never read, so nothing has
- *          to be cleared between calls.
+ *          The array keeps the last call's contents; a call never reads
+ *          them: the part that must start at zero (the histograms of the
+ *          selection over 16384 or more blocks) is cleared on the call's
+ *          stream first, and the rest is overwritten before it is read.
  * The array stays allocated on every GPU that loaded the library until the
  * process exits.
  */

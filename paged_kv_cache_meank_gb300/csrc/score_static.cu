@@ -13,9 +13,11 @@
 // The array is SCRATCH_BYTES (32 MiB) per device.  Every GPU on which the
 // library is loaded holds it until the process exits.  It is shared by every
 // call: two calls that overlap on the GPU (different streams, or different
-// host threads without ordering) race on it and produce garbage.  Every byte a
-// call reads from it is written earlier in the same call, so leftover contents
-// of a previous call are harmless and nothing needs clearing.
+// host threads without ordering) race on it and produce garbage.  The array
+// keeps whatever the last call left in it.  Every byte a call reads from it is
+// written earlier in the same call: the one part that must start at zero, the
+// histograms of the selection over 16384 blocks or more, is cleared on the
+// call's stream before its first use, and the rest is fully overwritten.
 #include <cstdio>
 #include <mutex>
 #include <string>

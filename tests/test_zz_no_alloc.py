@@ -7,8 +7,10 @@ that cannot pay for cudaMalloc / cudaFree (which may synchronise the device).
 The entry point keeps its scratch in a fixed array inside the library, so it
 needs no context and no workspace.  Here its output is checked against the
 workspace-based kvm_score_select, within the parity tolerance the other tests
-use, on two calls in a row with different shapes (so anything left in the
-shared scratch by the first call would show up in the second).
+use, on calls in a row with different shapes (so anything left in the
+shared scratch by one call would show up in the next).  The third call has
+enough blocks for the many-CTA selection, whose histograms live in the shared
+scratch and must start at zero on every call.
 """
 import ctypes
 
@@ -55,9 +57,12 @@ def _compare(kvm, wl, seed):
     ctx.close()
 
 
-def test_static_matches_workspace_entry_point_twice(kvm):
+def test_static_matches_workspace_entry_point_on_calls_in_a_row(kvm):
     _compare(kvm, MID, seed=41)                       # call 1: small, 4 layers x 2 heads
     _compare(kvm, configs.W256K, seed=42)             # call 2: 64 x 8 heads, 8192 blocks
+    many = MID.with_(name="mid-bf16-20000", n_blocks=20000, view_blocks=600)
+    _compare(kvm, many, seed=43)                      # call 3: many-CTA selection
+    _compare(kvm, many, seed=44)                      # call 4: its histograms cleared again
 
 
 def test_static_rejects_sizes_beyond_its_scratch(kvm):
