@@ -292,13 +292,15 @@ class HostStep:
     blocks are misses."""
     parts = ["step"]
 
-    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0, index_spill=1):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        self.index_spill = index_spill if wl.index_loc == "host" else 0
         cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
                              index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
                              else kvm.KVM_DEVICE, h2d_batch_blocks=256,
-                             score_variant=score_variant, h2d_mode=h2d_mode)
+                             score_variant=score_variant, h2d_mode=h2d_mode,
+                             index_spill=self.index_spill)
         self.ctx = kvm.Context(cfg, device=device, stream=stream)
         (self.raw_h, self.v_h, self.index, self.planted, u, _, _) = build_host_workspace(
             kvm, wl, seed, device, stream, self.ctx, wl.n_blocks, wl.index_loc == "host")
@@ -334,13 +336,14 @@ class HostStep:
         self.stats.append(st)
 
     def link_bytes(self):
-        """Host-to-device bytes of one step: the index tiles (streamed twice, once
-        per scoring pass, when the index is in host memory) plus the missed
-        blocks' raw K and V."""
+        """Host-to-device bytes of one step: the index tiles (when the index is in
+        host memory: streamed once with index_spill, else once per scoring pass)
+        plus the missed blocks' raw K and V."""
         wl = self.wl
         idx = 0
         if wl.index_loc == "host":
-            idx = 2 * wl.n_layers * wl.n_kv_heads * wl.n_blocks * wl.head_dim * 2
+            idx = (1 if self.index_spill else 2) * wl.n_layers * wl.n_kv_heads * wl.n_blocks * \
+                wl.head_dim * 2
         return idx + float(np.mean([s["h2d_bytes"] for s in self.stats[-8:]]))
 
     def cpu_sample(self, layers):
@@ -467,8 +470,9 @@ def bench_ours(args, wl, world, rank, local, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     kind = STEP_KIND.get(wl.name.split("@")[0], Step)
+    extra = {"index_spill": args.index_spill} if kind is HostStep else {}
     step = kind(wl, args.seed + rank, dev, stream, score_variant=args.score_variant,
-                h2d_mode=args.h2d_mode)
+                h2d_mode=args.h2d_mode, **extra)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize(dev)
@@ -541,7 +545,8 @@ def bench_ours(args, wl, world, rank, local, dist):
                    "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
                    "recent_blocks": wl.recent_blocks, "kv_dtype": wl.kv_dtype,
                    "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2, no flush"},
+                   "l2": "inputs larger than L2, no flush",
+                   **({"index_spill": step.index_spill} if hasattr(step, "index_spill") else {})},
         "components": comps,
         "roofline": roof,
         "gpu_launches": n_launches,
@@ -766,6 +771,9 @@ def main():
                     help="0: tensor-core scoring where supported, 1: CUDA cores")
     ap.add_argument("--h2d-mode", type=int, default=1,
                     help="host-resident repository: 0 copy engine, 1 GPU reads the host memory")
+    ap.add_argument("--index-spill", type=int, default=1, choices=[0, 1],
+                    help="host-resident index: 1 keeps pass 1's staged tiles in HBM for pass 2 "
+                         "(one read over the host link per step), 0 streams them per pass")
     ap.add_argument("--blocks", type=int, default=0,
                     help="override the history length (small cases for profiling)")
     args = ap.parse_args()

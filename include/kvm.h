@@ -116,12 +116,20 @@ typedef struct {
                                 blocks, >= view_blocks, fed with every step's
                                 selection, and reports its hits / misses */
     double  host_tier_lambda;/* the policy's decay, in [0, 1]              */
+    int32_t index_spill;     /* host-resident index ([KVMem] §5 tiled retrieval):
+                                0 = both scoring passes stream the index tiles over the
+                                    host link, through two tile-sized device buffers;
+                                1 = pass 1 keeps every staged tile in device memory
+                                    (the workspace then holds a copy of the whole
+                                    index) and pass 2 reads it there, so each step
+                                    moves the index over the link once. */
 } kvm_config;
 
 typedef struct kvm_ctx kvm_ctx;
 
 /* Device workspace bytes a context needs for `cfg` (RoPE table, scoring
- * scratch, index staging tiles, step descriptors).  0 if cfg is invalid. */
+ * scratch, index staging tiles -- two, or one per index tile with
+ * index_spill -- and step descriptors).  0 if cfg is invalid. */
 size_t kvm_workspace_bytes(const kvm_config *cfg);
 
 /* Create a context.  `workspace` is caller-owned device memory of at least

@@ -94,6 +94,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
         return bad("host_tier_blocks must be 0 or >= view_blocks");
     if (c->host_tier_blocks > 0 && !(c->host_tier_lambda >= 0.0 && c->host_tier_lambda <= 1.0))
         return bad("host_tier_lambda must be in [0, 1]");
+    if (c->index_spill != 0 && c->index_spill != 1) return bad("index_spill must be 0 or 1");
     return true;
 }
 
@@ -117,8 +118,15 @@ Layout layout_of(const kvm_config *c) {
     lo.stage_bytes = 0;
     if (c->index_location == KVM_HOST_PINNED)
         lo.stage_bytes = LG * (size_t)c->tile_blocks * c->head_dim * elt_bytes(c->index_dtype);
-    lo.stage0 = take(lo.stage_bytes);
-    lo.stage1 = take(lo.stage_bytes);
+    if (c->index_location == KVM_HOST_PINNED && c->index_spill) {
+        // one staging tile per index tile: pass 2 reads what pass 1 staged
+        const int64_t tiles = (c->max_blocks + c->tile_blocks - 1) / c->tile_blocks;
+        lo.stage0 = take(lo.stage_bytes * (size_t)tiles);
+        lo.stage1 = lo.stage0;
+    } else {
+        lo.stage0 = take(lo.stage_bytes);
+        lo.stage1 = take(lo.stage_bytes);
+    }
     lo.desc = take((size_t)(c->pool_pages + c->view_blocks) * sizeof(kvm::SlotDesc));
     lo.sel = take(kvm::select_scratch_bytes());
     lo.err = take(256);
@@ -399,7 +407,9 @@ static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void
 // Index in pinned host memory: tiles of tile_blocks staged through two device
 // buffers on the copy stream; the softmax stays global because pass 1 only
 // records per-chunk (max, sum) and the combine folds every tile's chunks
-// before pass 2 re-streams the tiles (KVMem §5, tiled retrieval).
+// before pass 2 re-streams the tiles (KVMem §5, tiled retrieval).  With
+// index_spill every tile has its own staging buffer: pass 1 copies each tile
+// once and pass 2 reads the staged tiles without copying again.
 static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q,
                                    const void *index, int64_t N, int64_t c0, int64_t c1,
                                    float *scores, cudaStream_t s) {
@@ -415,6 +425,7 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
     KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0));
     kvm::ScoreShape tsh = sh;
     tsh.index_cap = tile;
+    const bool spill = c->cfg.index_spill != 0;
     for (int pass = 1; pass <= 2 && c1 > c0; ++pass) {
         for (int64_t t = 0; t < T; ++t) {
             const int buf = (int)(t & 1);
@@ -423,25 +434,32 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
             // pass 1 so that its chunks hold (-inf, 0) for the combine
             const int64_t lo = std::min(std::max(b0, c0), b0 + nb);
             const int64_t hi = std::max(std::min(b0 + nb, c1), lo);
-            KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
-            KVM_CUDA(cudaMemcpy2DAsync(c->stage[buf], tile * row,
-                                       static_cast<const char *>(index) + b0 * row,
-                                       (size_t)c->cfg.max_blocks * row, nb * row, LG,
-                                       cudaMemcpyHostToDevice, c->copy_stream));
-            KVM_CUDA(cudaEventRecord(c->ev_ready[buf], c->copy_stream));
-            KVM_CUDA(cudaStreamWaitEvent(s, c->ev_ready[buf], 0));
+            void *tile_buf = spill ? static_cast<char *>(c->stage[0]) + (size_t)t * c->lo.stage_bytes
+                                   : c->stage[buf];
+            if (!spill || pass == 1) {
+                // a spilled tile's buffer is not reused within the call; the
+                // copy stream joined the caller's stream at the start, after
+                // the previous call's pass 2
+                if (!spill) KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
+                KVM_CUDA(cudaMemcpy2DAsync(tile_buf, tile * row,
+                                           static_cast<const char *>(index) + b0 * row,
+                                           (size_t)c->cfg.max_blocks * row, nb * row, LG,
+                                           cudaMemcpyHostToDevice, c->copy_stream));
+                KVM_CUDA(cudaEventRecord(c->ev_ready[buf], c->copy_stream));
+                KVM_CUDA(cudaStreamWaitEvent(s, c->ev_ready[buf], 0));
+            }
             if (pass == 1)
                 e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype,
                                             pass_shape(c, tsh), q,
-                                            c->stage[buf], b0, lo, hi, (int)(t * cpt), cpt,
+                                            tile_buf, b0, lo, hi, (int)(t * cpt), cpt,
                                             c->scr, s);
             else
                 e = kvm::launch_score_pass2(c->cfg.q_dtype, c->cfg.index_dtype,
                                             pass_shape(c, tsh), q,
-                                            c->stage[buf], b0, lo, hi, cpt, c->scr,
+                                            tile_buf, b0, lo, hi, cpt, c->scr,
                                             c->cfg.max_blocks, s);
             if (e != cudaSuccess) return cuda_fail(e, "tiled score pass");
-            KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
+            if (!spill) KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
         }
         if (pass == 1 && (e = kvm::launch_score_combine(sh, (int)(T * cpt), c->scr, s)) != cudaSuccess)
             return cuda_fail(e, "score combine");

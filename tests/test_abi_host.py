@@ -47,7 +47,7 @@ def test_workspace_bytes_and_validation(lib):
     for field, bad in [("head_dim", 96), ("block_tokens", 16), ("n_q_heads", 5),
                        ("view_blocks", 5), ("kv_dtype", 7), ("max_blocks", 0),
                        ("pool_pages", 1), ("max_queries", 1000), ("candidate_mode", 2),
-                       ("delta_rerope_limit", -1), ("h2d_mode", 3)]:
+                       ("delta_rerope_limit", -1), ("h2d_mode", 3), ("index_spill", 2)]:
         c = config_for(configs.TINY)
         setattr(c, field, bad)
         assert lib.kvm_workspace_bytes(ctypes.byref(c)) == 0, field

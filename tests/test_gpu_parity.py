@@ -109,21 +109,23 @@ def test_score_select_fewer_queries_and_ragged(kvm, variant):
 
 
 @pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
-@pytest.mark.parametrize("loc", ["device", "host-tiled"])
+@pytest.mark.parametrize("loc", ["device", "host-tiled", "host-tiled-spill"])
 def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
     """candidate_mode 1: the Eq. (10) softmax runs over the non-reserved blocks
     only; sink and recent blocks score exactly 0 and are still selected.  The
-    host-tiled index puts the candidate range's ends inside 96-block tiles."""
+    host-tiled index puts the candidate range's ends inside 96-block tiles;
+    with index_spill pass 2 reads the tiles pass 1 staged."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID.with_(n_blocks=1237, view_blocks=100)
     ws = workload.make_index_direct(wl, seed=4)
     kw = dict(score_variant=variant, candidate_mode=1)
     index = ws.index.to("cuda")
-    if loc == "host-tiled":
+    if loc.startswith("host-tiled"):
         kw["index_location"] = kvm.KVM_HOST_PINNED
+        kw["index_spill"] = int(loc.endswith("spill"))
         index = ws.index.pin_memory()
     cfg = kvm.config_for(wl, **kw)
-    if loc == "host-tiled":
+    if loc.startswith("host-tiled"):
         cfg.tile_blocks = 96
     ctx = kvm.Context(cfg)
     N, S, W = wl.n_blocks, wl.sink_blocks, wl.recent_blocks

@@ -24,7 +24,7 @@ def kvm():
 
 
 def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_step,
-               pool_extra=6, batch=7, h2d_mode=0, host_tier=None):
+               pool_extra=6, batch=7, h2d_mode=0, host_tier=None, index_spill=0):
     from paged_kv_cache_meank_gb300 import workload
     N_max = max(n_blocks_per_step)
     ws = workload.make_workspace(wl, seed=11, n_blocks=N_max, with_q=False)
@@ -37,7 +37,7 @@ def _run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per
         index_location=kvm.KVM_HOST_PINNED if index_host else kvm.KVM_DEVICE,
         h2d_batch_blocks=batch, h2d_mode=h2d_mode,
         host_tier_blocks=host_tier[0] if host_tier else 0,
-        host_tier_lambda=host_tier[1] if host_tier else 0.5)
+        host_tier_lambda=host_tier[1] if host_tier else 0.5, index_spill=index_spill)
     cfg.tile_blocks = 64
     tier_ref = oracle_tier.HostTier(*host_tier) if host_tier else None
     ctx = kvm.Context(cfg)
@@ -159,14 +159,16 @@ def test_step_host_tier_policy(kvm):
     assert sum(h["host_demoted"] for h in hist) > 0
 
 
-def test_step_host_index_tiled(kvm):
-    """Index in pinned host memory, scored in 64-block tiles (KVMem §5)."""
+@pytest.mark.parametrize("index_spill", [0, 1], ids=["restream", "spill"])
+def test_step_host_index_tiled(kvm, index_spill):
+    """Index in pinned host memory, scored in 64-block tiles (KVMem §5); with
+    index_spill the tiles cross the host link once per step."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID
     g = torch.Generator().manual_seed(22)
     u = workload.unit_vectors(1, wl.head_dim, g, "cpu")
     q = workload.make_queries(wl, g, "cpu", u[0])
-    _run_steps(kvm, wl, True, True, [q, q], [300, 300])
+    _run_steps(kvm, wl, True, True, [q, q], [300, 300], index_spill=index_spill)
 
 
 def test_step_failure_injection(kvm):
