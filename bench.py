@@ -464,6 +464,16 @@ def algorithmic_bytes(wl):
     return {"build": build, "score_select": score, "assemble": assemble}
 
 
+def workload_config(wl, world):
+    """The `config` object of a bench line: the workload and its sizes."""
+    return {"workload": wl.name, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
+            "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "history_blocks": wl.n_blocks,
+            "history_tokens": wl.n_tokens, "queries": wl.n_queries,
+            "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
+            "recent_blocks": wl.recent_blocks, "kv_dtype": wl.kv_dtype,
+            "parallelism": f"replicas{world}", "l2": "inputs larger than L2, no flush"}
+
+
 def bench_ours(args, wl, world, rank, local, dist):
     import paged_kv_cache_meank_gb300 as kvm_lib
     dev = torch.device("cuda", local)
@@ -539,13 +549,7 @@ def bench_ours(args, wl, world, rank, local, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.kv_dtype,
         "data": "synthetic (seeded N(0,1/128) raw K/V, 2% planted blocks, RoPE-free queries)",
-        "config": {"workload": wl.name, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
-                   "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "history_blocks": wl.n_blocks,
-                   "history_tokens": wl.n_tokens, "queries": wl.n_queries,
-                   "view_blocks": wl.view_blocks, "sink_blocks": wl.sink_blocks,
-                   "recent_blocks": wl.recent_blocks, "kv_dtype": wl.kv_dtype,
-                   "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2, no flush",
+        "config": {**workload_config(wl, world),
                    **({"index_spill": step.index_spill} if hasattr(step, "index_spill") else {})},
         "components": comps,
         "roofline": roof,
@@ -746,7 +750,7 @@ def bench_reference(args, wl, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": full * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name, "parallelism": "rank0 only"},
+        "config": workload_config(wl, world),
         "cpu_baseline": {"value": val, "unit": "scored blocks/s", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": f"each step restricted to {args.cpu_layers} of "
