@@ -204,6 +204,28 @@ def test_score_select_query_row_tilings(kvm, n_queries):
     check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
 
 
+@pytest.mark.parametrize("n_q_heads,n_queries", [(16, 32), (16, 16), (2, 129), (2, 1), (4, 3)],
+                         ids=["rows256", "rows128", "rows129", "rows1", "rows6"])
+def test_score_select_query_row_extremes(kvm, n_q_heads, n_queries):
+    """The ends of the tensor-core row tilings with other GQA ratios: the
+    largest count (256 rows, two full M = 128 tiles), exactly one tile (128),
+    one row past it (129, the duplicated second tile at its smallest), a single
+    row (MMA N = 16 with 15 padding columns) and 6 rows."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=389, view_blocks=40, n_q_heads=n_q_heads, n_queries=n_queries)
+    ws = workload.make_index_direct(wl, seed=60 + n_queries)
+    ctx = _ctx(kvm, wl)
+    scores = torch.empty(wl.n_blocks, device="cuda")
+    sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    ctx.score_select(ws.q.cuda(), n_queries, ws.index.cuda(), wl.n_blocks, scores, sel)
+    ctx.sync()
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q, "bf16"), "bf16"),
+                            ora.as_f64(to_np(ws.index, "bf16"), "bf16"), wl.n_blocks)
+    rows = n_queries * (n_q_heads // wl.n_kv_heads)
+    assert_scores_close(scores.cpu().numpy(), R, f"{rows} rows")
+    check_selection(sel.cpu().numpy(), R, wl.sink_blocks, wl.recent_blocks, wl.view_blocks)
+
+
 def test_select_ties_and_small_histories(kvm):
     """Equal Mean-K everywhere: all scores tie and the lowest ids win; histories
     of N <= V_b select everything; N = V_b + 1 leaves out exactly one block."""
