@@ -88,6 +88,25 @@ def test_layout_sizes_follow_the_workloads():
     assert 2 * w.block_bytes == 2 * w.n_layers * 32 * w.n_kv_heads * w.head_dim * 2
 
 
+def test_index_spill_workspace_holds_the_index(lib):
+    """With a host-resident index, index_spill keeps one staging tile per index
+    tile in the workspace: it grows by the index size less the two tiles that
+    the default double buffering needs."""
+    wl = configs.W1M
+    base = config_for(wl)
+    spill = config_for(wl, index_spill=1)
+    n0 = lib.kvm_workspace_bytes(ctypes.byref(base))
+    n1 = lib.kvm_workspace_bytes(ctypes.byref(spill))
+    tile = wl.n_layers * wl.n_kv_heads * base.tile_blocks * wl.head_dim * 2
+    tiles = -(-base.max_blocks // base.tile_blocks)
+    assert n1 - n0 == tiles * tile - 2 * tile
+    # a device-resident index stages nothing either way
+    dev = config_for(wl, index_location=0)
+    dev_spill = config_for(wl, index_location=0, index_spill=1)
+    assert lib.kvm_workspace_bytes(ctypes.byref(dev)) == lib.kvm_workspace_bytes(
+        ctypes.byref(dev_spill))
+
+
 def test_struct_layouts_match_the_header(tmp_path):
     """The ctypes mirrors of kvm_config, kvm_buffers, kvm_step_stats and
     kvm_tier_stats have the header's sizes and field offsets (a C program
