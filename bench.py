@@ -269,15 +269,14 @@ def build_host_workspace(kvm, wl, seed, device, stream, ctx, n_blocks, index_on_
         index = torch.zeros(ctx.index_shape(), dtype=ctx.index_dtype, device=device)
         ctx.build_index(kp, 0, n_blocks, index, ws.raw_k, stream=stream)
     ctx.sync(stream)
-    raw_h = torch.empty(ws.raw_k.shape, dtype=ws.raw_k.dtype, pin_memory=True)
-    raw_h.copy_(ws.raw_k)
-    v_h = torch.empty(ws.v.shape, dtype=ws.v.dtype, pin_memory=True)
-    v_h.copy_(ws.v)
+    # exact-size page-locked buffers: the pinned allocator would round each up
+    # to a power of two (a 74 GB repository half would lock 128 GB)
+    from paged_kv_cache_meank_gb300 import hostmem
+    raw_h = hostmem.pinned_copy(ws.raw_k)
+    v_h = hostmem.pinned_copy(ws.v)
     tail = kp[keep_pages_from:].clone() if keep_pages_from is not None else None
     if index_on_host:
-        idx_h = torch.empty(index.shape, dtype=index.dtype, pin_memory=True)
-        idx_h.copy_(index)
-        index = idx_h
+        index = hostmem.pinned_copy(index)
     planted, u, topic_of = ws.planted, ws.u, ws.topic_of
     del ws, kp
     torch.cuda.empty_cache()

@@ -369,6 +369,24 @@ const char *kvm_last_error(void);
  * and memsets are not kernels and are not counted. */
 int64_t kvm_launch_count(void);
 
+/*
+ * Page-locked host memory of exactly `bytes` bytes, for the buffers a caller
+ * hands the library in host memory (the raw K / V repository, a host-resident
+ * index).  A convenience for callers: the library itself never allocates.  The
+ * memory is portable (usable from every context) and mapped (kernels address
+ * it through its device alias), and the CUDA driver allocates it.  Measured on
+ * GB300 with a 148 GB repository, the GPU reads scattered blocks of it over
+ * the host link at the full pinned-copy rate; from ordinary host memory
+ * registered after allocation it read at 0.48-0.93 of that rate, depending on
+ * how the pages happened to be laid out.
+ * out      host; receives the pointer (NULL on failure).
+ * Errors:  KVM_ERR_INVALID_ARG for bytes == 0 or out == NULL; KVM_ERR_CUDA if
+ *          the driver cannot allocate (kvm_last_error has its message).
+ * Free with kvm_host_free once no copy or kernel uses the memory.
+ */
+kvm_status kvm_host_alloc(size_t bytes, void **out);
+kvm_status kvm_host_free(void *ptr);
+
 /* Fault injection for tests.  what = 1 / 2: make the n-th (1-based) next host
  * copy submission / kernel launch of kvm_step fail with KVM_ERR_INJECTED.
  * what = 3: the n-th next tensor-core scoring pass (kvm_score_select or

@@ -100,6 +100,8 @@ SIGNATURES = {
     "kvm_last_error": (ctypes.c_char_p, []),
     "kvm_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]),
     "kvm_launch_count": (ctypes.c_int64, []),
+    "kvm_host_alloc": (ctypes.c_int, [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]),
+    "kvm_host_free": (ctypes.c_int, [ctypes.c_void_p]),
 }
 
 _lib = None

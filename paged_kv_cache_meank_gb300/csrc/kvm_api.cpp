@@ -884,6 +884,24 @@ const char *kvm_last_error(void) { return g_last_error.c_str(); }
 
 int64_t kvm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+kvm_status kvm_host_alloc(size_t bytes, void **out) {
+    if (!out) return fail(KVM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (bytes == 0) return fail(KVM_ERR_INVALID_ARG, "bytes must be > 0");
+    void *p = nullptr;
+    const cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    *out = p;
+    return KVM_OK;
+}
+
+kvm_status kvm_host_free(void *ptr) {
+    if (!ptr) return KVM_OK;
+    const cudaError_t e = cudaFreeHost(ptr);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFreeHost");
+    return KVM_OK;
+}
+
 kvm_status kvm_debug_inject(kvm_ctx *c, int32_t what, int64_t nth) {
     if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
     if (what < 0 || what > 3 || (what != 0 && nth < 1))

@@ -6,6 +6,7 @@ every block when that is a few seconds of float64 work) and properties that
 hold at any size.  Inputs are seeded draws (raw K / V, Mean-K drawn directly,
 K pages drawn directly) -- nothing the oracle consumes comes from the CUDA path.
 """
+import contextlib
 import gc
 
 import numpy as np
@@ -15,7 +16,7 @@ import torch
 import oracle.kvmem as ora
 from gpu_helpers import (assert_meank_close, assert_scores_close, assert_storage_close,
                          check_selection, to_np)
-from paged_kv_cache_meank_gb300 import configs, workload
+from paged_kv_cache_meank_gb300 import configs, hostmem, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -37,10 +38,18 @@ def _release_memory():
         torch._C._host_emptyCache()
 
 
-def _pinned(t):
-    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-    h.copy_(t)
-    return h
+@contextlib.contextmanager
+def _pinned(*ts):
+    """Exact-size page-locked host copies of the tensors, unregistered on exit
+    (the pinned allocator would round each up to a power of two)."""
+    hs = []
+    try:
+        for t in ts:
+            hs.append(hostmem.pinned_copy(t))
+        yield hs
+    finally:
+        for h in hs:
+            hostmem.release(h)
 
 
 def _oracle_R(q, index, wl, n_blocks):
@@ -194,104 +203,105 @@ def test_1m_host_step(kvm):
     N, V = wl.n_blocks, wl.view_blocks
     ws = workload.make_workspace(wl, seed=105, device="cuda", with_q=False)
     idx = workload.make_index_direct(wl, seed=106, device="cuda")
-    raw_h, v_h, idx_h = _pinned(ws.raw_k), _pinned(ws.v), _pinned(idx.index)
-    q = idx.q
-    del ws
-    torch.cuda.empty_cache()
-    cfg = kvm.config_for(wl, h2d_batch_blocks=256, index_spill=1)
-    ctx = kvm.Context(cfg)
-    P = cfg.pool_pages
-    pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
-    pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
-    pt = torch.empty(V, dtype=torch.int32, device="cuda")
-    scores = torch.empty(N, device="cuda")
-    sel = torch.empty(V, dtype=torch.int32, device="cuda")
-    ctx.bind(index=idx_h, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
-             page_table=pt, scores=scores, sel_ids=sel)
-    st = ctx.step(q, wl.n_queries, N)
-    ctx.sync()
-    assert st["misses"] == V and st["hits"] == 0
-    R = _oracle_R(q, idx.index, wl, N)
-    assert_scores_close(scores.cpu().numpy(), R, "1M scores")
-    g_sel = sel.cpu().numpy()
-    check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, "1M")
-    page, _, _, _, _ = ora.residency_step([-1] * P, [-1] * P, g_sel)
-    assert pt.cpu().tolist() == page
-    rng = np.random.default_rng(9)
-    for j in np.unique(np.concatenate([[0, V - 1], rng.choice(V, 14, replace=False)])):
-        b, p = int(g_sel[j]), page[j]
-        raw = to_np(raw_h[b:b + 1], "bf16")
-        c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
-        ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
-        assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16", f"1M slot {j}")
-        assert torch.equal(pool_v[p].cpu(), v_h[b])
-        assert torch.equal(pool_r[p].cpu(), raw_h[b])
-
-
-def test_512k_churn_steps(kvm):
-    """Twenty agent steps over the 512K-token history (16-layer slice): each
-    step appends 64 blocks whose Mean-K the GPU builds, draws queries with 70%
-    topic overlap, and updates the page pool by the delta rule; scores and
-    selection against the oracle every fifth step, the page table every step."""
-    wl = configs.CHURN512K_16
-    total = wl.n_blocks + wl.steps * wl.append_blocks
-    V = wl.view_blocks
-    ws = workload.make_workspace(wl, seed=107, device="cuda", n_blocks=total, with_q=False)
-    raw_h, v_h = _pinned(ws.raw_k), _pinned(ws.v)
-    g = torch.Generator(device="cuda").manual_seed(108)
-    base = workload.make_index_direct(wl.with_(n_topics=1), seed=109, device="cuda",
-                                      n_blocks=wl.n_blocks)
-    new_pages = (torch.randn((wl.steps * wl.append_blocks, wl.n_layers, wl.n_kv_heads, 32,
-                              wl.head_dim), generator=g, device="cuda") * wl.k_std).to(torch.bfloat16)
-    topics = workload.churn_topics(wl, 107, "cuda")
-    cfg = kvm.config_for(wl, h2d_batch_blocks=256)
-    ctx = kvm.Context(cfg)
-    index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
-    index[:, :, :wl.n_blocks] = base.index
-    # the oracle's index: the same drawn base plus its own Mean-K of the appended pages
-    new_np = to_np(new_pages, "bf16")
-    ora_index = np.zeros((wl.n_layers, wl.n_kv_heads, total, wl.head_dim))
-    ora_index[:, :, :wl.n_blocks] = ora.as_f64(to_np(base.index, "bf16"), "bf16")
-    P = cfg.pool_pages
-    pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
-    pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
-    pt = torch.empty(V, dtype=torch.int32, device="cuda")
-    scores = torch.empty(total, device="cuda")
-    sel = torch.empty(V, dtype=torch.int32, device="cuda")
-    ctx.bind(index=index, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
-             page_table=pt, scores=scores, sel_ids=sel)
-    del ws
-    bop, bp = [-1] * P, [-1] * P
-    rng = np.random.default_rng(10)
-    hits = []
-    for t in range(wl.steps):
-        n_prev = wl.n_blocks + t * wl.append_blocks
-        n_now = n_prev + wl.append_blocks
-        a = t * wl.append_blocks
-        ctx.build_index(new_pages[a:a + wl.append_blocks], n_prev, wl.append_blocks, index, None)
-        mk = ora.meank(new_np[a:a + wl.append_blocks], "bf16", n_prev, wl.rope_theta)
-        ora_index[:, :, n_prev:n_now] = ora.as_f64(ora.round_to(mk.astype(np.float32), "bf16"),
-                                                   "bf16")
-        ws_like = workload.Workspace(wl=wl, u=base.u[None].expand(wl.n_topics, -1),
-                                     planted=base.planted)
-        q = workload.churn_queries(wl, ws_like, t, topics[t], 107, "cuda")
-        st = ctx.step(q, wl.n_queries, n_now)
+    with _pinned(ws.raw_k, ws.v, idx.index) as (raw_h, v_h, idx_h):
+        q = idx.q
+        del ws
+        torch.cuda.empty_cache()
+        cfg = kvm.config_for(wl, h2d_batch_blocks=256, index_spill=1)
+        ctx = kvm.Context(cfg)
+        P = cfg.pool_pages
+        pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+        pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
+        pt = torch.empty(V, dtype=torch.int32, device="cuda")
+        scores = torch.empty(N, device="cuda")
+        sel = torch.empty(V, dtype=torch.int32, device="cuda")
+        ctx.bind(index=idx_h, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
+                 page_table=pt, scores=scores, sel_ids=sel)
+        st = ctx.step(q, wl.n_queries, N)
         ctx.sync()
-        g_sel = sel[:V].cpu().numpy()
-        if t % 5 == 0 or t == wl.steps - 1:
-            R = ora.block_relevance(ora.as_f64(to_np(q, "bf16"), "bf16"), ora_index, n_now)
-            assert_scores_close(scores[:n_now].cpu().numpy(), R, f"churn step {t}")
-            check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, f"churn step {t}")
-        page, hit, rope, bop, bp = ora.residency_step(bop, bp, g_sel)
-        assert pt.cpu().tolist() == page, f"step {t} page table"
-        assert st["hits"] == sum(hit) and st["reroped"] == sum(rope)
-        hits.append(st["hits"])
-        for j in rng.choice(V, 4, replace=False):
+        assert st["misses"] == V and st["hits"] == 0
+        R = _oracle_R(q, idx.index, wl, N)
+        assert_scores_close(scores.cpu().numpy(), R, "1M scores")
+        g_sel = sel.cpu().numpy()
+        check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, "1M")
+        page, _, _, _, _ = ora.residency_step([-1] * P, [-1] * P, g_sel)
+        assert pt.cpu().tolist() == page
+        rng = np.random.default_rng(9)
+        for j in np.unique(np.concatenate([[0, V - 1], rng.choice(V, 14, replace=False)])):
             b, p = int(g_sel[j]), page[j]
             raw = to_np(raw_h[b:b + 1], "bf16")
             c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
             ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
-            assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16",
-                                 f"churn step {t} slot {j}")
+            assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16", f"1M slot {j}")
             assert torch.equal(pool_v[p].cpu(), v_h[b])
-    assert hits[0] == 0 and max(hits[1:]) > 0      # later steps reuse resident pages
+            assert torch.equal(pool_r[p].cpu(), raw_h[b])
+
+
+def test_512k_churn_steps(kvm):
+    """Twenty agent steps over the 512K-token history (64 layers; the host
+    repository holds 148 GB of raw K and V in exact-size page-locked memory): each
+    step appends 64 blocks whose Mean-K the GPU builds, draws queries with 70%
+    topic overlap, and updates the page pool by the delta rule; scores and
+    selection against the oracle every fifth step, the page table every step."""
+    wl = configs.CHURN512K
+    total = wl.n_blocks + wl.steps * wl.append_blocks
+    V = wl.view_blocks
+    ws = workload.make_workspace(wl, seed=107, device="cuda", n_blocks=total, with_q=False)
+    with _pinned(ws.raw_k, ws.v) as (raw_h, v_h):
+        g = torch.Generator(device="cuda").manual_seed(108)
+        base = workload.make_index_direct(wl.with_(n_topics=1), seed=109, device="cuda",
+                                          n_blocks=wl.n_blocks)
+        new_pages = (torch.randn((wl.steps * wl.append_blocks, wl.n_layers, wl.n_kv_heads, 32,
+                                  wl.head_dim), generator=g, device="cuda") * wl.k_std).to(torch.bfloat16)
+        topics = workload.churn_topics(wl, 107, "cuda")
+        cfg = kvm.config_for(wl, h2d_batch_blocks=256)
+        ctx = kvm.Context(cfg)
+        index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+        index[:, :, :wl.n_blocks] = base.index
+        # the oracle's index: the same drawn base plus its own Mean-K of the appended pages
+        new_np = to_np(new_pages, "bf16")
+        ora_index = np.zeros((wl.n_layers, wl.n_kv_heads, total, wl.head_dim))
+        ora_index[:, :, :wl.n_blocks] = ora.as_f64(to_np(base.index, "bf16"), "bf16")
+        P = cfg.pool_pages
+        pool_k = torch.empty(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+        pool_v, pool_r = torch.empty_like(pool_k), torch.empty_like(pool_k)
+        pt = torch.empty(V, dtype=torch.int32, device="cuda")
+        scores = torch.empty(total, device="cuda")
+        sel = torch.empty(V, dtype=torch.int32, device="cuda")
+        ctx.bind(index=index, raw_k=raw_h, v=v_h, pool_k=pool_k, pool_v=pool_v, pool_raw_k=pool_r,
+                 page_table=pt, scores=scores, sel_ids=sel)
+        del ws
+        bop, bp = [-1] * P, [-1] * P
+        rng = np.random.default_rng(10)
+        hits = []
+        for t in range(wl.steps):
+            n_prev = wl.n_blocks + t * wl.append_blocks
+            n_now = n_prev + wl.append_blocks
+            a = t * wl.append_blocks
+            ctx.build_index(new_pages[a:a + wl.append_blocks], n_prev, wl.append_blocks, index, None)
+            mk = ora.meank(new_np[a:a + wl.append_blocks], "bf16", n_prev, wl.rope_theta)
+            ora_index[:, :, n_prev:n_now] = ora.as_f64(ora.round_to(mk.astype(np.float32), "bf16"),
+                                                       "bf16")
+            ws_like = workload.Workspace(wl=wl, u=base.u[None].expand(wl.n_topics, -1),
+                                         planted=base.planted)
+            q = workload.churn_queries(wl, ws_like, t, topics[t], 107, "cuda")
+            st = ctx.step(q, wl.n_queries, n_now)
+            ctx.sync()
+            g_sel = sel[:V].cpu().numpy()
+            if t % 5 == 0 or t == wl.steps - 1:
+                R = ora.block_relevance(ora.as_f64(to_np(q, "bf16"), "bf16"), ora_index, n_now)
+                assert_scores_close(scores[:n_now].cpu().numpy(), R, f"churn step {t}")
+                check_selection(g_sel, R, wl.sink_blocks, wl.recent_blocks, V, f"churn step {t}")
+            page, hit, rope, bop, bp = ora.residency_step(bop, bp, g_sel)
+            assert pt.cpu().tolist() == page, f"step {t} page table"
+            assert st["hits"] == sum(hit) and st["reroped"] == sum(rope)
+            hits.append(st["hits"])
+            for j in rng.choice(V, 4, replace=False):
+                b, p = int(g_sel[j]), page[j]
+                raw = to_np(raw_h[b:b + 1], "bf16")
+                c, s = ora.cos_sin_f32(ora.slot_positions(V)[j], wl.head_dim, wl.rope_theta)
+                ref = ora.round_to(ora.rope_f32(ora.as_f32(raw, "bf16"), c, s), "bf16")
+                assert_storage_close(to_np(pool_k[p:p + 1], "bf16"), ref, "bf16",
+                                     f"churn step {t} slot {j}")
+                assert torch.equal(pool_v[p].cpu(), v_h[b])
+        assert hits[0] == 0 and max(hits[1:]) > 0      # later steps reuse resident pages
