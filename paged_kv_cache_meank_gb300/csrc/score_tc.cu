@@ -397,8 +397,11 @@ bool make_index_map(CUtensorMap *m, const void *index, int d, int64_t n_rows, in
 }
 
 bool score_tc_supported(int q_dtype, int index_dtype, const ScoreShape &sh) {
+    // the TMA row coordinate (l * G + g) * index_cap + block is a 32-bit int:
+    // larger indexes take the CUDA-core kernels, which index in 64 bits
+    const bool rows_fit = (int64_t)sh.L * sh.G * sh.index_cap <= (int64_t)INT32_MAX;
     return q_dtype == BF16 && index_dtype == BF16 && (sh.d == 64 || sh.d == 128) &&
-           sh.rows >= 1 && sh.rows <= kQRows && encode_fn() != nullptr;
+           sh.rows >= 1 && sh.rows <= kQRows && rows_fit && encode_fn() != nullptr;
 }
 
 template <int D, int NC>
