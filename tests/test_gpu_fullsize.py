@@ -237,6 +237,17 @@ def test_1m_host_step(kvm):
             assert torch.equal(pool_r[p].cpu(), raw_h[b])
 
 
+def _host_available_bytes() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def test_512k_churn_steps(kvm):
     """Twenty agent steps over the 512K-token history (64 layers; the host
     repository holds 148 GB of raw K and V in exact-size page-locked memory): each
@@ -246,6 +257,10 @@ def test_512k_churn_steps(kvm):
     wl = configs.CHURN512K
     total = wl.n_blocks + wl.steps * wl.append_blocks
     V = wl.view_blocks
+    # 148 GB of page-locked repository plus the oracle's float64 index (9 GB)
+    need = 2 * total * wl.block_bytes + 24 * 10 ** 9
+    if _host_available_bytes() < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of free host memory")
     ws = workload.make_workspace(wl, seed=107, device="cuda", n_blocks=total, with_q=False)
     with _pinned(ws.raw_k, ws.v) as (raw_h, v_h):
         g = torch.Generator(device="cuda").manual_seed(108)
