@@ -534,6 +534,11 @@ def bench_ours(args, wl, world, rank, local, dist):
     comps = {"recall_ms": recall_ms, **{f"{p}_ms": parts[p] for p in parts}, "kernels": kern}
     if "score_select" in parts:
         comps["index_hbm_gbs"] = kern["score_select"]["gbs"]
+    if link is None and len(parts) > 1:
+        # the whole step against HBM: every part's algorithmic bytes, with the
+        # index read twice (the two exact scoring passes), over the step time
+        step_bytes = sum(ab[p] for p in parts) + ab.get("score_select", 0)
+        comps["step_hbm_frac"] = step_bytes / (ms * 1e-3) / 1e9 / peak
     if "assemble" in parts:
         comps["assembly_tokens_per_s"] = wl.view_tokens / (parts["assemble"] * 1e-3)
     if getattr(step, "stats", None):
