@@ -284,6 +284,31 @@ def test_empty_and_degenerate_inputs(kvm, variant):
     ctx.sync()
 
 
+@pytest.mark.parametrize("N", [389, 20000], ids=["one-cta", "many-cta"])
+@pytest.mark.parametrize("S,W,V", [(0, 0, 40), (0, 8, 40), (4, 0, 40), (4, 8, 13), (0, 0, 1)],
+                         ids=["topk-only", "no-sink", "no-recent", "k1", "k1-no-reserved"])
+def test_select_budget_edges(kvm, N, S, W, V):
+    """Budgets at their edges -- no sink blocks, no recent blocks, a top-k of one
+    -- through both select paths, against the oracle's Eq. (10) and the band
+    rule."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=N, sink_blocks=S, recent_blocks=W, view_blocks=V)
+    ws = workload.make_index_direct(wl, seed=70 + S + W + V)
+    ctx = _ctx(kvm, wl)
+    scores = torch.empty(N, device="cuda")
+    sel = torch.full((V,), -1, dtype=torch.int32, device="cuda")
+    n_sel = ctx.score_select(ws.q.cuda(), wl.n_queries, ws.index.cuda(), N, scores, sel)
+    ctx.sync()
+    assert n_sel == V
+    R = ora.block_relevance(ora.as_f64(to_np(ws.q, "bf16"), "bf16"),
+                            ora.as_f64(to_np(ws.index, "bf16"), "bf16"), N)
+    assert_scores_close(scores.cpu().numpy(), R, f"S={S} W={W} V={V}")
+    check_selection(sel.cpu().numpy(), R, S, W, V, f"S={S} W={W} V={V}")
+    # and exactly the oracle's selection over the GPU's own scores
+    want = ora.select_blocks(scores.cpu().double().numpy(), S, W, V)
+    assert np.array_equal(sel.cpu().numpy(), want)
+
+
 @pytest.mark.parametrize("pattern", ["random", "uniform", "classes"])
 @pytest.mark.parametrize("N", [16384, 40000, 100003])
 def test_select_long_histories_exact(kvm, N, pattern):

@@ -129,6 +129,25 @@ def test_step_sequence(kvm, repo_host, h2d_mode):
     assert hist[2]["misses"] == 0 and hist[2]["reroped"] == 0
 
 
+@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 1)],
+                         ids=["repo-device", "repo-host-gpu-pull"])
+def test_step_history_shrinks_and_grows(kvm, repo_host, h2d_mode):
+    """The history shrinks between steps, below the view budget (50 blocks for
+    60 slots: everything is selected, fewer slots than the budget), then grows
+    back: pages holding blocks past the end are free, and blocks still resident
+    from earlier steps are hits again."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    g = torch.Generator().manual_seed(23)
+    u = workload.unit_vectors(2, wl.head_dim, g, "cpu")
+    qa = workload.make_queries(wl, g, "cpu", u[0])
+    qb = workload.make_queries(wl, g, "cpu", u[1])
+    hist = _run_steps(kvm, wl, repo_host, False, [qa, qb, qa, qa, qb], [300, 200, 50, 300, 300],
+                      h2d_mode=h2d_mode)
+    assert hist[2]["misses"] + hist[2]["hits"] == 50
+    assert hist[3]["hits"] > 0 and hist[4]["hits"] > 0
+
+
 @pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 0), (True, 1)],
                          ids=["repo-device", "repo-host-copy-engine", "repo-host-gpu-pull"])
 def test_step_sequence_fp8_pages(kvm, repo_host, h2d_mode):
