@@ -139,15 +139,14 @@ __global__ void score_simt_kernel(const TQ *__restrict__ q, const TI *__restrict
 }
 
 int sm_count() {
-    static int n = 0;
-    if (n <= 0) {
+    // read once per process (thread-safe initialisation of a local static)
+    static const int n = [] {
         int dev = 0, v = 0;
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            return 152;
-    }
+            return v;
+        return 152;
+    }();
     return n;
 }
 

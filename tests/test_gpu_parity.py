@@ -284,6 +284,48 @@ def test_empty_and_degenerate_inputs(kvm, variant):
     ctx.sync()
 
 
+def test_two_host_threads_two_contexts(kvm):
+    """Two host threads, each with its own context and stream, score, select
+    and assemble at the same time (ctypes releases the GIL around the calls);
+    each gets exactly what the same calls return one after the other."""
+    import threading
+    from paged_kv_cache_meank_gb300 import workload
+    wls = [MID.with_(n_blocks=700, view_blocks=60), MID64.with_(n_blocks=20000, view_blocks=50)]
+    inputs = []
+    for i, wl in enumerate(wls):
+        ws = workload.make_index_direct(wl, seed=80 + i)
+        raw = torch.randn(wl.n_blocks, wl.n_layers, wl.n_kv_heads, 32, wl.head_dim,
+                          device="cuda", generator=torch.Generator("cuda").manual_seed(90 + i))
+        inputs.append((wl, ws.q.cuda(), ws.index.cuda(), raw.to(torch.bfloat16)))
+
+    def run(i, out, stream):
+        wl, q, index, raw = inputs[i]
+        ctx = kvm.Context(kvm.config_for(wl), stream=stream)
+        scores = torch.empty(wl.n_blocks, device="cuda")
+        sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+        pages = torch.empty(ctx.block_shape(wl.view_blocks), dtype=torch.bfloat16, device="cuda")
+        for _ in range(5):
+            ctx.score_select(q, wl.n_queries, index, wl.n_blocks, scores, sel, stream=stream)
+            ctx.assemble_view(sel, None, wl.view_blocks, raw, None, pages, None, stream=stream)
+        ctx.sync(stream)
+        out[i] = (scores.cpu(), sel.cpu(), pages.cpu())
+        ctx.close()
+
+    seq = {}
+    for i in range(2):
+        run(i, seq, torch.cuda.Stream())
+    par = {}
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ts = [threading.Thread(target=run, args=(i, par, streams[i])) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    for i in range(2):
+        for a, b in zip(seq[i], par[i]):
+            assert torch.equal(a, b), i
+
+
 @pytest.mark.parametrize("N", [389, 20000], ids=["one-cta", "many-cta"])
 @pytest.mark.parametrize("S,W,V", [(0, 0, 40), (0, 8, 40), (4, 0, 40), (4, 8, 13), (0, 0, 1)],
                          ids=["topk-only", "no-sink", "no-recent", "k1", "k1-no-reserved"])
