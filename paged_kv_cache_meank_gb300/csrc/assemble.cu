@@ -160,7 +160,8 @@ assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
 
 static int lg_split(int n_slots, int LG) {
     int lpc = LG;
-    while (lpc > 8 && (int64_t)n_slots * ((LG + lpc - 1) / lpc) < 152 * 16) lpc = (lpc + 1) / 2;
+    const int64_t want_ctas = (int64_t)sm_count() * 16;
+    while (lpc > 8 && (int64_t)n_slots * ((LG + lpc - 1) / lpc) < want_ctas) lpc = (lpc + 1) / 2;
     return lpc > 64 ? 64 : lpc;
 }
 

@@ -130,7 +130,7 @@ static cudaError_t launch_meank_t(const void *k_pages, void *raw_out, void *inde
     // built.  The cap was measured on the 256K build: 128 pairs for 2- and
     // 4-byte elements, 256 for e4m3, whose pairs carry half the bytes.
     int lg_per_cta = LG;
-    const int64_t want_ctas = 152 * 16;
+    const int64_t want_ctas = (int64_t)sm_count() * 16;
     while (lg_per_cta > kMeanKWarps &&
            n_blocks * ((LG + lg_per_cta - 1) / lg_per_cta) < want_ctas)
         lg_per_cta = (lg_per_cta + 1) / 2;

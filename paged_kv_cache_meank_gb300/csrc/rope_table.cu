@@ -24,7 +24,7 @@ cudaError_t launch_rope_table(float2 *table, int64_t n_pos, int half_d, const Om
                               cudaStream_t s) {
     const int64_t total = n_pos * half_d;
     int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 64) blocks = 152 * 64;
+    if (blocks > (int64_t)sm_count() * 64) blocks = (int64_t)sm_count() * 64;
     if (blocks < 1) blocks = 1;
     rope_table_kernel<<<(unsigned)blocks, 256, 0, s>>>(table, n_pos, half_d, om);
     note_launch();
