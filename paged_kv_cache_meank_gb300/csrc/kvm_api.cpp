@@ -604,6 +604,64 @@ kvm_status kvm_reset_pool(kvm_ctx *c) {
     return KVM_OK;
 }
 
+// The delta working set of [KVMem] §4.4: hits keep their pages; misses take
+// the free pages (those not holding a selected block) in ascending page order,
+// in ascending slot order.  Fills the page of every slot and whether it is a hit.
+static kvm_status assign_pages(kvm_ctx *c, const std::vector<int32_t> &sel,
+                               std::vector<int32_t> *page_of_slot, std::vector<uint8_t> *is_hit) {
+    const int n_sel = (int)sel.size();
+    const int P = c->cfg.pool_pages;
+    page_of_slot->assign(n_sel, -1);
+    is_hit->assign(n_sel, 0);
+    for (int j = 0; j < n_sel; ++j)
+        if (sel[j] < 0 || sel[j] >= c->cfg.max_blocks)
+            return fail(KVM_ERR_DEVICE, "selected id %d out of range", sel[j]);
+    for (int j = 0; j < n_sel; ++j) {
+        const int32_t b = sel[j];
+        c->mark[b] = 1;
+        if (c->page_of_block[b] >= 0) {
+            (*page_of_slot)[j] = c->page_of_block[b];
+            (*is_hit)[j] = 1;
+        }
+    }
+    std::vector<int32_t> free_pages;
+    free_pages.reserve(P);
+    for (int p = 0; p < P; ++p) {
+        const int64_t b = c->block_of_page[p];
+        if (b < 0 || !c->mark[b]) free_pages.push_back(p);
+    }
+    for (int j = 0; j < n_sel; ++j) c->mark[sel[j]] = 0;
+    int n_miss = 0;
+    for (int j = 0; j < n_sel; ++j) n_miss += !(*is_hit)[j];
+    if (n_miss > (int)free_pages.size())
+        return fail(KVM_ERR_CAPACITY, "%d misses but only %zu free pages", n_miss, free_pages.size());
+    int f = 0;
+    for (int j = 0; j < n_sel; ++j)
+        if (!(*is_hit)[j]) (*page_of_slot)[j] = free_pages[f++];
+    return KVM_OK;
+}
+
+// Records the step's residency once its transfers are enqueued: each missed
+// block now owns its page (evicting the block the page held), and every page's
+// K is baked at its slot's positions.  Returns the number of evicted blocks.
+static int commit_residency(kvm_ctx *c, const std::vector<int32_t> &sel,
+                            const std::vector<int32_t> &page_of_slot,
+                            const std::vector<int> &miss_slots) {
+    int evicted = 0;
+    for (int j : miss_slots) {
+        const int p = page_of_slot[j];
+        const int64_t old = c->block_of_page[p];
+        if (old >= 0) {
+            c->page_of_block[old] = -1;
+            ++evicted;
+        }
+        c->block_of_page[p] = sel[j];
+        c->page_of_block[sel[j]] = p;
+    }
+    for (size_t j = 0; j < sel.size(); ++j) c->baked_pos[page_of_slot[j]] = (int64_t)j * 32;
+    return evicted;
+}
+
 static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
                             kvm_step_stats *stats, kvm_stream stream) {
     const kvm_config &cfg = c->cfg;
@@ -619,38 +677,9 @@ static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_
                              cudaMemcpyDeviceToHost, s));
     KVM_CUDA(cudaStreamSynchronize(s));
 
-    // delta working set: hits keep their pages, misses take free pages in
-    // ascending page order, in ascending slot order
-    const int P = cfg.pool_pages;
-    std::vector<int32_t> page_of_slot(n_sel, -1);
-    std::vector<uint8_t> is_hit(n_sel, 0);
-    for (int j = 0; j < n_sel; ++j)
-        if (sel[j] < 0 || sel[j] >= cfg.max_blocks)
-            return fail(KVM_ERR_DEVICE, "selected id %d out of range", sel[j]);
-    for (int j = 0; j < n_sel; ++j) {
-        const int32_t b = sel[j];
-        c->mark[b] = 1;
-        if (c->page_of_block[b] >= 0) {
-            page_of_slot[j] = c->page_of_block[b];
-            is_hit[j] = 1;
-        }
-    }
-    std::vector<int32_t> free_pages;
-    free_pages.reserve(P);
-    for (int p = 0; p < P; ++p) {
-        const int64_t b = c->block_of_page[p];
-        if (b < 0 || !c->mark[b]) free_pages.push_back(p);
-    }
-    for (int j = 0; j < n_sel; ++j) c->mark[sel[j]] = 0;
-    int n_miss = 0;
-    for (int j = 0; j < n_sel; ++j) n_miss += !is_hit[j];
-    if (n_miss > (int)free_pages.size())
-        return fail(KVM_ERR_CAPACITY, "%d misses but only %zu free pages", n_miss, free_pages.size());
-    {
-        int f = 0;
-        for (int j = 0; j < n_sel; ++j)
-            if (!is_hit[j]) page_of_slot[j] = free_pages[f++];
-    }
+    std::vector<int32_t> page_of_slot;
+    std::vector<uint8_t> is_hit;
+    if ((st = assign_pages(c, sel, &page_of_slot, &is_hit)) != KVM_OK) return st;
 
     const size_t blk = block_bytes(cfg);
     const bool host_repo = cfg.repo_location == KVM_HOST_PINNED;
@@ -800,18 +829,7 @@ static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_
                              cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return abort_step(cuda_fail(e, "page table upload"));
 
-    // commit the new residency
-    for (int j : miss_slots) {
-        const int p = page_of_slot[j];
-        const int64_t old = c->block_of_page[p];
-        if (old >= 0) {
-            c->page_of_block[old] = -1;
-            ++evicted;
-        }
-        c->block_of_page[p] = sel[j];
-        c->page_of_block[sel[j]] = p;
-    }
-    for (int j = 0; j < n_sel; ++j) c->baked_pos[page_of_slot[j]] = (int64_t)j * 32;
+    evicted = commit_residency(c, sel, page_of_slot, miss_slots);
     c->delta_count.swap(new_count);
 
     kvm_tier_stats ts{};
