@@ -526,6 +526,21 @@ def bench_ours(args, wl, world, rank, local, dist):
     roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["gbs"], "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_hbm"],
             "traffic": traffic, "algorithmic_bytes": ab[dom]}
+    if dom == "score_select" and len(parts) == 1:
+        # scoring alone: each exact pass of Eq. (10) takes one exponential per
+        # (query row, block, layer, kv head) on the MUFU unit, 16 per clock per
+        # SM, and that binds as tightly as HBM does (reported beside it)
+        n_exp = 2 * wl.n_queries * wl.gqa * wl.n_blocks * wl.n_layers * wl.n_kv_heads
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        max_mhz = float(clk.get("sm_max_mhz") or 2070.0)
+        ach = n_exp / (parts[dom] * 1e-3) / 1e9
+        mufu_peak = 16 * sms * max_mhz * 1e-3
+        roof = {"bound": "alu", "kernel": dom, "unit": "Gex2/s", "achieved": ach,
+                "peak": mufu_peak, "frac": ach / mufu_peak,
+                "peak_kind": f"MUFU ex2: 16 per clock per SM x {sms} SMs x {max_mhz:.0f} MHz",
+                "traffic": None, "algorithmic_ops": n_exp, "hbm": dict(roof)}
+        if clk.get("sm_mhz"):
+            roof["frac_at_sampled_clock"] = ach / (16 * sms * float(clk["sm_mhz"]) * 1e-3)
     if link is not None and dom == "step":
         hp = h2d_peak(dev, stream)
         roof.update(bound="h2d", peak=hp, peak_kind="measured pinned H2D (256 MiB copy)",
