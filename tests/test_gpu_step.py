@@ -229,28 +229,30 @@ def test_step_failure_injection(kvm):
     assert_storage_close(got, ref, "bf16", "after recovery")
 
 
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
 @pytest.mark.parametrize("repo_host", [False, True], ids=["repo-device", "repo-host-pull-no-raw-copy"])
-def test_step_bounded_delta_rerope(kvm, repo_host):
+def test_step_bounded_delta_rerope(kvm, repo_host, dt):
     """Bounded delta re-RoPE (KVMem §4.4): hits whose slot moved are rotated in
     place by the position change at most once in a row, then rebuilt from raw K;
     every page is compared with the oracle's own pool that applies the same
-    actions (delta rotation of its stored page, or RoPE of raw K)."""
+    actions (delta rotation of its stored page, or RoPE of raw K).  Both page
+    types: bf16, and e4m3 rotated in place from its 8-bit values."""
     from paged_kv_cache_meank_gb300 import workload
-    wl = MID
+    wl = MID.with_(kv_dtype=dt)
     limit = 1
     N_max = 300
     ws = workload.make_workspace(wl, seed=61, n_blocks=N_max, with_q=False)
-    raw_np, v_np = to_np(ws.raw_k, "bf16"), to_np(ws.v, "bf16")
-    kp = prefill_k_pages(raw_np, "bf16", wl.rope_theta)
+    raw_np, v_np = to_np(ws.raw_k, dt), to_np(ws.v, dt)
+    kp = prefill_k_pages(raw_np, dt, wl.rope_theta)
     cfg = kvm.config_for(wl, max_blocks=N_max, pool_pages=wl.view_blocks + 6,
                          repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
                          h2d_mode=1, delta_rerope_limit=limit)
     ctx = kvm.Context(cfg)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
-    raw_d = torch.empty(ctx.block_shape(N_max), dtype=torch.bfloat16, device="cuda")
-    ctx.build_index(from_np(kp, "bf16"), 0, N_max, index, raw_d)
+    raw_d = torch.empty(ctx.block_shape(N_max), dtype=ctx.kv_dtype, device="cuda")
+    ctx.build_index(from_np(kp, dt), 0, N_max, index, raw_d)
     ctx.sync()
-    v_d = from_np(v_np, "bf16")
+    v_d = from_np(v_np, dt)
     if repo_host:
         raw_repo = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
         raw_repo.copy_(raw_d)
@@ -259,14 +261,14 @@ def test_step_bounded_delta_rerope(kvm, repo_host):
     else:
         raw_repo, v_repo = raw_d, v_d
     P = cfg.pool_pages
-    pool_k = torch.zeros(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
+    pool_k = torch.zeros(ctx.block_shape(P), dtype=ctx.kv_dtype, device="cuda")
     pool_v = torch.zeros_like(pool_k)
     pt = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
     scores = torch.empty(N_max, device="cuda")
     sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
     ctx.bind(index=index, raw_k=raw_repo, v=v_repo, pool_k=pool_k, pool_v=pool_v,
              pool_raw_k=None, page_table=pt, scores=scores, sel_ids=sel)
-    raw_ref = to_np(raw_d, "bf16")          # the repository's raw K, as the GPU stored it
+    raw_ref = to_np(raw_d, dt)          # the repository's raw K, as the GPU stored it
     g = torch.Generator().manual_seed(62)
     u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
     qs = [workload.make_queries(wl, g, "cpu", u[i % 3]) for i in range(6)]
@@ -285,15 +287,15 @@ def test_step_bounded_delta_rerope(kvm, repo_host):
         for j, (p, a) in enumerate(zip(page, act)):
             if a in ("miss", "rebuild"):
                 c, s = ora.cos_sin_f32(ora.slot_positions(j + 1)[j], wl.head_dim, wl.rope_theta)
-                ora_pool[p] = ora.round_to(ora.rope_f32(ora.as_f32(raw_ref[g_sel[j]], "bf16"), c, s),
-                                           "bf16")
+                ora_pool[p] = ora.round_to(ora.rope_f32(ora.as_f32(raw_ref[g_sel[j]], dt), c, s),
+                                           dt)
             elif a == "delta":
-                ora_pool[p] = ora.delta_rerope_k(ora_pool[p][None], "bf16", j * 32 - prev_bp[p],
+                ora_pool[p] = ora.delta_rerope_k(ora_pool[p][None], dt, j * 32 - prev_bp[p],
                                                  wl.rope_theta)[0]
         n_delta += act.count("delta")
         n_rebuild += act.count("rebuild")
-        got = to_np(pool_k, "bf16")
+        got = to_np(pool_k, dt)
         for j, p in enumerate(page):
-            assert_storage_close(got[p][None], ora_pool[p][None], "bf16", f"step {step} slot {j}")
-        assert np.array_equal(to_np(pool_v, "bf16")[page], v_np[g_sel])
+            assert_storage_close(got[p][None], ora_pool[p][None], dt, f"step {step} slot {j}")
+        assert np.array_equal(to_np(pool_v, dt)[page], v_np[g_sel])
     assert n_delta > 0 and n_rebuild > 0      # both branches of the bound were taken
