@@ -578,7 +578,7 @@ def bench_ours(args, wl, world, rank, local, dist):
     if not args.no_e2e:
         out["e2e"] = bench_e2e(args, step, dev, stream, world, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl, step, args.cpu_layers)
+        out["cpu_baseline"] = cpu_baseline(wl, step, args.cpu_layers or 3)
     return out
 
 
@@ -739,12 +739,14 @@ def cpu_baseline(wl, step, layers):
 
 def bench_reference(args, wl, world, rank):
     """The CPU oracle as the reference arm: each step is the oracle's recall step
-    on a bounded slice (args.cpu_layers layers) of the same workload, scaled to
-    the whole step."""
+    on a bounded slice (args.cpu_layers layers, 1 unless given, about 4 s at
+    256K on 16 cores, so that warm-up and timed steps together stay within a
+    few minutes) of the same workload, scaled to the whole step."""
     if rank != 0:
         return None
+    layers = args.cpu_layers if args.cpu_layers else 1
     gen_dev = "cpu"
-    ws = workload.make_workspace(wl.with_(n_layers=args.cpu_layers), seed=args.seed,
+    ws = workload.make_workspace(wl.with_(n_layers=layers), seed=args.seed,
                                  device=gen_dev)
     import oracle.kvmem as ora
     raw = _np_bits(ws.raw_k)
@@ -756,16 +758,16 @@ def bench_reference(args, wl, world, rank):
         kp32[i] = ora.rope_f32(r32[i], c, s)
     kp = ora.round_to(kp32, wl.kv_dtype)
     vv, qq = _np_bits(ws.v), _np_bits(ws.q)
-    sub = wl.with_(n_layers=args.cpu_layers)
+    sub = wl.with_(n_layers=layers)
     for _ in range(args.warmup if args.warmup < 2 else 1):
-        _oracle_step_slice(sub, kp, vv, qq, args.cpu_layers)
+        _oracle_step_slice(sub, kp, vv, qq, layers)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step_slice(sub, kp, vv, qq, args.cpu_layers)
+        _oracle_step_slice(sub, kp, vv, qq, layers)
         times.append(time.perf_counter() - t0)
     dt = float(np.mean(times))
-    full = dt * wl.n_layers / args.cpu_layers
+    full = dt * wl.n_layers / layers
     val = wl.n_blocks / full
     return {
         "metric": METRIC, "value": val, "unit": "scored blocks/s", "n_gpus": world,
@@ -775,7 +777,7 @@ def bench_reference(args, wl, world, rank):
         "config": workload_config(wl, world),
         "cpu_baseline": {"value": val, "unit": "scored blocks/s", "cores": os.cpu_count(),
                          "kind": "oracle",
-                         "sample": f"each step restricted to {args.cpu_layers} of "
+                         "sample": f"each step restricted to {layers} of "
                                    f"{wl.n_layers} layers, scaled to the whole step"},
         "e2e": {"value": val, "unit": "scored blocks/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -792,7 +794,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-layers", type=int, default=3)
+    ap.add_argument("--cpu-layers", type=int, default=0,
+                    help="layers of the oracle sample (default: 3 for cpu_baseline, "
+                         "1 per step of --impl reference)")
     ap.add_argument("--score-variant", type=int, default=0,
                     help="0: tensor-core scoring where supported, 1: CUDA cores")
     ap.add_argument("--h2d-mode", type=int, default=1,
