@@ -78,10 +78,13 @@ def unit_vectors(n: int, d: int, gen, device) -> torch.Tensor:
 
 
 def planted_blocks(wl: Workload, n_blocks: int, gen) -> torch.Tensor:
+    # candidates lie between the sink and the recent blocks; a history shorter
+    # than the reserved blocks has none
     lo, hi = wl.sink_blocks, n_blocks - wl.recent_blocks
+    span = max(0, hi - lo)
     n = wl.n_planted if wl.n_planted > 0 else int(round(wl.planted_frac * n_blocks))
-    n = max(0, min(n, hi - lo))
-    perm = torch.randperm(hi - lo, generator=gen, device=gen.device)[:n] + lo
+    n = max(0, min(n, span))
+    perm = torch.randperm(span, generator=gen, device=gen.device)[:n] + lo
     return torch.sort(perm).values.to(torch.int64)
 
 

@@ -28,3 +28,15 @@ def test_tiny_workspace_recall():
     assert np.array_equal(out["view_v"], to_np(ws.v, wl.kv_dtype)[sel])
     pos = ora.slot_positions(len(sel))
     assert pos.min() == 0 and pos.max() == 415
+
+
+def test_history_shorter_than_reserved_blocks():
+    """A history shorter than sink + recent has no candidate block to plant:
+    the generator returns no planted ids and still draws K, V and queries."""
+    wl = configs.TINY.with_(n_blocks=3, sink_blocks=1, recent_blocks=4, view_blocks=13)
+    ws = workload.make_workspace(wl, seed=0)
+    assert ws.planted.numel() == 0
+    assert tuple(ws.raw_k.shape) == (3, wl.n_layers, wl.n_kv_heads, 32, wl.head_dim)
+    assert ws.q.shape[1] == wl.n_queries
+    ws2 = workload.make_index_direct(wl.with_(n_blocks=5), seed=0)
+    assert ws2.planted.numel() == 0
