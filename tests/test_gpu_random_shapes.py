@@ -58,7 +58,7 @@ def _cases(seed: int, n_short: int, n_long: int):
     return out
 
 
-CASES = _cases(20261202, n_short=14, n_long=2)
+CASES = _cases(20261202, n_short=30, n_long=4)
 
 
 @pytest.fixture(scope="module")
@@ -142,3 +142,63 @@ def test_random_shape_recall(kvm, case):
     assert_storage_close(to_np(kp_out, wl.kv_dtype)[perm], ref_k, wl.kv_dtype,
                          wl.name + " view K")
     assert np.array_equal(to_np(vp_out, wl.kv_dtype)[perm], to_np(ws.v, wl.kv_dtype)[ids])
+
+
+def _step_cases(seed: int, n: int):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        d = int(rng.choice([64, 128]))
+        G = int(rng.choice([1, 2, 4]))
+        r = int(rng.choice([1, 2, 3, 6]))
+        L = int(rng.integers(1, 4))
+        kv = str(rng.choice(["f32", "bf16", "e4m3"]))
+        idx = str(rng.choice(["f32", "bf16", "bf16"]))
+        qd = str(rng.choice(["f32", "bf16", "bf16"]))
+        S = int(rng.integers(0, 5))
+        W = int(rng.integers(0, 9))
+        V = S + W + int(rng.integers(1, 80))
+        n_cap = max(2, min(1500, 20_000_000 // (L * G * 32 * d)))
+        ns = [int(rng.integers(1, n_cap))]
+        for _ in range(3):   # the history grows, or shrinks (possibly below V)
+            ns.append(int(np.clip(ns[-1] + rng.integers(-ns[-1] // 2 - 1, 200), 1, n_cap)))
+        repo_host = bool(rng.integers(0, 2))
+        h2d_mode = int(rng.integers(0, 2)) if repo_host else 0
+        index_host = bool(rng.integers(0, 2))
+        spill = int(rng.integers(0, 2)) if index_host else 0
+        q_order = [int(x) for x in rng.integers(0, 3, size=len(ns))]
+        wl = configs.Workload(
+            name=(f"steps{i}-L{L}G{G}r{r}d{d}-{kv}-{idx}-{qd}-S{S}W{W}V{V}-"
+                  f"N{'_'.join(map(str, ns))}-{'host' if repo_host else 'dev'}{h2d_mode}"
+                  f"-{'hidx' if index_host else 'didx'}{spill}"),
+            n_layers=L, n_kv_heads=G, n_q_heads=G * r, head_dim=d,
+            rope_theta=float(rng.choice([1e4, 1e6])), kv_dtype=kv, index_dtype=idx,
+            q_dtype=qd, n_blocks=max(ns), n_queries=int(rng.integers(1, min(24, 256 // r) + 1)),
+            sink_blocks=S, recent_blocks=W, view_blocks=V, planted_frac=0.03,
+            k_std=1.0 / d ** 0.5)
+        out.append((wl, ns, repo_host, h2d_mode, index_host, spill, q_order,
+                    int(rng.integers(0, 1 << 30))))
+    return out
+
+
+STEP_CASES = _step_cases(20261203, 20)
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: c[0].name)
+def test_random_shape_steps(kvm, case):
+    """kvm_step over four steps on a random shape: scores, selection, the
+    oracle's delta working set applied to the GPU's selection (page table,
+    hits, misses, re-RoPE count, H2D bytes) and the materialised view."""
+    from paged_kv_cache_meank_gb300 import workload
+    from test_gpu_step import _run_steps
+    wl, ns, repo_host, h2d_mode, index_host, spill, q_order, seed = case
+    g = torch.Generator().manual_seed(seed)
+    u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
+    qs = [workload.make_queries(wl, g, "cpu", u[k]) for k in range(3)]
+    hist = _run_steps(kvm, wl, repo_host, index_host, [qs[k] for k in q_order], ns,
+                      h2d_mode=h2d_mode, index_spill=spill)
+    assert hist[0]["hits"] == 0 and hist[0]["misses"] == min(ns[0], wl.view_blocks)
+    for a in range(1, len(ns)):
+        if q_order[a] == q_order[a - 1] and ns[a] == ns[a - 1]:
+            # the same queries over the same history: nothing moves
+            assert hist[a]["misses"] == 0 and hist[a]["reroped"] == 0
