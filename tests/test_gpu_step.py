@@ -200,10 +200,11 @@ def test_step_failure_injection(kvm):
                                      h2d_mode=0))       # copy-engine transfers can fail
     kp = prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
-    raw_d = torch.empty(ctx.block_shape(200), dtype=torch.bfloat16, device="cuda")
-    ctx.build_index(from_np(kp, "bf16"), 0, 200, index, raw_d)
-    raw_h = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
-    raw_h.copy_(raw_d)
+    ctx.build_index(from_np(kp, "bf16"), 0, 200, index, None)
+    # the host repository holds the oracle's raw K of the same prefill pages
+    raw_ref = ora.raw_k(kp, "bf16", 0, wl.rope_theta)
+    raw_h = torch.empty(ctx.block_shape(200), dtype=torch.bfloat16, pin_memory=True)
+    raw_h.copy_(from_np(raw_ref, "bf16"))
     v_h = ws.v.pin_memory()
     P = ctx.cfg.pool_pages
     pool_k = torch.zeros(ctx.block_shape(P), dtype=torch.bfloat16, device="cuda")
@@ -224,7 +225,7 @@ def test_step_failure_injection(kvm):
         st = ctx.step(q, wl.n_queries, 200)   # recovers: the pool starts empty again
         ctx.sync()
         assert st["misses"] == wl.view_blocks
-    ref = ora.view_k(to_np(raw_d, "bf16")[sel.cpu().numpy()], "bf16", wl.rope_theta)
+    ref = ora.view_k(raw_ref[sel.cpu().numpy()], "bf16", wl.rope_theta)
     got = to_np(pool_k, "bf16")[pt.cpu().numpy()]
     assert_storage_close(got, ref, "bf16", "after recovery")
 
@@ -249,9 +250,11 @@ def test_step_bounded_delta_rerope(kvm, repo_host, dt):
                          h2d_mode=1, delta_rerope_limit=limit)
     ctx = kvm.Context(cfg)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
-    raw_d = torch.empty(ctx.block_shape(N_max), dtype=ctx.kv_dtype, device="cuda")
-    ctx.build_index(from_np(kp, dt), 0, N_max, index, raw_d)
+    ctx.build_index(from_np(kp, dt), 0, N_max, index, None)
     ctx.sync()
+    # the repository holds the oracle's raw K of the same prefill pages
+    raw_ref = ora.raw_k(kp, dt, 0, wl.rope_theta)
+    raw_d = from_np(raw_ref, dt)
     v_d = from_np(v_np, dt)
     if repo_host:
         raw_repo = torch.empty(raw_d.shape, dtype=raw_d.dtype, pin_memory=True)
@@ -268,7 +271,6 @@ def test_step_bounded_delta_rerope(kvm, repo_host, dt):
     sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
     ctx.bind(index=index, raw_k=raw_repo, v=v_repo, pool_k=pool_k, pool_v=pool_v,
              pool_raw_k=None, page_table=pt, scores=scores, sel_ids=sel)
-    raw_ref = to_np(raw_d, dt)          # the repository's raw K, as the GPU stored it
     g = torch.Generator().manual_seed(62)
     u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
     qs = [workload.make_queries(wl, g, "cpu", u[i % 3]) for i in range(6)]
