@@ -340,7 +340,9 @@ kvm_status kvm_tier_destroy(kvm_tier *tier);
  *          KVM_ERR_CAPACITY with a message, before any work is enqueued.
  * Set-up:  the first call on each device looks up the array's device address
  *          (cudaGetSymbolAddress) with that device current; make that first
- *          call before any stream capture.
+ *          call before any stream capture.  The address belongs to the
+ *          device's context and is kept for the life of the process, so do
+ *          not call this entry point on a device after cudaDeviceReset of it.
  * Sharing: every call on a device uses the same array.  Calls that overlap on
  *          the GPU (unordered streams or threads) race on it; order them.
  *          The array keeps the last call's contents; a call never reads

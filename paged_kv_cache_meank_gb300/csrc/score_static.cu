@@ -39,7 +39,8 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // The device address of g_scratch on the current device.  In host code the
 // name g_scratch is only a host-side stand-in, so the address is looked up
-// once per device with that device current and then reused.
+// once per device with that device current and then reused for the life of
+// the process (a cudaDeviceReset of that device would leave it stale).
 kvm_status scratch_for_current_device(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
