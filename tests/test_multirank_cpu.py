@@ -54,3 +54,17 @@ def test_reference_arm_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_one_core_baseline_child():
+    """The one-core oracle baseline runs in a child process limited to one BLAS
+    thread and reports a positive throughput for one core; an unknown workload
+    is reported as unavailable instead of failing the bench."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_meank_gb300 import configs
+    d = bench.cpu_baseline_one_core(configs.TINY, 0, 2)
+    assert d["cores"] == 1 and d["value"] > 0, d
+    assert "2 of 2 layers" in d["sample"]
+    bad = bench.cpu_baseline_one_core(configs.TINY.with_(name="no-such-workload"), 0, 1)
+    assert bad["value"] is None and bad["unavailable"]
