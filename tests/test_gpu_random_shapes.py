@@ -20,6 +20,7 @@ from gpu_helpers import (assert_meank_close, assert_scores_close, assert_storage
                          check_selection, from_np, to_np)
 from paged_kv_cache_meank_gb300 import configs
 from recall_ref import prefill_k_pages
+from step_helpers import run_steps
 
 pytestmark = pytest.mark.gpu
 
@@ -190,12 +191,11 @@ def test_random_shape_steps(kvm, case):
     oracle's delta working set applied to the GPU's selection (page table,
     hits, misses, re-RoPE count, H2D bytes) and the materialised view."""
     from paged_kv_cache_meank_gb300 import workload
-    from test_gpu_step import _run_steps
     wl, ns, repo_host, h2d_mode, index_host, spill, q_order, seed = case
     g = torch.Generator().manual_seed(seed)
     u = workload.unit_vectors(3, wl.head_dim, g, "cpu")
     qs = [workload.make_queries(wl, g, "cpu", u[k]) for k in range(3)]
-    hist = _run_steps(kvm, wl, repo_host, index_host, [qs[k] for k in q_order], ns,
+    hist = run_steps(kvm, wl, repo_host, index_host, [qs[k] for k in q_order], ns,
                       h2d_mode=h2d_mode, index_spill=spill)
     assert hist[0]["hits"] == 0 and hist[0]["misses"] == min(ns[0], wl.view_blocks)
     for a in range(1, len(ns)):
