@@ -96,9 +96,13 @@ class Clocks:
         except Exception:
             self.proc = None
 
+    @staticmethod
+    def _none(why):
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": why}
+
     def stop(self):
         if self.proc is None:
-            return None
+            return self._none("nvidia-smi could not be started")
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -115,7 +119,7 @@ class Clocks:
             except ValueError:
                 continue
         if not rows:
-            return None
+            return self._none("no sample inside the timed region (shorter than the 50 ms period)")
         dev = os.environ.get("CUDA_VISIBLE_DEVICES", "")
         if dev.isdigit() and any(r[0] == int(dev) for r in rows):
             rows = [r for r in rows if r[0] == int(dev)]
@@ -535,10 +539,15 @@ def bench_ours(args, wl, world, rank, local, dist):
         max_mhz = float(clk.get("sm_max_mhz") or 2070.0)
         ach = n_exp / (parts[dom] * 1e-3) / 1e9
         mufu_peak = 16 * sms * max_mhz * 1e-3
+        hbm = dict(roof)
+        if hbm.get("traffic"):
+            hbm["traffic_note"] = ("both exact passes read the index (2 x algorithmic_bytes); "
+                                   "pass 2 writes and the reduce reads 4 B of partial "
+                                   "relevance per (layer, kv head, block)")
         roof = {"bound": "alu", "kernel": dom, "unit": "Gex2/s", "achieved": ach,
                 "peak": mufu_peak, "frac": ach / mufu_peak,
                 "peak_kind": f"MUFU ex2: 16 per clock per SM x {sms} SMs x {max_mhz:.0f} MHz",
-                "traffic": None, "algorithmic_ops": n_exp, "hbm": dict(roof)}
+                "traffic": None, "algorithmic_ops": n_exp, "hbm": hbm}
         if clk.get("sm_mhz"):
             roof["frac_at_sampled_clock"] = ach / (16 * sms * float(clk["sm_mhz"]) * 1e-3)
     if link is not None and dom == "step":
@@ -616,9 +625,13 @@ def _traffic_from_profile(workload_name, kernel):
             d = json.load(f).get(workload_name, {}).get(kernel)
         if not d:
             return None
-        with open(os.path.join(ROOT, d["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != d["sha256_16"]:
-                return None   # the kernel changed since the counters were taken
+        # one source file, or a list of them (a part made of several kernels)
+        srcs = d["source"] if isinstance(d["source"], list) else [d["source"]]
+        shas = d["sha256_16"] if isinstance(d["sha256_16"], list) else [d["sha256_16"]]
+        for src, sha in zip(srcs, shas, strict=True):
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest()[:16] != sha:
+                    return None   # a kernel changed since the counters were taken
         return d["bytes"]
     except Exception:
         return None
