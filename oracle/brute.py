@@ -75,3 +75,16 @@ def select(R, sink, recent, view_blocks):
     k = view_blocks - len(reserved)
     order = sorted((b for b in range(N) if b not in reserved), key=lambda b: (-R[b], b))
     return sorted(reserved | set(order[:k]))
+
+
+def kth_score(R, sink, recent, view_blocks):
+    """The selection threshold by exhaustive ranking: the score of the k-th
+    candidate when every candidate is sorted by (score desc, id asc); None when
+    every block is selected."""
+    N = len(R)
+    if N <= view_blocks:
+        return None
+    reserved = set(range(sink)) | set(range(N - recent, N))
+    k = view_blocks - len(reserved)
+    order = sorted((b for b in range(N) if b not in reserved), key=lambda b: (-R[b], b))
+    return R[order[k - 1]]

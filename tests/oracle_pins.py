@@ -339,6 +339,37 @@ def pin_select_special(o):
     assert sel.tolist() == [0, 47, 48, 49]
 
 
+def pin_kth_boundary_golden(o):
+    """The threshold T of the parity rule's near-tie band on hand-worked cases:
+    a tie at the k-th place, reserved blocks with the largest scores, k = 1, no
+    sink blocks, and a budget that covers every block."""
+    for case in _load("selector_toys.json")["kth_cases"]:
+        T = o.kth_boundary(np.array(case["R"]), case["S"], case["W"], case["V"])
+        want = float(case["T"])
+        assert T == want, (case["name"], T, want)
+
+
+def pin_kth_boundary_brute(o):
+    """T equals the k-th score of an exhaustive (score desc, id asc) ranking of
+    the candidates, and every selected candidate scores at least T, on random
+    small cases with many ties."""
+    rng = np.random.default_rng(21)
+    for trial in range(60):
+        N = int(rng.integers(1, 40))
+        S, W = int(rng.integers(0, 4)), int(rng.integers(0, 5))
+        V = int(rng.integers(S + W + 1, S + W + 12))
+        R = np.round(rng.random(N), 1)
+        T = o.kth_boundary(R, S, W, V)
+        Tb = brute.kth_score(list(R), S, W, V)
+        if Tb is None:
+            assert T == -np.inf, (trial, T)
+            continue
+        assert T == Tb, (trial, T, Tb)
+        reserved = set(range(S)) | set(range(N - W, N))
+        chosen = set(o.select_blocks(R, S, W, V).tolist()) - reserved
+        assert min(R[b] for b in chosen) == T, trial
+
+
 # ---------------------------------------------------------------- execution view
 
 def pin_view_roundtrip(o):

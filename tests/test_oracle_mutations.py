@@ -189,6 +189,25 @@ def _e4m3_no_saturation(x):
 _ORIG_E4M3 = ora.f32_to_e4m3
 
 
+def _kth_off_by_one(R, sink, recent, view_blocks):
+    N = len(R)
+    if N <= view_blocks:
+        return -np.inf
+    res = set(range(min(sink, N))) | set(range(max(N - recent, 0), N))
+    k = view_blocks - len(res)
+    cand = np.array([R[b] for b in range(N) if b not in res])
+    return float(np.sort(cand)[::-1][k])
+
+
+def _kth_counts_reserved(R, sink, recent, view_blocks):
+    N = len(R)
+    if N <= view_blocks:
+        return -np.inf
+    res = set(range(min(sink, N))) | set(range(max(N - recent, 0), N))
+    k = view_blocks - len(res)
+    return float(np.sort(np.asarray(R, dtype=np.float64))[::-1][k - 1])
+
+
 MUTANTS = {
     "e4m3 ties away from zero": ("f32_to_e4m3", _e4m3_ties_away),
     "e4m3 overflows to NaN instead of saturating": ("f32_to_e4m3", _e4m3_no_saturation),
@@ -213,6 +232,8 @@ MUTANTS = {
     "bf16 by truncation": ("f32_to_bf16", _f32_to_bf16_truncate),
     "tiled partition sum not rescaled": ("block_relevance_tiled", _tiled_no_rescale),
     "free pages taken in descending order": ("residency_step", _residency_descending),
+    "selection threshold one place too far": ("kth_boundary", _kth_off_by_one),
+    "selection threshold ranks the reserved blocks": ("kth_boundary", _kth_counts_reserved),
 }
 
 
