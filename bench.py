@@ -202,6 +202,46 @@ class Step:
     def cpu_sample(self, layers):
         return cpu_sample(self.wl, self.k_pages, self.v, self.q, layers)
 
+    def time_recall(self, args, dev, dist):
+        """kvm_step on this HBM-resident workspace (the index the timed steps
+        built, raw K / V as the repository): scoring, selection, residency diff
+        and assembly of every selected block from the repository into the page
+        pool, timed from queries ready to page table written.  Every step starts
+        from an empty pool, so all view slots are misses."""
+        wl = self.wl
+        self.page_table = torch.empty(wl.view_blocks, dtype=torch.int32, device=self.dev)
+        self.ctx.bind(index=self.index, raw_k=self.raw, v=self.v, pool_k=self.pool_k,
+                      pool_v=self.pool_v, page_table=self.page_table, scores=self.scores,
+                      sel_ids=self.sel)
+        outer = self
+
+        class Recall:
+            parts = ["step"]
+            stats = []
+
+            def run(self, ev=None):
+                outer.ctx.reset_pool()
+                if ev:
+                    ev[0].record(outer.stream)
+                st = outer.ctx.step(outer.q, wl.n_queries, wl.n_blocks, stream=outer.stream)
+                if ev:
+                    ev[1].record(outer.stream)
+                self.stats.append(st)
+
+        r = Recall()
+        K = args.extra_steps
+        ms, parts, n_launches, clk = time_steps(r, K, args.warmup, dev, self.stream, dist)
+        st = r.stats[-K:]
+        return {"ms": parts["step"], "steps": K, "gpu_launches": n_launches, "clocks": clk,
+                "definition": "kvm_step on the HBM-resident workspace, queries ready to page "
+                              "table written (CUDA events; includes the host's residency diff "
+                              "between the selection and the assembly)",
+                "misses": float(np.mean([x["misses"] for x in st])),
+                "hits": float(np.mean([x["hits"] for x in st]))}
+
+    def close(self):
+        self.ctx.close()
+
 
 class ScoreStep:
     """Scoring + selection only, over a Mean-K index drawn directly in HBM (the
@@ -257,6 +297,9 @@ class ScoreStep:
             f"Eq. (10) + selection on {layers} of {wl.n_layers} layers and {nb} of " \
             f"{wl.n_blocks} blocks"
 
+    def close(self):
+        self.ctx.close()
+
 
 def build_host_workspace(kvm, wl, seed, device, stream, ctx, n_blocks, index_on_host,
                          keep_pages_from=None):
@@ -298,12 +341,9 @@ class HostStep:
     def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0, index_spill=1):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
+        self.score_variant, self.h2d_mode = score_variant, h2d_mode
         self.index_spill = index_spill if wl.index_loc == "host" else 0
-        cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
-                             index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
-                             else kvm.KVM_DEVICE, h2d_batch_blocks=256,
-                             score_variant=score_variant, h2d_mode=h2d_mode,
-                             index_spill=self.index_spill)
+        cfg = self._config(self.index_spill)
         self.ctx = kvm.Context(cfg, device=device, stream=stream)
         (self.raw_h, self.v_h, self.index, self.planted, u, _, _) = build_host_workspace(
             kvm, wl, seed, device, stream, self.ctx, wl.n_blocks, wl.index_loc == "host")
@@ -316,10 +356,41 @@ class HostStep:
         self.page_table = torch.empty(V, dtype=torch.int32, device=device)
         self.scores = torch.empty(wl.n_blocks, dtype=torch.float32, device=device)
         self.sel = torch.empty(V, dtype=torch.int32, device=device)
+        self._bind()
+        self.stats = []
+
+    def _config(self, spill):
+        kvm, wl = self.kvm, self.wl
+        return kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
+                              index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
+                              else kvm.KVM_DEVICE, h2d_batch_blocks=256,
+                              score_variant=self.score_variant, h2d_mode=self.h2d_mode,
+                              index_spill=spill)
+
+    def _bind(self):
         self.ctx.bind(index=self.index, raw_k=self.raw_h, v=self.v_h, pool_k=self.pool_k,
                       pool_v=self.pool_v, pool_raw_k=self.pool_raw, page_table=self.page_table,
                       scores=self.scores, sel_ids=self.sel)
-        self.stats = []
+
+    def respill(self, spill):
+        """The same workspace under a new context with another index_spill
+        setting; this step's context is closed and the returned step owns the
+        host buffers."""
+        import copy
+        other = copy.copy(self)
+        self.ctx.close()
+        other.index_spill = spill if self.wl.index_loc == "host" else 0
+        other.ctx = self.kvm.Context(other._config(other.index_spill), device=self.dev,
+                                     stream=self.stream)
+        other._bind()
+        other.stats = []
+        return other
+
+    def close(self):
+        from paged_kv_cache_meank_gb300 import hostmem
+        self.ctx.close()
+        for t in (self.raw_h, self.v_h, self.index):
+            hostmem.release(t)
 
     def inputs(self):
         return {"q": self.q}
@@ -424,6 +495,12 @@ class ChurnStep:
         """Host-to-device bytes of one step: the missed blocks' raw K and V."""
         return float(np.mean([s["h2d_bytes"] for s in self.stats[-self.wl.steps:]]))
 
+    def close(self):
+        from paged_kv_cache_meank_gb300 import hostmem
+        self.ctx.close()
+        for t in (self.raw_h, self.v_h):
+            hostmem.release(t)
+
     def cpu_sample(self, layers):
         wl = self.wl
         return oracle_select_view_sample(wl.with_(n_blocks=wl.n_blocks + wl.append_blocks),
@@ -477,20 +554,15 @@ def workload_config(wl, world):
             "parallelism": f"replicas{world}", "l2": "inputs larger than L2, no flush"}
 
 
-def bench_ours(args, wl, world, rank, local, dist):
+def time_steps(step, K, warmup, dev, stream, dist):
+    """W untimed warm-up steps, then K timed steps bracketed by a barrier and a
+    synchronisation, with CUDA events per part and nvidia-smi clock samples.
+    Returns (ms per step, max over ranks; mean ms per part; kernels this library
+    launched in the timed region; clock record)."""
     import paged_kv_cache_meank_gb300 as kvm_lib
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(device=dev)
-    kind = STEP_KIND.get(wl.name.split("@")[0], Step)
-    extra = {"index_spill": args.index_spill} if kind is HostStep else {}
-    step = kind(wl, args.seed + rank, dev, stream, score_variant=args.score_variant,
-                h2d_mode=args.h2d_mode, **extra)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step.run()
     torch.cuda.synchronize(dev)
-
-    K = args.steps
     npart = len(step.parts)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(npart + 1)] for _ in range(K)]
     clocks = Clocks()
@@ -511,9 +583,14 @@ def bench_ours(args, wl, world, rank, local, dist):
         dist.barrier()
     clk = clocks.stop()
     total_ms = max_over_ranks(dist, t0.elapsed_time(t1), dev)
-    ms = total_ms / K
     parts = {p: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs]))
              for i, p in enumerate(step.parts)}
+    return total_ms / K, parts, n_launches, clk
+
+
+def summarize(wl, step, ms, parts, clk, dev, stream):
+    """Throughput, per-part figures and the roofline of the dominant part for a
+    timed workload.  Returns (components, roofline)."""
     ab = algorithmic_bytes(wl)
     peak, peak_kind = _peaks()
     link = getattr(step, "link_bytes", None)
@@ -541,9 +618,7 @@ def bench_ours(args, wl, world, rank, local, dist):
         mufu_peak = 16 * sms * max_mhz * 1e-3
         hbm = dict(roof)
         if hbm.get("traffic"):
-            hbm["traffic_note"] = ("both exact passes read the index (2 x algorithmic_bytes); "
-                                   "pass 2 writes and the reduce reads 4 B of partial "
-                                   "relevance per (layer, kv head, block)")
+            hbm["traffic_note"] = "DRAM bytes per scoring call, from the committed ncu summary"
         roof = {"bound": "alu", "kernel": dom, "unit": "Gex2/s", "achieved": ach,
                 "peak": mufu_peak, "frac": ach / mufu_peak,
                 "peak_kind": f"MUFU ex2: 16 per clock per SM x {sms} SMs x {max_mhz:.0f} MHz",
@@ -554,10 +629,21 @@ def bench_ours(args, wl, world, rank, local, dist):
         hp = h2d_peak(dev, stream)
         roof.update(bound="h2d", peak=hp, peak_kind="measured pinned H2D (256 MiB copy)",
                     frac=kern[dom]["gbs"] / hp, traffic=None)
-    recall_ms = parts.get("step", parts.get("score_select", 0.0) + parts.get("assemble", 0.0))
-    comps = {"recall_ms": recall_ms, **{f"{p}_ms": parts[p] for p in parts}, "kernels": kern}
+    comps = {**{f"{p}_ms": parts[p] for p in parts}, "kernels": kern}
+    if "step" in parts:
+        comps["recall_ms"] = parts["step"]
+        comps["recall_def"] = "kvm_step, queries ready to page table written (CUDA events)"
     if "score_select" in parts:
         comps["index_hbm_gbs"] = kern["score_select"]["gbs"]
+        comps["score_blocks_per_s"] = wl.n_blocks / (parts["score_select"] * 1e-3)
+    if "build" in parts and link is None:
+        # the pages build the index incrementally during prefill, one completed
+        # block at a time; the timed step rebuilds the whole history (a stress
+        # measurement), so the per-block cost is the figure that recurs
+        comps["build_us_per_block"] = parts["build"] * 1e3 / wl.n_blocks
+        comps["build_note"] = ("the timed step rebuilds the index over the whole history; in "
+                               "use it is built incrementally as blocks complete "
+                               "(build_us_per_block per block)")
     if link is None and len(parts) > 1:
         # the whole step against HBM: every part's algorithmic bytes, with the
         # index read twice (the two exact scoring passes), over the step time
@@ -566,9 +652,39 @@ def bench_ours(args, wl, world, rank, local, dist):
     if "assemble" in parts:
         comps["assembly_tokens_per_s"] = wl.view_tokens / (parts["assemble"] * 1e-3)
     if getattr(step, "stats", None):
-        st = step.stats[-K:]
+        st = step.stats[-max(1, len(step.stats) // 2):]
         comps["step_stats"] = {k: float(np.mean([s[k] for s in st]))
                                for k in ("hits", "misses", "reroped", "h2d_bytes", "h2d_copies")}
+    if link is not None:
+        comps["h2d_gbs"] = kern["step"]["gbs"]
+        if roof.get("bound") == "h2d":
+            comps["h2d_peak_gbs"] = roof["peak"]
+            comps["h2d_frac"] = roof["frac"]
+    return comps, roof
+
+
+def make_step(args, wl, seed, dev, stream, **extra):
+    kind = STEP_KIND.get(wl.name.split("@")[0], Step)
+    if kind is HostStep and "index_spill" not in extra:
+        extra["index_spill"] = args.index_spill
+    return kind(wl, seed, dev, stream, score_variant=args.score_variant,
+                h2d_mode=args.h2d_mode, **extra)
+
+
+def bench_ours(args, wl, world, rank, local, dist):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    step = make_step(args, wl, args.seed + rank, dev, stream)
+    K = args.steps
+    ms, parts, n_launches, clk = time_steps(step, K, args.warmup, dev, stream, dist)
+    comps, roof = summarize(wl, step, ms, parts, clk, dev, stream)
+    if isinstance(step, Step):
+        # kvm_step on the same HBM-resident workspace: recall from queries ready
+        # to page table written, every step from an empty page pool
+        comps["recall"] = step.time_recall(args, dev, dist)
+        comps["recall_ms"] = comps["recall"]["ms"]
+        comps["recall_def"] = comps["recall"]["definition"]
     out = {
         "metric": METRIC,
         "value": job_throughput(world, wl.n_blocks, ms),
@@ -579,6 +695,8 @@ def bench_ours(args, wl, world, rank, local, dist):
         "data": "synthetic (seeded N(0,1/128) raw K/V, 2% planted blocks, RoPE-free queries)",
         "config": {**workload_config(wl, world),
                    **({"index_spill": step.index_spill} if hasattr(step, "index_spill") else {})},
+        "value_def": ("history blocks per second over whole steps: Mean-K build of the whole "
+                      "history + Eq. (10) scoring + selection + view assembly"),
         "components": comps,
         "roofline": roof,
         "gpu_launches": n_launches,
@@ -589,8 +707,58 @@ def bench_ours(args, wl, world, rank, local, dist):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         layers = min(wl.n_layers, args.cpu_layers or 3)
         out["cpu_baseline"] = cpu_baseline(wl, step, layers)
-        if kind is Step and wl.name in configs.ALL:
+        if isinstance(step, Step) and wl.name in configs.ALL:
             out["cpu_baseline"]["one_core"] = cpu_baseline_one_core(wl, args.seed, layers)
+    if not args.no_extra and wl.name == configs.W256K.name:
+        step.close()
+        del step
+        out["workloads"] = bench_extra(args, world, rank, dev, stream, dist)
+    return out
+
+
+# The other workloads the default run times in the same process, each with its
+# own warm-up, clock samples and roofline: the 1M-token host-resident step with
+# the index streamed through a bounded staging buffer (and, second, with the
+# index kept in HBM after its first crossing), the 10M-token scoring step and
+# the multi-step churn on its 16-layer slice.
+EXTRA = [("q27x16-1m", {"index_spill": 0}), ("q27x16-1m", {"index_spill": 1}),
+         ("q27-10m-score", {}), ("q27x16-512k-churn", {})]
+
+
+def bench_extra(args, world, rank, dev, stream, dist):
+    import gc
+    out = {}
+    host_share = None
+    for name, extra in EXTRA:
+        wl = configs.ALL[name]
+        t_setup = time.perf_counter()
+        if host_share is not None and name == host_share.wl.name:
+            step = host_share.respill(extra["index_spill"])
+        else:
+            if host_share is not None:
+                host_share.close()
+                host_share = None
+            step = make_step(args, wl, args.seed + rank, dev, stream, **extra)
+        setup_s = time.perf_counter() - t_setup
+        K = wl.steps if isinstance(step, ChurnStep) else args.extra_steps
+        ms, parts, n_launches, clk = time_steps(step, K, args.warmup, dev, stream, dist)
+        comps, roof = summarize(wl, step, ms, parts, clk, dev, stream)
+        key = name + ("" if "index_spill" not in extra else
+                      ("-spill" if extra["index_spill"] else "-bounded"))
+        out[key] = {"value": job_throughput(world, wl.n_blocks, ms), "unit": "scored blocks/s",
+                    "ms_per_step": ms, "steps": K, "warmup": args.warmup,
+                    "config": {**workload_config(wl, world), **extra},
+                    "components": comps, "roofline": roof, "gpu_launches": n_launches,
+                    "clocks": clk, "setup_s": setup_s}
+        if isinstance(step, HostStep):
+            host_share = step
+        else:
+            step.close()
+        del step
+        gc.collect()
+        torch.cuda.empty_cache()
+    if host_share is not None:
+        host_share.close()
     return out
 
 
@@ -869,6 +1037,11 @@ def main():
     ap.add_argument("--one-core-sample", action="store_true",
                     help="internal: time the oracle's sample step once and print it (the "
                          "one-core baseline runs this in a child with one BLAS thread)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the chosen workload (the default 256K run also times the "
+                         "1M, 10M-scoring and churn workloads)")
+    ap.add_argument("--extra-steps", type=int, default=10,
+                    help="timed steps of each extra single-step workload")
     ap.add_argument("--blocks", type=int, default=0,
                     help="override the history length (small cases for profiling)")
     args = ap.parse_args()

@@ -21,6 +21,11 @@
  * leave the context unchanged.  Device-side range checks (block ids, page ids)
  * skip the offending access and raise a sticky device error flag that
  * kvm_sync() reports as KVM_ERR_DEVICE and clears.
+ * One context's calls share its workspace (scoring scratch, step descriptors,
+ * page table) and its host bookkeeping: issue them on one stream, or order
+ * the streams yourself (an event per call).  Two calls of one context that
+ * run at the same time on unordered streams race.  Different contexts are
+ * independent and may run concurrently on different streams and threads.
  *
  * Layouts (row-major, innermost last; B = block_tokens = 32, d = head_dim):
  *   K pages, V pages, raw K, V      [block or page][layer][kv_head][B][d]
@@ -323,26 +328,39 @@ kvm_status kvm_tier_destroy(kvm_tier *tier);
  * kvm_score_select without any device allocation: the paper has no
  * counterpart; this is a deployment convenience.
  *
- * Computes exactly what kvm_score_select computes for a device-resident index
- * (same kernels, same results), but needs no context and no workspace: its
- * scratch is a fixed 32 MiB array in the library's own device memory.  It is
- * meant for callers that cannot allocate device memory -- for example a plugin
- * inside an inference engine whose memory planner already owns the whole
- * device, or a latency-critical caller that cannot afford cudaMalloc/cudaFree,
- * which may synchronise the device.  The call allocates nothing
- * (no cudaMalloc, no cudaFree, no allocating library routine).
+ * Computes what kvm_score_select computes for a device-resident index, with
+ * the same kernels and the same chunking, so scores and selection are bit
+ * for bit those of kvm_score_select on the same inputs.  It needs no context
+ * and no workspace: its scratch is a fixed 32 MiB array in the library's own
+ * device memory.  It is meant for callers that cannot allocate device memory
+ * -- for example a plugin inside an inference engine whose memory planner
+ * already owns the whole device, or a latency-critical caller that cannot
+ * afford cudaMalloc/cudaFree, which may synchronise the device.  The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
  *
- * cfg      host; the shape fields, dtypes, sink/recent/view budget and
- *          max_blocks (the index row stride) are used; index_location must be
- *          KVM_DEVICE.  The other arguments are those of kvm_score_select.
+ * cfg      host; the shape fields, dtypes, sink/recent/view budget,
+ *          candidate_mode, score_variant and max_blocks (the index row
+ *          stride) are used; index_location must be KVM_DEVICE.
+ * index    device memory (checked: KVM_ERR_INVALID_ARG otherwise).
+ * q, scores_out, sel_ids_out
+ *          device memory or pinned host memory (checked as for
+ *          kvm_score_select; pageable memory gives KVM_ERR_INVALID_ARG).
+ *          n_sel_out is a host pointer, as for kvm_score_select.
  * Limit:   the scratch needs about 4 * L * G * n_blocks bytes (plus a little
  *          per query row); calls needing more than 32 MiB return
  *          KVM_ERR_CAPACITY with a message, before any work is enqueued.
- * Set-up:  the first call on each device looks up the array's device address
- *          (cudaGetSymbolAddress) with that device current; make that first
- *          call before any stream capture.  The address belongs to the
- *          device's context and is kept for the life of the process, so do
+ * Set-up:  the first call in each CUDA context (normally: on each device)
+ *          looks up the array's device address (cudaGetSymbolAddress) with
+ *          that context current; make that first call before any stream
+ *          capture.  The address is kept for the life of the process, so do
  *          not call this entry point on a device after cudaDeviceReset of it.
+ * Errors on the device: a bounded wait that gave up inside a tensor-core pass
+ *          raises a flag in the array's error word; the call itself has
+ *          already returned KVM_OK by then.  The word collects the flags of
+ *          every call until kvm_score_select_static_status reads and clears
+ *          it.  A call whose flag was raised left meaningless scores and
+ *          selection (ids stay in range).
  * Sharing: every call on a device uses the same array.  Calls that overlap on
  *          the GPU (unordered streams or threads) race on it; order them.
  *          The array keeps the last call's contents; a call never reads
@@ -355,6 +373,16 @@ kvm_status kvm_tier_destroy(kvm_tier *tier);
 kvm_status kvm_score_select_static(const kvm_config *cfg, const void *q, int32_t n_queries,
                                    const void *index, int64_t n_blocks, float *scores_out,
                                    int32_t *sel_ids_out, int32_t *n_sel_out, kvm_stream stream);
+
+/*
+ * The device errors of kvm_score_select_static calls in the current CUDA
+ * context: waits for `stream` (the stream of those calls), reads the error
+ * word of the fixed array, and clears it.  Returns KVM_OK when no flag was
+ * raised since the last read, KVM_ERR_TIMEOUT when a bounded wait gave up,
+ * KVM_ERR_DEVICE for any other flag, KVM_ERR_CUDA when the word cannot be
+ * read.  Allocates nothing.  Synchronises with `stream`.
+ */
+kvm_status kvm_score_select_static_status(kvm_stream stream);
 
 /* Wait for all work of the context (its internal streams and `stream`) and
  * report a raised device error flag (KVM_ERR_DEVICE), clearing it. */

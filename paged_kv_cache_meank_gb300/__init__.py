@@ -95,6 +95,14 @@ def score_select_static(cfg: KvmConfig, q, n_queries: int, index, n_blocks: int,
     return n_sel.value
 
 
+def score_select_static_status(stream=None) -> None:
+    """kvm_score_select_static_status: waits for ``stream`` and raises
+    KvmError (KVM_ERR_TIMEOUT or KVM_ERR_DEVICE) when a device flag was raised
+    by kvm_score_select_static calls since the last check; the flag is cleared."""
+    check(load().kvm_score_select_static_status(_stream(stream)),
+          "kvm_score_select_static_status")
+
+
 def launch_count() -> int:
     """kvm_launch_count: kernels the library has launched in this process so
     far (the difference across a region counts the kernels it launched)."""

@@ -88,6 +88,7 @@ SIGNATURES = {
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                                ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    "kvm_score_select_static_status": (ctypes.c_int, [ctypes.c_void_p]),
     "kvm_tier_create": (ctypes.c_int, [ctypes.c_int64, ctypes.c_double,
                                        ctypes.POINTER(ctypes.c_void_p)]),
     "kvm_tier_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,

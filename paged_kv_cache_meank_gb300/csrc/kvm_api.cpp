@@ -243,6 +243,11 @@ static kvm_status kernel_ptr(const void *p, const void **out, const char *what) 
     return fail(KVM_ERR_INVALID_ARG,
                 "%s: pageable host memory; use device memory or pinned host memory", what);
 }
+
+int kvm::resolve_kernel_ptr(const void *p, const void **out, const char *what) {
+    return kernel_ptr(p, out, what);
+}
+
 template <typename T>
 static kvm_status kernel_ptr(T *p, T **out, const char *what) {
     const void *q = nullptr;

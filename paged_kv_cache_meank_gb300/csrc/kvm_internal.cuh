@@ -16,6 +16,13 @@ void set_last_error(const std::string &msg);
 // Counts one kernel launch of this library (read by kvm_launch_count).
 void note_launch();
 
+// The address a kernel uses for a caller buffer: device (or managed) memory as
+// is, pinned host memory through its device alias; NULL stays NULL.  Pageable
+// host memory and addresses the GPU cannot use are rejected.  Returns a
+// kvm_status value (KVM_OK, KVM_ERR_INVALID_ARG or KVM_ERR_CUDA) and sets the
+// last-error message.  Defined in kvm_api.cpp.
+int resolve_kernel_ptr(const void *p, const void **out, const char *what);
+
 constexpr int kBlockTokens = 32;
 constexpr int kMaxHalfDim = 64;       // head_dim <= 128
 constexpr int kMaxRows = 256;         // query rows per KV head (M_q * H/G)

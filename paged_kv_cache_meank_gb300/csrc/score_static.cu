@@ -15,12 +15,19 @@
 // call: two calls that overlap on the GPU (different streams, or different
 // host threads without ordering) race on it and produce garbage.  The array
 // keeps whatever the last call left in it.  Every byte a call reads from it is
-// written earlier in the same call: the one part that must start at zero, the
-// histograms of the selection over 16384 blocks or more, is cleared on the
-// call's stream before its first use, and the rest is fully overwritten.
+// written earlier in the same call, except the error word: the one part that
+// must start at zero, the histograms of the selection over 16384 blocks or
+// more, is cleared on the call's stream before its first use, and the rest is
+// fully overwritten.  The error word (the array's first 4 bytes) collects the
+// device error flags of every call until kvm_score_select_static_status reads
+// and clears it.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "kvm.h"
 #include "kvm_internal.cuh"
@@ -31,38 +38,64 @@ constexpr size_t SCRATCH_BYTES = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_ptr[kMaxDevices] = {};
-
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// The device address of g_scratch on the current device.  In host code the
-// name g_scratch is only a host-side stand-in, so the address is looked up
-// once per device with that device current and then reused for the life of
-// the process (a cudaDeviceReset of that device would leave it stale).
-kvm_status scratch_for_current_device(void **out) {
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+
+// cuCtxGetCurrent from the driver, looked up once per process.
+CtxGetCurrent ctx_get_current() {
+    static const CtxGetCurrent fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrent>(p);
+        return static_cast<CtxGetCurrent>(nullptr);
+    }();
+    return fn;
+}
+
+std::mutex g_mu;
+std::vector<std::pair<CUcontext, void *>> g_addr;   // (CUDA context, address of g_scratch)
+
+CUcontext current_ctx() {
+    CUcontext ctx = nullptr;
+    CtxGetCurrent fn = ctx_get_current();
+    if (fn && fn(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    return ctx;
+}
+
+// The device address of g_scratch in the calling thread's current CUDA context
+// (the current device's primary context unless the caller made another one
+// current).  In host code the name g_scratch is only a host-side stand-in, so
+// the address is looked up with cudaGetSymbolAddress the first time a context
+// calls, then reused for the life of the process.  A context destroyed and
+// re-created (cudaDeviceReset) may leave a stale entry behind.
+kvm_status scratch_for_current_context(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
         kvm::set_last_error(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
         return KVM_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        kvm::set_last_error("device ordinal beyond the supported range");
-        return KVM_ERR_INVALID_ARG;
-    }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            kvm::set_last_error(std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-            return KVM_ERR_CUDA;
-        }
-        g_ptr[dev] = p;
+    CUcontext ctx = current_ctx();
+    if (ctx)
+        for (const auto &p : g_addr)
+            if (p.first == ctx) {
+                *out = p.second;
+                return KVM_OK;
+            }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);    // makes the primary context current if none is
+    if (e != cudaSuccess || p == nullptr) {
+        kvm::set_last_error(std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+        return KVM_ERR_CUDA;
     }
-    *out = g_ptr[dev];
+    if (!ctx) ctx = current_ctx();
+    if (ctx) g_addr.emplace_back(ctx, p);
+    *out = p;
     return KVM_OK;
 }
 
@@ -107,9 +140,16 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     sh.gqa = gqa;
     sh.rows = n_queries * gqa;
     sh.index_cap = cfg->max_blocks;
-    const int nch = kvm::score_chunks(sh, n_blocks, kvm::kMaxChunks);
-    sh.chunk_cap = nch;
     sh.variant = cfg->score_variant;
+    // the candidate set and the chunk count exactly as kvm_score_select takes
+    // them, so that both entry points sum in the same order
+    int64_t c0 = 0, c1 = n_blocks;
+    if (cfg->candidate_mode == 1) {
+        c0 = cfg->sink_blocks < n_blocks ? cfg->sink_blocks : n_blocks;
+        c1 = n_blocks - cfg->recent_blocks > c0 ? n_blocks - cfg->recent_blocks : c0;
+    }
+    const int nch = c1 > c0 ? kvm::score_chunks(sh, c1 - c0, kvm::kMaxChunks) : 1;
+    sh.chunk_cap = nch;
 
     const size_t LG = (size_t)sh.L * sh.G;
     const size_t part = up256(LG * nch * sh.rows * sizeof(float));
@@ -126,10 +166,31 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
         return bad(KVM_ERR_CAPACITY, msg);
     }
 
+    // the kernels take device addresses: the index must be device memory (the
+    // tensor-core passes stream it with TMA); q and the outputs may also be
+    // pinned host memory, used through its device alias
+    {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, index) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            return bad(KVM_ERR_INVALID_ARG, "index: device memory required");
+        }
+    }
+    int rs;
+    if ((rs = kvm::resolve_kernel_ptr(q, &q, "q")) != KVM_OK) return (kvm_status)rs;
+    {
+        const void *p = scores_out;
+        if ((rs = kvm::resolve_kernel_ptr(p, &p, "scores_out")) != KVM_OK) return (kvm_status)rs;
+        scores_out = static_cast<float *>(const_cast<void *>(p));
+        p = sel_ids_out;
+        if ((rs = kvm::resolve_kernel_ptr(p, &p, "sel_ids_out")) != KVM_OK) return (kvm_status)rs;
+        sel_ids_out = static_cast<int32_t *>(const_cast<void *>(p));
+    }
+
     void *base = nullptr;
-    kvm_status st = scratch_for_current_device(&base);
+    kvm_status st = scratch_for_current_context(&base);
     if (st != KVM_OK) return st;
-    char *b = static_cast<char *>(base) + 256;   // the first 256 bytes hold an error word
+    char *b = static_cast<char *>(base) + 256;   // the first 256 bytes hold the error word
     kvm::ScoreScratch scr{};
     scr.part_m = reinterpret_cast<float *>(b);
     scr.part_z = reinterpret_cast<float *>(b + part);
@@ -140,11 +201,6 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     scr.err = static_cast<int *>(base);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int64_t c0 = 0, c1 = n_blocks;
-    if (cfg->candidate_mode == 1) {
-        c0 = cfg->sink_blocks < n_blocks ? cfg->sink_blocks : n_blocks;
-        c1 = n_blocks - cfg->recent_blocks > c0 ? n_blocks - cfg->recent_blocks : c0;
-    }
     cudaError_t e = cudaSuccess;
     if ((c1 > c0 &&
          ((e = kvm::launch_score_pass1(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, c0, c1,
@@ -161,4 +217,34 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     }
     if (n_sel_out) *n_sel_out = (int32_t)(n_blocks < cfg->view_blocks ? n_blocks : cfg->view_blocks);
     return KVM_OK;
+}
+
+extern "C" kvm_status kvm_score_select_static_status(kvm_stream stream) {
+    void *base = nullptr;
+    kvm_status st = scratch_for_current_context(&base);
+    if (st != KVM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int flag = 0;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(&flag, base, sizeof(int), cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+        kvm::set_last_error(std::string("reading the error word: ") + cudaGetErrorString(e));
+        return KVM_ERR_CUDA;
+    }
+    if (flag == 0) return KVM_OK;
+    if ((e = cudaMemsetAsync(base, 0, sizeof(int), s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+        kvm::set_last_error(std::string("clearing the error word: ") + cudaGetErrorString(e));
+        return KVM_ERR_CUDA;
+    }
+    char msg[96];
+    if (flag & 4) {
+        snprintf(msg, sizeof msg, "a bounded device wait gave up (flag 0x%x)", flag);
+        kvm::set_last_error(msg);
+        return KVM_ERR_TIMEOUT;
+    }
+    snprintf(msg, sizeof msg, "device check raised flag 0x%x", flag);
+    kvm::set_last_error(msg);
+    return KVM_ERR_DEVICE;
 }
