@@ -1028,7 +1028,8 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=0,
                     help="layers of the oracle sample (default 3)")
     ap.add_argument("--score-variant", type=int, default=0,
-                    help="0: tensor-core scoring where supported, 1: CUDA cores")
+                    help="0: tensor-core scoring where supported, 1: CUDA cores, 2: tensor cores "
+                         "with both passes in one launch")
     ap.add_argument("--h2d-mode", type=int, default=1,
                     help="host-resident repository: 0 copy engine, 1 GPU reads the host memory")
     ap.add_argument("--index-spill", type=int, default=1, choices=[0, 1],

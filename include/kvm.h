@@ -102,7 +102,11 @@ typedef struct {
                                    device-mapped */
     int32_t score_variant;   /* 0: tcgen05 tensor cores for bf16 q/index (d 64 or 128,
                                 <= 256 query rows per KV head), CUDA cores otherwise;
-                                1: CUDA cores always */
+                                1: CUDA cores always;
+                                2: as 0, with both softmax passes over a device index
+                                in one persistent launch (<= 192 query rows per KV
+                                head; the second pass reads each (layer, kv head)
+                                slice again from L2) */
     int32_t delta_rerope_limit; /* kvm_step, hits whose slot moved ([KVMem] §4.4 bounded
                                 delta re-RoPE): 0 = rebuild K from raw K every time;
                                 n > 0 = rotate the page's K in place by the position

@@ -26,6 +26,7 @@ SOURCES = [
     "score.cu",
     "score_tc.cu",
     "score_tc1.cu",
+    "score_fused.cu",
     "score_dispatch.cu",
     "select.cu",
     "assemble.cu",

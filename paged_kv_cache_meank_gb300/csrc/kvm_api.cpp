@@ -51,7 +51,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t elt_bytes(int dt) { return dt == KVM_E4M3 ? 1 : dt == KVM_BF16 ? 2 : 4; }
 
 struct Layout {
-    size_t table, part_m, part_z, row_m, row_invz, partial, stage0, stage1, desc, sel, err, total;
+    size_t table, part_m, part_z, row_m, row_invz, partial, fused, qstage, stage0, stage1, desc,
+        sel, err, total;
+    size_t qstage_bytes;
     size_t stage_bytes;
     int rows_max, chunk_cap;
 };
@@ -86,7 +88,7 @@ bool config_ok(const kvm_config *c, std::string *why) {
         return bad("tile_blocks must be >= 1 for a host-resident index");
     if (c->pool_pages < c->view_blocks) return bad("pool_pages must be >= view_blocks");
     if (c->h2d_batch_blocks < 1) return bad("h2d_batch_blocks must be >= 1");
-    if (c->score_variant != 0 && c->score_variant != 1) return bad("score_variant must be 0 or 1");
+    if (c->score_variant < 0 || c->score_variant > 2) return bad("score_variant must be 0, 1 or 2");
     if (c->h2d_mode != 0 && c->h2d_mode != 1) return bad("h2d_mode must be 0 or 1");
     if (c->delta_rerope_limit < 0) return bad("delta_rerope_limit must be >= 0");
     if (c->candidate_mode != 0 && c->candidate_mode != 1) return bad("candidate_mode must be 0 or 1");
@@ -115,6 +117,14 @@ Layout layout_of(const kvm_config *c) {
     lo.row_m = take(LG * lo.rows_max * sizeof(float));
     lo.row_invz = take(LG * lo.rows_max * sizeof(float));
     lo.partial = take(LG * (size_t)c->max_blocks * sizeof(float));
+    lo.fused = take(kvm::fused_scratch_bytes(lo.rows_max));
+    // queries in host memory are copied here for the one-launch scoring,
+    // whose TMA reads them from device memory
+    lo.qstage_bytes = c->index_location == KVM_DEVICE
+                          ? (size_t)c->n_layers * c->max_queries * c->n_q_heads * c->head_dim *
+                                elt_bytes(c->q_dtype)
+                          : 0;
+    lo.qstage = take(lo.qstage_bytes);
     lo.stage_bytes = 0;
     if (c->index_location == KVM_HOST_PINNED)
         lo.stage_bytes = LG * (size_t)c->tile_blocks * c->head_dim * elt_bytes(c->index_dtype);
@@ -286,6 +296,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->scr.row_m = reinterpret_cast<float *>(c->ws + lo.row_m);
     c->scr.row_invz = reinterpret_cast<float *>(c->ws + lo.row_invz);
     c->scr.partial = reinterpret_cast<float *>(c->ws + lo.partial);
+    kvm::fused_scratch_carve(&c->scr, c->ws + lo.fused, lo.rows_max);
     c->stage[0] = c->ws + lo.stage0;
     c->stage[1] = c->ws + lo.stage1;
     c->desc_dev = reinterpret_cast<kvm::SlotDesc *>(c->ws + lo.desc);
@@ -391,7 +402,24 @@ static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void
                                const void *index, int64_t N, int64_t c0, int64_t c1,
                                float *scores, cudaStream_t s) {
     cudaError_t e;
-    if (c1 > c0) {
+    if (c1 > c0 && kvm::score_fused_supported(c->cfg.q_dtype, c->cfg.index_dtype, sh)) {
+        // both passes in one launch; an injection of kind 3 counts it as two
+        // passes (pass 1, then pass 2)
+        if (!kvm::fused_q_ok(q)) {
+            void *qs = c->ws + c->lo.qstage;
+            KVM_CUDA(cudaMemcpyAsync(qs, q,
+                                     (size_t)sh.L * sh.n_queries * sh.H * sh.d *
+                                         elt_bytes(c->cfg.q_dtype),
+                                     cudaMemcpyDefault, s));
+            q = qs;
+        }
+        kvm::ScoreShape fs = sh;
+        fs.idle_producer = injected(c, 3) ? 1 : 0;
+        fs.idle_producer |= injected(c, 3) ? 2 : 0;
+        if ((e = kvm::launch_score_fused(fs, q, index, c0, c1, c->scr, c->cfg.max_blocks, s)) !=
+            cudaSuccess)
+            return cuda_fail(e, "score (one launch)");
+    } else if (c1 > c0) {
         const int nch = kvm::score_chunks(sh, c1 - c0, kvm::kMaxChunks);
         if ((e = kvm::launch_score_pass1(c->cfg.q_dtype, c->cfg.index_dtype, pass_shape(c, sh),
                                          q, index, 0, c0, c1, 0, nch, c->scr, s)) != cudaSuccess)

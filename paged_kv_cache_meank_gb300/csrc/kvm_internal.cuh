@@ -27,6 +27,8 @@ constexpr int kBlockTokens = 32;
 constexpr int kMaxHalfDim = 64;       // head_dim <= 128
 constexpr int kMaxRows = 256;         // query rows per KV head (M_q * H/G)
 constexpr int kMaxChunks = 64;        // block chunks per (layer, kv head) in scoring
+constexpr int kFusedMaxRows = 192;    // query rows per KV head the one-launch scoring takes
+constexpr int kFusedMaxCtas = 256;    // CTAs of one one-launch scoring grid, at most
 
 enum DType { F32 = 0, BF16 = 1, E4M3 = 2 };
 
@@ -90,7 +92,28 @@ struct ScoreScratch {
     float *row_invz;   // [LG][rows]
     float *partial;    // [LG][max_blocks]   per-(layer, kv head) relevance
     int *err;          // device error flag (bit 4: a bounded wait gave up)
+    // one-launch scoring, two slices deep: per-CTA row statistics, per-group
+    // row offsets o = M + log2 Z, and two arrival counters per CTA group
+    // (cleared by the launcher)
+    float2 *fpart;     // [kFusedMaxCtas][2][rows]  (max, sum) of a CTA's share
+    float *fo;         // [kFusedMaxCtas][2][rows]
+    int *fcnt;         // [2][kFusedMaxCtas]
 };
+
+// Bytes of the one-launch scoring scratch (fpart, fo, then fcnt) for up to
+// `rows` query rows per KV head; fused_scratch_carve sets the three pointers.
+inline size_t fused_scratch_bytes(int rows) {
+    return (size_t)kFusedMaxCtas * 2 * rows * (sizeof(float2) + sizeof(float)) +
+           (size_t)2 * kFusedMaxCtas * sizeof(int);
+}
+inline void fused_scratch_carve(ScoreScratch *s, void *base, int rows) {
+    char *b = static_cast<char *>(base);
+    s->fpart = reinterpret_cast<float2 *>(b);
+    b += (size_t)kFusedMaxCtas * 2 * rows * sizeof(float2);
+    s->fo = reinterpret_cast<float *>(b);
+    b += (size_t)kFusedMaxCtas * 2 * rows * sizeof(float);
+    s->fcnt = reinterpret_cast<int *>(b);
+}
 
 // Pass 1 over blocks [b_begin, b_end) of the index (rows of `index` addressed
 // relative to b_index0), writing chunks [chunk0, chunk0 + n_chunks).
@@ -113,6 +136,19 @@ cudaError_t launch_score_reduce(const ScoreShape &sh, int64_t n_blocks, int64_t 
                                 float *scores_out, cudaStream_t s);
 // Number of chunks used for a range of n blocks.
 int score_chunks(const ScoreShape &sh, int64_t n_blocks, int max_chunks);
+
+// One-launch tensor-core scoring (score_fused.cu): both passes over a
+// device-resident bf16 index in one persistent cooperative launch, for the
+// candidate blocks [c0, c1); writes scr.partial like pass 2.  Supported for
+// bf16 queries and index, d = 64 or 128 and at most kFusedMaxRows query rows
+// per KV head, with the queries in device memory (fused_q_ok: TMA reads them).
+// sh.idle_producer: bit 0 / bit 1 keep the TMA producer from loading pass-1 /
+// pass-2 tiles (failure-detection tests).
+bool score_fused_supported(int q_dtype, int index_dtype, const ScoreShape &sh);
+bool fused_q_ok(const void *q);
+cudaError_t launch_score_fused(const ScoreShape &sh, const void *q, const void *index,
+                               int64_t c0, int64_t c1, const ScoreScratch &scr,
+                               int64_t partial_stride, cudaStream_t s);
 
 // ---- select.cu
 // Device scratch of one selection (histograms and segment counts); fixed size.

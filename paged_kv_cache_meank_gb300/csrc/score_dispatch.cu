@@ -7,7 +7,7 @@
 namespace kvm {
 
 bool score_uses_tc(int q_dtype, int index_dtype, const ScoreShape &sh) {
-    return sh.variant == 0 && score_tc_supported(q_dtype, index_dtype, sh);
+    return (sh.variant == 0 || sh.variant == 2) && score_tc_supported(q_dtype, index_dtype, sh);
 }
 
 cudaError_t launch_score_pass1(int q_dtype, int index_dtype, const ScoreShape &sh,

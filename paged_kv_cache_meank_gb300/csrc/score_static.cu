@@ -122,6 +122,8 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     if (cfg->sink_blocks < 0 || cfg->recent_blocks < 0 ||
         cfg->view_blocks < cfg->sink_blocks + cfg->recent_blocks + 1)
         return bad(KVM_ERR_INVALID_ARG, "view_blocks must be >= sink + recent + 1");
+    if (cfg->score_variant < 0 || cfg->score_variant > 2)
+        return bad(KVM_ERR_INVALID_ARG, "score_variant must be 0, 1 or 2");
     if (cfg->candidate_mode != 0 && cfg->candidate_mode != 1)
         return bad(KVM_ERR_INVALID_ARG, "candidate_mode must be 0 or 1");
     if (n_queries < 1 || n_blocks < 1) return bad(KVM_ERR_INVALID_ARG, "empty input");
@@ -156,7 +158,8 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     const size_t rowb = up256(LG * sh.rows * sizeof(float));
     const size_t partial = up256(LG * (size_t)n_blocks * sizeof(float));
     const size_t selb = up256(kvm::select_scratch_bytes());
-    const size_t need = 256 + 2 * part + 2 * rowb + partial + selb;
+    const size_t fused = up256(kvm::fused_scratch_bytes(sh.rows));
+    const size_t need = 256 + 2 * part + 2 * rowb + partial + selb + fused;
     if (need > SCRATCH_BYTES) {
         char msg[200];
         snprintf(msg, sizeof msg,
@@ -198,11 +201,17 @@ extern "C" kvm_status kvm_score_select_static(const kvm_config *cfg, const void 
     scr.row_invz = reinterpret_cast<float *>(b + 2 * part + rowb);
     scr.partial = reinterpret_cast<float *>(b + 2 * part + 2 * rowb);
     int *sel_scratch = reinterpret_cast<int *>(b + 2 * part + 2 * rowb + partial);
+    kvm::fused_scratch_carve(&scr, b + 2 * part + 2 * rowb + partial + selb, sh.rows);
     scr.err = static_cast<int *>(base);
+    const bool one_launch = c1 > c0 &&
+                            kvm::score_fused_supported(cfg->q_dtype, cfg->index_dtype, sh) &&
+                            kvm::fused_q_ok(q);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if ((c1 > c0 &&
+    if ((one_launch &&
+         (e = kvm::launch_score_fused(sh, q, index, c0, c1, scr, n_blocks, s)) != cudaSuccess) ||
+        (!one_launch && c1 > c0 &&
          ((e = kvm::launch_score_pass1(cfg->q_dtype, cfg->index_dtype, sh, q, index, 0, c0, c1,
                                        0, nch, scr, s)) != cudaSuccess ||
           (e = kvm::launch_score_combine(sh, nch, scr, s)) != cudaSuccess ||

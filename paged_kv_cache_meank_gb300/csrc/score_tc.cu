@@ -60,53 +60,6 @@ struct Lay {
     static constexpr int SMEM = 1024 + OFF_BAR + 512;
 };
 
-// Sum of 2^(v*c + no) over n loaded columns (n a multiple of 16, at most 64;
-// no = minus the row offset).  Arguments and partial sums use the packed
-// float32x2 FMA / add of sm_100-family GPUs, two elements per instruction.
-__device__ __forceinline__ float exp_sum(const uint32_t *r, const float *no, int n, float c) {
-    const float2 c2 = make_float2(c, c);
-    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 64; k += 4) {
-        if (k < n) {
-            const float4 o4 = *reinterpret_cast<const float4 *>(no + k);
-            const float2 x01 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2,
-                make_float2(o4.x, o4.y));
-            const float2 x23 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2,
-                make_float2(o4.z, o4.w));
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
-        }
-    }
-    return (a0.x + a0.y) + (a1.x + a1.y);
-}
-
-// exp_sum over a compile-time count of columns (the common shapes), with no
-// per-column guards, so that the whole sum is one straight-line schedule.
-template <int NC>
-__device__ __forceinline__ float exp_sum_n(const uint32_t *r, const float *no, float c) {
-    const float2 c2 = make_float2(c, c);
-    float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                   make_float2(0.f, 0.f)};
-#pragma unroll
-    for (int k = 0; k < NC; k += 4) {
-        const float4 o4 = *reinterpret_cast<const float4 *>(no + k);
-        const float2 x01 = __ffma2_rn(
-            make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2,
-            make_float2(o4.x, o4.y));
-        const float2 x23 = __ffma2_rn(
-            make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2,
-            make_float2(o4.z, o4.w));
-        const int j = (k >> 2) & 1;
-        a[2 * j] = __fadd2_rn(a[2 * j], make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
-        a[2 * j + 1] = __fadd2_rn(a[2 * j + 1], make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
-    }
-    const float2 s01 = __fadd2_rn(a[0], a[1]), s23 = __fadd2_rn(a[2], a[3]);
-    return (s01.x + s01.y) + (s23.x + s23.y);
-}
-
 }  // namespace
 
 // NC: columns per epilogue warp when fixed at compile time (96 for 192 query
@@ -391,6 +344,21 @@ bool make_index_map(CUtensorMap *m, const void *index, int d, int64_t n_rows, in
     cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(index), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_q_map(CUtensorMap *m, const void *q, int d, int H, int64_t n_lq, int gqa,
+                int n_queries) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)n_lq};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)gqa, (cuuint32_t)n_queries};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

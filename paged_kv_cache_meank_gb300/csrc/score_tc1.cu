@@ -59,63 +59,6 @@ struct Lay1 {
     static constexpr int SMEM = 1024 + OFF_BAR + 512;
 };
 
-// Online softmax statistics of one query row over the first nv of NV loaded
-// scores: running max m (log2 units) and the partition sum z rescaled to it.
-template <int NV>
-__device__ __forceinline__ void online_update(const uint32_t *r, int nv, float c, float &m,
-                                              float &z) {
-    if (nv <= 0) return;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-    if (nv == NV) {
-#pragma unroll
-        for (int k = 0; k < NV; k += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-            mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (k < nv) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-    }
-    const float mn = fmaxf(m, fmaxf(mx0, mx1) * c);
-    float zs = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-        if (k < nv) zs += fast_exp2(fmaf(__uint_as_float(r[k]), c, -mn));
-    z = z * fast_exp2(m - mn) + zs;
-    m = mn;
-}
-
-// Row statistics with the reference held fixed: while every term of a full
-// tile stays below 2^64 relative to the row's current reference m, the tile
-// only adds its terms to z (no max over the tile).  A larger term, the row's
-// first tile and a ragged tile take the exact online update, which moves m to
-// the running maximum.  (m, z) stays an exact pair for any m: the partition sum
-// is z * 2^m, and pass 2 divides by it through m + log2 z.
-template <int NV>
-__device__ __forceinline__ void row_update(const uint32_t *r, int nv, float c, float &m,
-                                           float &z) {
-    if (nv == NV && m != -INFINITY) {
-        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
-        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < NV; k += 4) {
-            const float2 x01 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), c2, nm2);
-            const float2 x23 = __ffma2_rn(
-                make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), c2, nm2);
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
-        }
-        const float zs = (a0.x + a0.y) + (a1.x + a1.y);
-        if (zs <= 0x1p64f) {   // false for inf and NaN as well
-            z += zs;
-            return;
-        }
-    }
-    online_update<NV>(r, nv, c, m, z);
-}
-
 }  // namespace
 
 template <int D>
