@@ -70,7 +70,7 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitNs = 1000000000u;   // 1 s
 constexpr int kEpiBar = 1;                  // named barrier of the epilogue warps
-constexpr int kPrefetch = 2;                // pass-1 tiles loaded into L2 ahead of the ring
+constexpr int kPrefetch = 3;                // pass-1 tiles loaded into L2 ahead of the ring
 
 template <int D>
 struct LayF {
@@ -128,9 +128,7 @@ __device__ __forceinline__ void epi_sync() {
 
 }  // namespace
 
-// NC: pass-2 columns per epilogue warp when fixed at compile time (96 for 192
-// query rows), 0 for any row count.
-template <int D, int NC>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_constant__ CUtensorMap tq,
                    FusedArgs a) {
@@ -510,10 +508,14 @@ score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_consta
                                     Z += s1[s4 * 128].y * fast_exp2(s1[s4 * 128].x - M);
                         }
                         a.part[((size_t)blockIdx.x * 2 + (k & 1)) * rows + et] = make_float2(M, Z);
-                        __threadfence();
                     }
+                    // the writes above, ordered by the barrier, are published by
+                    // one fence and release of thread 0
                     epi_sync();
-                    if (et == 0) tc::red_release_gpu_add(a.cnt + grp, 1);
+                    if (et == 0) {
+                        __threadfence();
+                        tc::red_release_gpu_add(a.cnt + grp, 1);
+                    }
                 }
                 if (j == jA) {
                     // ---------------- rows p, p + P, ...: fold the group's P shares
@@ -541,14 +543,15 @@ score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_consta
                             }
 #pragma unroll
                         for (int o = 16; o; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-                        if (lane == 0) {
+                        if (lane == 0)
                             a.fo[((size_t)grp * 2 + (k & 1)) * rows + p + i * a.P] =
                                 M != -INFINITY && Z > 0.f ? M + log2f(Z) : INFINITY;
-                            __threadfence();
-                        }
                     }
                     epi_sync();
-                    if (et == 0) tc::red_release_gpu_add(a.cnt + kFusedMaxCtas + grp, 1);
+                    if (et == 0) {
+                        __threadfence();
+                        tc::red_release_gpu_add(a.cnt + kFusedMaxCtas + grp, 1);
+                    }
                 }
                 if (j == nT + nH) break;
                 // ---------------- one pass-1 tile (of slice k, or of k + 1 in H)
@@ -597,6 +600,11 @@ score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_consta
             }
             epi_sync();
             // ---------------- P2(k), tiles in reverse order
+            // the next slice's row statistics wait in shared memory (fewer live
+            // registers in the pass-2 loop); the stat area is free until the
+            // next (m, z) step
+            stat[et] = make_float2(m_run[0], z_run[0]);
+            stat[kEpiThreads + et] = make_float2(m_run[1], z_run[1]);
             bool pend = false;
             float pend_sum = 0.f;
             int64_t pend_b0 = 0;
@@ -620,45 +628,30 @@ score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_consta
                 if (!waitb(&tfull[buf], ph, abort_flag, a.err)) continue;
                 tc::tc_fence_after();
                 const uint32_t taddr = tmem + lane_base + buf * 256;
-                uint32_t r[48];
-                float sum;
-                if (NC == 96) {   // 192 query rows: 96 columns per warp, two chunks of 48
-                    tc::tmem_ld32_async(taddr + my_c0, r);
-                    tc::tmem_ld16_async(taddr + my_c0 + 32, r + 32);
-                    tc::tmem_wait_ld(r);
-                    tc::tmem_wait_ld(r + 16);
-                    tc::tmem_wait_ld(r + 32);
-                    sum = exp_sum_n<48>(r, o_neg + my_c0, a.scale_log2);
-                    tc::tmem_ld32_async(taddr + my_c0 + 48, r);
-                    tc::tmem_ld16_async(taddr + my_c0 + 80, r + 32);
-                    tc::tmem_wait_ld(r);
-                    tc::tmem_wait_ld(r + 16);
-                    tc::tmem_wait_ld(r + 32);
+                uint32_t r[32];
+                // the row columns in 32-column runs; the accumulator goes back
+                // once the last run is loaded
+                float sum = 0.f;
+                if (my_nc == 0) {
                     tc::tc_fence_before();
                     tc::mbar_arrive(&tempty2[buf]);
-                    sum += exp_sum_n<48>(r, o_neg + my_c0 + 48, a.scale_log2);
-                } else {
-                    sum = 0.f;
-                    if (my_nc == 0) {
+                }
+                for (int c = 0; c < my_nc; c += 32) {
+                    const int nc = min(32, my_nc - c);    // 16 or 32
+                    if (nc == 32) {
+                        tc::tmem_ld32_async(taddr + my_c0 + c, r);
+                        tc::tmem_wait_ld(r);
+                        tc::tmem_wait_ld(r + 16);
+                    } else {
+                        tc::tmem_ld16_async(taddr + my_c0 + c, r);
+                        tc::tmem_wait_ld(r);
+                    }
+                    if (c + 32 >= my_nc) {
                         tc::tc_fence_before();
                         tc::mbar_arrive(&tempty2[buf]);
                     }
-                    for (int c = 0; c < my_nc; c += 32) {
-                        const int nc = min(32, my_nc - c);    // 16 or 32
-                        if (nc == 32) {
-                            tc::tmem_ld32_async(taddr + my_c0 + c, r);
-                            tc::tmem_wait_ld(r);
-                            tc::tmem_wait_ld(r + 16);
-                        } else {
-                            tc::tmem_ld16_async(taddr + my_c0 + c, r);
-                            tc::tmem_wait_ld(r);
-                        }
-                        if (c + 32 >= my_nc) {
-                            tc::tc_fence_before();
-                            tc::mbar_arrive(&tempty2[buf]);
-                        }
-                        sum += exp_sum(r, o_neg + my_c0 + c, nc, a.scale_log2);
-                    }
+                    sum += nc == 32 ? exp_sum_n<32>(r, o_neg + my_c0 + c, a.scale_log2)
+                                    : exp_sum(r, o_neg + my_c0 + c, nc, a.scale_log2);
                 }
                 // the partner's sum goes through a four-deep ring of slots per
                 // group (see score_tc.cu for why a slot is read before reuse)
@@ -676,6 +669,13 @@ score_fused_kernel(const __grid_constant__ CUtensorMap tidx, const __grid_consta
                 }
             }
             if (hf == 0 && pend) combine();
+            {
+                const float2 v0 = stat[et], v1 = stat[kEpiThreads + et];
+                m_run[0] = v0.x;
+                z_run[0] = v0.y;
+                m_run[1] = v1.x;
+                z_run[1] = v1.y;
+            }
         }
     }
     tc::tc_fence_before();
@@ -751,7 +751,7 @@ Plan plan_groups(int64_t n, int LG, int d, int sms) {
     return best;
 }
 
-template <int D, int NC>
+template <int D>
 cudaError_t fused_t(const ScoreShape &sh, const void *q, const void *index, int64_t c0,
                     int64_t c1, const ScoreScratch &scr, int64_t partial_stride,
                     cudaStream_t s) {
@@ -760,7 +760,7 @@ cudaError_t fused_t(const ScoreShape &sh, const void *q, const void *index, int6
         return cudaErrorInvalidValue;
     if (!make_q_map(&mq, q, D, sh.H, (int64_t)sh.L * sh.n_queries, sh.gqa, sh.n_queries))
         return cudaErrorInvalidValue;
-    auto kern = score_fused_kernel<D, NC>;
+    auto kern = score_fused_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          LayF<D>::SMEM);
     if (e != cudaSuccess) return e;
@@ -827,12 +827,8 @@ cudaError_t launch_score_fused(const ScoreShape &sh, const void *q, const void *
                                int64_t partial_stride, cudaStream_t s) {
     if (c1 <= c0) return cudaSuccess;
     if (((uintptr_t)index & 15) != 0) return cudaErrorMisalignedAddress;
-    const bool n192 = ((sh.rows + 15) & ~15) == 192;
-    if (sh.d == 128)
-        return n192 ? fused_t<128, 96>(sh, q, index, c0, c1, scr, partial_stride, s)
-                    : fused_t<128, 0>(sh, q, index, c0, c1, scr, partial_stride, s);
-    return n192 ? fused_t<64, 96>(sh, q, index, c0, c1, scr, partial_stride, s)
-                : fused_t<64, 0>(sh, q, index, c0, c1, scr, partial_stride, s);
+    if (sh.d == 128) return fused_t<128>(sh, q, index, c0, c1, scr, partial_stride, s);
+    return fused_t<64>(sh, q, index, c0, c1, scr, partial_stride, s);
 }
 
 }  // namespace kvm
