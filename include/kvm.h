@@ -281,8 +281,18 @@ typedef struct {
  * bound, else the repository), or rotated in place by the position change
  * under delta_rerope_limit.  pool_raw_k may be NULL unless the repository is
  * host-resident with h2d_mode 0.
- * Synchronises with `stream` once (to read the selected ids) and returns
- * with the rest enqueued; `stats` (nullable, host) is filled before return.
+ * Where the GPU reads the repository itself (repo_location == KVM_DEVICE, or
+ * KVM_HOST_PINNED with h2d_mode 1) and no host-tier policy runs, the residency
+ * diff (hits, misses, free pages, the page table, the assembly descriptors) is
+ * a kernel over residency kept in the workspace: the step waits for nothing and
+ * returns with all of its work enqueued on `stream`, and `stats` (nullable,
+ * host) is filled by the next kvm_sync, so it must stay valid until then.
+ * Otherwise (copy-engine transfers, which the host issues per run of missed
+ * blocks, or a host-tier policy fed with the selection) the step synchronises
+ * with `stream` once to read the selected ids, diffs on the host, returns with
+ * the rest enqueued and fills `stats` before returning.  Both diffs give the
+ * same pages.  kvm_bind and kvm_reset_pool empty the pool; they must not be
+ * called while another thread enqueues a step on the same context.
  */
 kvm_status kvm_step(kvm_ctx *ctx, const void *q, int32_t n_queries, int64_t n_blocks,
                     kvm_step_stats *stats, kvm_stream stream);

@@ -16,6 +16,7 @@ Serving" (§2 RoPE background, Theorem 6).
 from __future__ import annotations
 
 import ctypes
+from collections.abc import Mapping
 
 import torch
 
@@ -150,6 +151,27 @@ class HostTier:
             pass
 
 
+class StepStats(Mapping):
+    """The counters of one kvm_step, read from the kvm_step_stats the library
+    fills (by the next kvm_sync at the latest)."""
+
+    _KEYS = tuple(f for f, _ in KvmStepStats._fields_)
+
+    def __init__(self, st: KvmStepStats):
+        self._st = st
+
+    def __getitem__(self, k):
+        if k not in self._KEYS:
+            raise KeyError(k)
+        return getattr(self._st, k)
+
+    def __iter__(self):
+        return iter(self._KEYS)
+
+    def __len__(self):
+        return len(self._KEYS)
+
+
 class Context:
     """A kvm_ctx plus its caller-owned device workspace (a torch uint8 tensor)."""
 
@@ -165,6 +187,7 @@ class Context:
                                   _stream(stream), ctypes.byref(h)), "kvm_create")
         self.handle = h
         self._bound = None
+        self._pending = []
 
     # -- shapes -----------------------------------------------------------
     @property
@@ -225,14 +248,18 @@ class Context:
     def reset_pool(self) -> None:
         check(self.lib.kvm_reset_pool(self.handle), "kvm_reset_pool")
 
-    def step(self, q, n_queries: int, n_blocks: int, stream=None) -> dict:
+    def step(self, q, n_queries: int, n_blocks: int, stream=None) -> "StepStats":
+        """One kvm_step.  The returned counters are final once sync() returns
+        (a step whose residency diff runs on the device fills them then)."""
         st = KvmStepStats()
         check(self.lib.kvm_step(self.handle, _ptr(q), n_queries, n_blocks, ctypes.byref(st),
                                 _stream(stream)), "kvm_step")
-        return {f: getattr(st, f) for f, _ in KvmStepStats._fields_}
+        self._pending.append(st)           # the library writes it until the next sync
+        return StepStats(st)
 
     def sync(self, stream=None) -> None:
         check(self.lib.kvm_sync(self.handle, _stream(stream)), "kvm_sync")
+        self._pending.clear()
 
     def debug_inject(self, what: int, nth: int) -> None:
         check(self.lib.kvm_debug_inject(self.handle, what, nth), "kvm_debug_inject")

@@ -30,6 +30,7 @@ SOURCES = [
     "score_dispatch.cu",
     "select.cu",
     "assemble.cu",
+    "residency.cu",
     "score_static.cu",
     "kvm_api.cpp",
     "host_tier.cpp",

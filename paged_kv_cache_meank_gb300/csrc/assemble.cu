@@ -139,8 +139,10 @@ assemble_ids_kernel(const int32_t *__restrict__ sel_ids, const int32_t *__restri
 template <typename T, int D>
 __global__ void __launch_bounds__(SlotWork<T, D>::NT)
 assemble_desc_kernel(const SlotDesc *__restrict__ desc, int LG, int lg_per_cta,
-                     const float2 *__restrict__ table, int64_t max_pos, int *err) {
+                     const float2 *__restrict__ table, int64_t max_pos, int *err,
+                     const int32_t *__restrict__ n_dev) {
     __shared__ float2 tab[kBlockTokens * (D / 2)];
+    if (n_dev && (int)blockIdx.x >= *n_dev) return;   // count known on the device only
     const SlotDesc sd = desc[blockIdx.x];
     const bool delta = (sd.flags & kSlotDelta) != 0;
     const bool pos_ok = delta ? (sd.pos0 > -max_pos && sd.pos0 < max_pos)
@@ -179,12 +181,12 @@ static cudaError_t ids_t(const int32_t *sel_ids, const int32_t *page_ids, int n_
 }
 
 template <typename T, int D>
-static cudaError_t desc_t(const SlotDesc *desc, int n_desc, int LG, const float2 *table,
-                          int64_t max_pos, int *err, cudaStream_t s) {
+static cudaError_t desc_t(const SlotDesc *desc, int n_desc, const int32_t *n_dev, int LG,
+                          const float2 *table, int64_t max_pos, int *err, cudaStream_t s) {
     const int lpc = lg_split(n_desc, LG);
     dim3 grid((unsigned)n_desc, (unsigned)((LG + lpc - 1) / lpc));
     assemble_desc_kernel<T, D><<<grid, SlotWork<T, D>::NT, 0, s>>>(desc, LG, lpc, table,
-                                                                     max_pos, err);
+                                                                     max_pos, err, n_dev);
     note_launch();
     return cudaGetLastError();
 }
@@ -217,23 +219,35 @@ cudaError_t launch_assemble_ids(int kv_dtype, int d, const int32_t *sel_ids,
     return cudaErrorInvalidValue;
 }
 
+static cudaError_t desc_dispatch(int kv_dtype, int d, const SlotDesc *desc, int n_desc,
+                                 const int32_t *n_dev, int LG, const float2 *table,
+                                 int64_t max_pos, int *err, cudaStream_t s) {
+    if (n_desc <= 0) return cudaSuccess;
+    if (kv_dtype == BF16 && d == 128)
+        return desc_t<__nv_bfloat16, 128>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    if (kv_dtype == BF16 && d == 64)
+        return desc_t<__nv_bfloat16, 64>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    if (kv_dtype == F32 && d == 128)
+        return desc_t<float, 128>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    if (kv_dtype == F32 && d == 64)
+        return desc_t<float, 64>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    if (kv_dtype == E4M3 && d == 128)
+        return desc_t<e4m3, 128>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    if (kv_dtype == E4M3 && d == 64)
+        return desc_t<e4m3, 64>(desc, n_desc, n_dev, LG, table, max_pos, err, s);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_assemble_desc(int kv_dtype, int d, const SlotDesc *desc, int n_desc, int LG,
                                  const float2 *table, int64_t max_pos, int *err,
                                  cudaStream_t s) {
-    if (n_desc <= 0) return cudaSuccess;
-    if (kv_dtype == BF16 && d == 128)
-        return desc_t<__nv_bfloat16, 128>(desc, n_desc, LG, table, max_pos, err, s);
-    if (kv_dtype == BF16 && d == 64)
-        return desc_t<__nv_bfloat16, 64>(desc, n_desc, LG, table, max_pos, err, s);
-    if (kv_dtype == F32 && d == 128)
-        return desc_t<float, 128>(desc, n_desc, LG, table, max_pos, err, s);
-    if (kv_dtype == F32 && d == 64)
-        return desc_t<float, 64>(desc, n_desc, LG, table, max_pos, err, s);
-    if (kv_dtype == E4M3 && d == 128)
-        return desc_t<e4m3, 128>(desc, n_desc, LG, table, max_pos, err, s);
-    if (kv_dtype == E4M3 && d == 64)
-        return desc_t<e4m3, 64>(desc, n_desc, LG, table, max_pos, err, s);
-    return cudaErrorInvalidValue;
+    return desc_dispatch(kv_dtype, d, desc, n_desc, nullptr, LG, table, max_pos, err, s);
+}
+
+cudaError_t launch_assemble_desc_dev(int kv_dtype, int d, const SlotDesc *desc, int n_max,
+                                     const int32_t *n_dev, int LG, const float2 *table,
+                                     int64_t max_pos, int *err, cudaStream_t s) {
+    return desc_dispatch(kv_dtype, d, desc, n_max, n_dev, LG, table, max_pos, err, s);
 }
 
 }  // namespace kvm

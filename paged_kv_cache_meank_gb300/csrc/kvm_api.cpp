@@ -50,9 +50,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t elt_bytes(int dt) { return dt == KVM_E4M3 ? 1 : dt == KVM_BF16 ? 2 : 4; }
 
+constexpr int kStatSlots = 64;   // steps whose counters can wait for kvm_sync
+
 struct Layout {
     size_t table, part_m, part_z, row_m, row_invz, partial, fused, qstage, stage0, stage1, desc,
-        sel, err, total;
+        sel, resid, err, total;
     size_t qstage_bytes;
     size_t stage_bytes;
     int rows_max, chunk_cap;
@@ -139,6 +141,12 @@ Layout layout_of(const kvm_config *c) {
     }
     lo.desc = take((size_t)(c->pool_pages + c->view_blocks) * sizeof(kvm::SlotDesc));
     lo.sel = take(kvm::select_scratch_bytes());
+    // the device-side residency of kvm_step (int32 each): page_of_block and
+    // stamp per block; block_of_page, baked_pos, delta_count and a free list
+    // per page; a page per slot; kStatSlots steps of counters
+    lo.resid = take(((size_t)2 * c->max_blocks + (size_t)4 * c->pool_pages + c->view_blocks +
+                     (size_t)kStatSlots * 8) *
+                    sizeof(int32_t));
     lo.err = take(256);
     lo.total = off;
     return lo;
@@ -180,6 +188,24 @@ struct kvm_ctx {
     std::vector<int32_t> delta_count;    // delta rotations since the page's K was rebuilt
     std::vector<int32_t> page_of_block;
     std::vector<uint8_t> mark;
+    // residency diff on the device (repository read by the GPU, no host tier):
+    // the state lives in the workspace and kvm_step never waits for the GPU
+    bool device_diff = false;
+    int32_t *d_page_of_block = nullptr, *d_stamp = nullptr, *d_block_of_page = nullptr,
+            *d_baked_pos = nullptr, *d_delta_count = nullptr, *d_free_list = nullptr,
+            *d_slot_page = nullptr, *d_counts = nullptr;
+    int32_t epoch = 0;
+    int64_t n_dev_steps = 0;
+    struct Pending {
+        kvm_step_stats *out;
+        int slot;
+        int64_t n_blocks;
+        int32_t n_sel;
+    };
+    std::vector<Pending> pending;        // steps whose counters kvm_sync copies out
+    cudaEvent_t ev_reset = nullptr;      // the device residency was cleared on the copy stream
+    cudaEvent_t ev_step = nullptr;       // the last device-diff step's work is enqueued
+    bool reset_pending = false;
     kvm_tier *tier = nullptr;            // host-tier policy (host_tier_blocks > 0)
     // fault injection
     int inject_what = 0;
@@ -217,7 +243,34 @@ size_t block_bytes(const kvm_config &c) {
     return (size_t)c.n_layers * c.n_kv_heads * 32 * c.head_dim * elt_bytes(c.kv_dtype);
 }
 
-void reset_pool(kvm_ctx *c) {
+// Clears the device-side residency on the copy stream, after the work already
+// on `after` when `has_after` (a stream handle may be 0, the legacy default
+// stream), else after the last step enqueued; the next step waits for it.
+cudaError_t reset_device(kvm_ctx *c, cudaStream_t after, bool has_after) {
+    if (!c->device_diff || !c->copy_stream) return cudaSuccess;
+    cudaError_t e;
+    if (has_after) {
+        if ((e = cudaEventRecord(c->ev_main, after)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0)) != cudaSuccess)
+            return e;
+    } else if (c->n_dev_steps > 0 &&
+               (e = cudaStreamWaitEvent(c->copy_stream, c->ev_step, 0)) != cudaSuccess) {
+        return e;   // after the last step enqueued
+    }
+    const size_t nb = (size_t)c->cfg.max_blocks, np = (size_t)c->cfg.pool_pages;
+    if ((e = cudaMemsetAsync(c->d_page_of_block, 0xFF, nb * 4, c->copy_stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(c->d_block_of_page, 0xFF, np * 4, c->copy_stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(c->d_baked_pos, 0xFF, np * 4, c->copy_stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(c->d_delta_count, 0, np * 4, c->copy_stream)) != cudaSuccess ||
+        (e = cudaEventRecord(c->ev_reset, c->copy_stream)) != cudaSuccess)
+        return e;
+    c->reset_pending = true;
+    return cudaSuccess;
+}
+
+void reset_pool(kvm_ctx *c, cudaStream_t after = nullptr, bool has_after = false) {
+    if (reset_device(c, after, has_after) != cudaSuccess)
+        kvm::set_last_error("device residency reset failed");
     for (int64_t b : c->block_of_page)
         if (b >= 0 && b < (int64_t)c->page_of_block.size()) c->page_of_block[b] = -1;
     std::fill(c->block_of_page.begin(), c->block_of_page.end(), -1);
@@ -303,6 +356,22 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     c->sel_scratch = reinterpret_cast<int *>(c->ws + lo.sel);
     c->err_dev = reinterpret_cast<int *>(c->ws + lo.err);
     c->scr.err = c->err_dev;
+    {
+        int32_t *r = reinterpret_cast<int32_t *>(c->ws + lo.resid);
+        c->d_page_of_block = r;
+        c->d_stamp = r + cfg->max_blocks;
+        c->d_block_of_page = c->d_stamp + cfg->max_blocks;
+        c->d_baked_pos = c->d_block_of_page + cfg->pool_pages;
+        c->d_delta_count = c->d_baked_pos + cfg->pool_pages;
+        c->d_free_list = c->d_delta_count + cfg->pool_pages;
+        c->d_slot_page = c->d_free_list + cfg->pool_pages;
+        c->d_counts = c->d_slot_page + cfg->view_blocks;
+    }
+    // the diff runs on the device when the kernels read the repository
+    // themselves; copy-engine transfers and the host-tier policy need the
+    // selected ids on the host
+    c->device_diff = (cfg->repo_location == KVM_DEVICE || cfg->h2d_mode == 1) &&
+                     cfg->host_tier_blocks == 0;
     try {   // no exception crosses the C ABI
         c->block_of_page.assign(cfg->pool_pages, -1);
         c->baked_pos.assign(cfg->pool_pages, -1);
@@ -327,7 +396,9 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
             return cleanup(cuda_fail(e, "cudaEventCreate"));
     }
     if ((e = cudaEventCreateWithFlags(&c->ev_main, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&c->ev_stage, cudaEventDisableTiming)) != cudaSuccess)
+        (e = cudaEventCreateWithFlags(&c->ev_stage, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_reset, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_step, cudaEventDisableTiming)) != cudaSuccess)
         return cleanup(cuda_fail(e, "cudaEventCreate"));
     for (auto &ev : c->ev_batch)
         if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
@@ -345,6 +416,12 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
         return cleanup(cuda_fail(e, "rope table"));
     if ((e = cudaMemsetAsync(c->err_dev, 0, sizeof(int), s)) != cudaSuccess)
         return cleanup(cuda_fail(e, "cudaMemsetAsync"));
+    if (c->device_diff) {
+        // an empty pool; no block has been selected yet (stamp 0 < every epoch)
+        if ((e = cudaMemsetAsync(c->d_stamp, 0, (size_t)cfg->max_blocks * 4, s)) != cudaSuccess ||
+            (e = reset_device(c, s, true)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "residency init"));
+    }
     *out = c;
     return KVM_OK;
 }
@@ -353,7 +430,7 @@ kvm_status kvm_destroy(kvm_ctx *c) {
     if (!c) return KVM_OK;
     if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
     for (auto ev : {c->ev_ready[0], c->ev_ready[1], c->ev_free[0], c->ev_free[1], c->ev_main,
-                    c->ev_stage})
+                    c->ev_stage, c->ev_reset, c->ev_step})
         if (ev) cudaEventDestroy(ev);
     for (auto ev : c->ev_batch)
         if (ev) cudaEventDestroy(ev);
@@ -695,6 +772,98 @@ static int commit_residency(kvm_ctx *c, const std::vector<int32_t> &sel,
     return evicted;
 }
 
+// Copies the counters of every step still waiting for them to the caller's
+// stats (host tier fields 0); the steps' work must be complete.
+static kvm_status flush_pending(kvm_ctx *c) {
+    if (c->pending.empty()) return KVM_OK;
+    int32_t ring[kStatSlots * 8];
+    KVM_CUDA(cudaEventSynchronize(c->ev_step));
+    KVM_CUDA(cudaMemcpy(ring, c->d_counts, sizeof ring, cudaMemcpyDeviceToHost));
+    const bool pull = c->cfg.repo_location == KVM_HOST_PINNED;
+    const int64_t blk = (int64_t)block_bytes(c->cfg);
+    for (const auto &pd : c->pending) {
+        const int32_t *k = ring + pd.slot * 8;
+        kvm_step_stats *st = pd.out;
+        *st = kvm_step_stats{};
+        st->n_blocks = pd.n_blocks;
+        st->n_sel = pd.n_sel;
+        st->hits = k[1];
+        st->misses = k[2];
+        st->reroped = k[0];
+        st->delta_reroped = k[3];
+        st->evicted = k[4];
+        st->h2d_bytes = pull ? 2 * (int64_t)k[2] * blk : 0;
+    }
+    c->pending.clear();
+    return KVM_OK;
+}
+
+// kvm_step when the residency diff runs on the device (the repository in
+// device memory, or in pinned host memory read by the GPU): selection ->
+// diff -> assembly, all enqueued on the stream with no wait on the host.
+static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
+                              kvm_step_stats *stats, cudaStream_t s) {
+    const kvm_config &cfg = c->cfg;
+    cudaError_t e;
+    if (c->pending.size() >= (size_t)kStatSlots) {
+        // the counter ring is full: the oldest steps' counters go out first
+        if (kvm_status st = flush_pending(c); st != KVM_OK) return st;
+    }
+    if (c->reset_pending) {
+        KVM_CUDA(cudaStreamWaitEvent(s, c->ev_reset, 0));
+        c->reset_pending = false;
+    }
+    const int slot = (int)(c->n_dev_steps % kStatSlots);
+    const bool pull = cfg.repo_location == KVM_HOST_PINNED;
+    auto abort_step = [&](kvm_status err) {
+        // the diff may have run: forget the whole pool, after this stream's work
+        reset_pool(c, s, true);
+        return err;
+    };
+    kvm::ResidencyArgs a{};
+    a.sel = c->bufs.sel_ids;
+    a.n_sel = n_sel;
+    a.page_of_block = c->d_page_of_block;
+    a.block_of_page = c->d_block_of_page;
+    a.baked_pos = c->d_baked_pos;
+    a.delta_count = c->d_delta_count;
+    a.stamp = c->d_stamp;
+    a.epoch = ++c->epoch;
+    a.P = cfg.pool_pages;
+    a.max_blocks = cfg.max_blocks;
+    a.delta_limit = cfg.delta_rerope_limit;
+    a.page_table = c->bufs.page_table;
+    a.desc = c->desc_dev;
+    a.counts = c->d_counts + slot * 8;
+    a.slot_page = c->d_slot_page;
+    a.free_list = c->d_free_list;
+    a.pool_k = static_cast<char *>(c->bufs.pool_k);
+    a.pool_v = static_cast<char *>(c->bufs.pool_v);
+    a.pool_raw = static_cast<char *>(c->bufs.pool_raw_k);
+    a.repo_k = static_cast<const char *>(c->repo_k_dev);
+    a.repo_v = static_cast<const char *>(c->repo_v_dev);
+    a.blk = block_bytes(cfg);
+    a.pull = pull ? 1 : 0;
+    a.err = c->err_dev;
+    if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
+    if ((e = kvm::launch_residency_diff(a, s)) != cudaSuccess)
+        return abort_step(cuda_fail(e, "residency diff launch"));
+    if (pull && c->staged) {
+        // the kernel reads the host repository: order it after earlier stage-outs
+        if ((e = cudaStreamWaitEvent(s, c->ev_stage, 0)) != cudaSuccess)
+            return abort_step(cuda_fail(e, "stage-out wait"));
+    }
+    if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
+    if ((e = kvm::launch_assemble_desc_dev(cfg.kv_dtype, cfg.head_dim, c->desc_dev, n_sel,
+                                           a.counts, cfg.n_layers * cfg.n_kv_heads, c->table,
+                                           cfg.max_positions, c->err_dev, s)) != cudaSuccess)
+        return abort_step(cuda_fail(e, "assemble launch"));
+    KVM_CUDA(cudaEventRecord(c->ev_step, s));
+    ++c->n_dev_steps;
+    if (stats) c->pending.push_back({stats, slot, n_blocks, n_sel});
+    return KVM_OK;
+}
+
 static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_t n_blocks,
                             kvm_step_stats *stats, kvm_stream stream) {
     const kvm_config &cfg = c->cfg;
@@ -703,6 +872,7 @@ static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_
     kvm_status st = kvm_score_select(c, q, n_queries, c->bufs.index, n_blocks, c->bufs.scores,
                                      c->bufs.sel_ids, &n_sel, stream);
     if (st != KVM_OK) return st;
+    if (c->device_diff) return step_device(c, n_blocks, n_sel, stats, s);
 
     // the selected ids drive the host-side residency diff
     std::vector<int32_t> sel(n_sel);
@@ -906,6 +1076,7 @@ kvm_status kvm_sync(kvm_ctx *c, kvm_stream stream) {
     if (!c) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
     KVM_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
     KVM_CUDA(cudaStreamSynchronize(c->copy_stream));
+    if (kvm_status st = flush_pending(c); st != KVM_OK) return st;
     int flag = 0;
     KVM_CUDA(cudaMemcpy(&flag, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost));
     if (flag) {

@@ -82,6 +82,40 @@ cudaError_t launch_assemble_ids(int kv_dtype, int d, const int32_t *sel_ids,
 cudaError_t launch_assemble_desc(int kv_dtype, int d, const SlotDesc *desc, int n_desc, int LG,
                                  const float2 *table, int64_t max_pos, int *err,
                                  cudaStream_t s);
+// The same with the descriptor count in device memory (*n_dev <= n_max).
+cudaError_t launch_assemble_desc_dev(int kv_dtype, int d, const SlotDesc *desc, int n_max,
+                                     const int32_t *n_dev, int LG, const float2 *table,
+                                     int64_t max_pos, int *err, cudaStream_t s);
+
+// ---- residency.cu
+// One kvm_step's residency diff on the device (the delta working set): reads
+// the selection, writes the page table, the assembly descriptors (count in
+// counts[0]) and the new residency; counts[1..4] = hits, misses, delta
+// rotations, evicted blocks.  Residency arrays are int32, -1 = none.
+struct ResidencyArgs {
+    const int32_t *sel;        // [n_sel] selected block ids
+    int n_sel;
+    int32_t *page_of_block;    // [max_blocks]
+    int32_t *block_of_page;    // [P]
+    int32_t *baked_pos;        // [P] first token position of the K in the page
+    int32_t *delta_count;      // [P] delta rotations since the page's K was rebuilt
+    int32_t *stamp;            // [max_blocks] epoch of the last step that selected it
+    int32_t epoch;             // this step's stamp (> every earlier one)
+    int P;
+    int64_t max_blocks;
+    int delta_limit;
+    int32_t *page_table;       // [n_sel] out
+    SlotDesc *desc;            // [n_sel] out
+    int32_t *counts;           // [8] out
+    int32_t *slot_page;        // [n_sel] scratch
+    int32_t *free_list;        // [P] scratch
+    char *pool_k, *pool_v, *pool_raw;    // pool_raw may be NULL
+    const char *repo_k, *repo_v;         // repository as the GPU addresses it
+    size_t blk;                // bytes of one block ([L][G][32][d])
+    int pull;                  // host repository read by the GPU (keep raw K in the page)
+    int *err;
+};
+cudaError_t launch_residency_diff(const ResidencyArgs &a, cudaStream_t s);
 
 // ---- score.cu
 // Scratch for one scoring call (device pointers inside the workspace).
