@@ -137,8 +137,10 @@ typedef struct {
 typedef struct kvm_ctx kvm_ctx;
 
 /* Device workspace bytes a context needs for `cfg` (RoPE table, scoring
- * scratch, index staging tiles -- two, or one per index tile with
- * index_spill -- and step descriptors).  0 if cfg is invalid. */
+ * scratch including that of the one-launch variant, a copy of the queries for
+ * a device index when they are passed in host memory, index staging tiles --
+ * two, or one per index tile with index_spill -- step descriptors and the
+ * device-side residency of the page pool).  0 if cfg is invalid. */
 size_t kvm_workspace_bytes(const kvm_config *cfg);
 
 /* Create a context.  `workspace` is caller-owned device memory of at least
@@ -180,7 +182,10 @@ kvm_status kvm_build_index(kvm_ctx *ctx, const void *k_pages, int64_t first_bloc
  * the largest R_b (ties: lower block id; NaN last); output ascending.  If
  * N <= V_b every block is selected.
  *
- * q         device, [L][n_queries][H][d], q_dtype (RoPE-free queries).
+ * q         device, [L][n_queries][H][d], q_dtype (RoPE-free queries); with
+ *           score_variant 2 and a device index, queries in pinned host memory
+ *           are first copied into the workspace (the one-launch kernel reads
+ *           them by TMA from device memory).
  * index     [L][G][max_blocks][d], index_dtype; device memory when
  *           cfg.index_location == KVM_DEVICE, pinned host memory when
  *           KVM_HOST_PINNED (then scored in tiles of tile_blocks staged on the GPU).
