@@ -145,7 +145,7 @@ Layout layout_of(const kvm_config *c) {
     // stamp per block; block_of_page, baked_pos, delta_count and a free list
     // per page; a page per slot; kStatSlots steps of counters
     lo.resid = take(((size_t)2 * c->max_blocks + (size_t)4 * c->pool_pages + c->view_blocks +
-                     (size_t)kStatSlots * 8) *
+                     (size_t)kStatSlots * 8 + 1) *
                     sizeof(int32_t));
     lo.err = take(256);
     lo.total = off;
@@ -193,8 +193,7 @@ struct kvm_ctx {
     bool device_diff = false;
     int32_t *d_page_of_block = nullptr, *d_stamp = nullptr, *d_block_of_page = nullptr,
             *d_baked_pos = nullptr, *d_delta_count = nullptr, *d_free_list = nullptr,
-            *d_slot_page = nullptr, *d_counts = nullptr;
-    int32_t epoch = 0;
+            *d_slot_page = nullptr, *d_counts = nullptr, *d_epoch = nullptr;
     int64_t n_dev_steps = 0;
     struct Pending {
         kvm_step_stats *out;
@@ -366,6 +365,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
         c->d_free_list = c->d_delta_count + cfg->pool_pages;
         c->d_slot_page = c->d_free_list + cfg->pool_pages;
         c->d_counts = c->d_slot_page + cfg->view_blocks;
+        c->d_epoch = c->d_counts + kStatSlots * 8;
     }
     // the diff runs on the device when the kernels read the repository
     // themselves; copy-engine transfers and the host-tier policy need the
@@ -419,6 +419,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
     if (c->device_diff) {
         // an empty pool; no block has been selected yet (stamp 0 < every epoch)
         if ((e = cudaMemsetAsync(c->d_stamp, 0, (size_t)cfg->max_blocks * 4, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(c->d_epoch, 0, sizeof(int32_t), s)) != cudaSuccess ||
             (e = reset_device(c, s, true)) != cudaSuccess)
             return cleanup(cuda_fail(e, "residency init"));
     }
@@ -828,7 +829,7 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
     a.baked_pos = c->d_baked_pos;
     a.delta_count = c->d_delta_count;
     a.stamp = c->d_stamp;
-    a.epoch = ++c->epoch;
+    a.epoch = c->d_epoch;
     a.P = cfg.pool_pages;
     a.max_blocks = cfg.max_blocks;
     a.delta_limit = cfg.delta_rerope_limit;

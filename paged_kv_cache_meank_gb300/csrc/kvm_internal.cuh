@@ -100,7 +100,7 @@ struct ResidencyArgs {
     int32_t *baked_pos;        // [P] first token position of the K in the page
     int32_t *delta_count;      // [P] delta rotations since the page's K was rebuilt
     int32_t *stamp;            // [max_blocks] epoch of the last step that selected it
-    int32_t epoch;             // this step's stamp (> every earlier one)
+    int32_t *epoch;            // the last step's epoch; the kernel counts it up
     int P;
     int64_t max_blocks;
     int delta_limit;

@@ -62,16 +62,20 @@ __device__ int block_scan(int n, F flag, O out, int *warp_tot) {
 __global__ void __launch_bounds__(kThreads, 1) residency_diff_kernel(ResidencyArgs a) {
     __shared__ int warp_tot[32];
     __shared__ int s_count[4];                      // hits, delta, evicted, bad ids
+    __shared__ int32_t s_epoch;
     const int tid = threadIdx.x;
     const int n = a.n_sel, P = a.P;
     if (tid < 4) s_count[tid] = 0;
+    // this step's stamp: one more than the last step's, counted on the device
+    if (tid == 0) s_epoch = ++*a.epoch;
     __syncthreads();
+    const int32_t epoch = s_epoch;
     // hits and the epoch stamp of every selected block
     for (int j = tid; j < n; j += kThreads) {
         const int32_t b = a.sel[j];
         int32_t p = -1;
         if (b >= 0 && b < a.max_blocks) {
-            a.stamp[b] = a.epoch;
+            a.stamp[b] = epoch;
             p = a.page_of_block[b];
         } else {
             atomicAdd(&s_count[3], 1);
@@ -90,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) residency_diff_kernel(ResidencyAr
         P,
         [&](int p) {
             const int32_t b = a.block_of_page[p];
-            return b < 0 || a.stamp[b] != a.epoch;
+            return b < 0 || a.stamp[b] != epoch;
         },
         [&](int p, int r) { a.free_list[r] = p; }, warp_tot);
     const int n_miss = n - s_count[0];
