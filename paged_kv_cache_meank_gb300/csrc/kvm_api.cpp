@@ -197,7 +197,7 @@ struct kvm_ctx {
     int64_t n_dev_steps = 0;
     struct Pending {
         kvm_step_stats *out;
-        int slot;
+        int64_t step;                    // its step number: ring slot step % kStatSlots
         int64_t n_blocks;
         int32_t n_sel;
     };
@@ -783,7 +783,7 @@ static kvm_status flush_pending(kvm_ctx *c) {
     const bool pull = c->cfg.repo_location == KVM_HOST_PINNED;
     const int64_t blk = (int64_t)block_bytes(c->cfg);
     for (const auto &pd : c->pending) {
-        const int32_t *k = ring + pd.slot * 8;
+        const int32_t *k = ring + (pd.step % kStatSlots) * 8;
         kvm_step_stats *st = pd.out;
         *st = kvm_step_stats{};
         st->n_blocks = pd.n_blocks;
@@ -806,8 +806,9 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
                               kvm_step_stats *stats, cudaStream_t s) {
     const kvm_config &cfg = c->cfg;
     cudaError_t e;
-    if (c->pending.size() >= (size_t)kStatSlots) {
-        // the counter ring is full: the oldest steps' counters go out first
+    if (!c->pending.empty() && c->n_dev_steps - c->pending.front().step >= kStatSlots) {
+        // this step's ring slot still holds the counters of a step waiting
+        // for them (steps without stats use slots too): copy them out first
         if (kvm_status st = flush_pending(c); st != KVM_OK) return st;
     }
     if (c->reset_pending) {
@@ -861,7 +862,7 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
         return abort_step(cuda_fail(e, "assemble launch"));
     KVM_CUDA(cudaEventRecord(c->ev_step, s));
     ++c->n_dev_steps;
-    if (stats) c->pending.push_back({stats, slot, n_blocks, n_sel});
+    if (stats) c->pending.push_back({stats, c->n_dev_steps - 1, n_blocks, n_sel});
     return KVM_OK;
 }
 

@@ -98,7 +98,8 @@ def test_steps_back_to_back_match_the_residency_rule(kvm, repo_host):
 
 def test_more_steps_than_the_counter_ring(kvm):
     """70 steps between two syncs: the oldest counters are copied out when the
-    64-slot ring is full, and every step's counters are right."""
+    64-slot ring is full, and every step's counters are right; steps without
+    a stats pointer do not overwrite a waiting step's counters."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID.with_(n_blocks=200, view_blocks=40)
     ws = workload.make_workspace(wl, seed=43)
@@ -109,6 +110,15 @@ def test_more_steps_than_the_counter_ring(kvm):
     assert stats[0]["misses"] == wl.view_blocks and stats[0]["hits"] == 0
     for st in stats[1:]:       # the same queries again: every block is a resident hit
         assert (st["hits"], st["misses"], st["reroped"]) == (wl.view_blocks, 0, 0)
+    # a step with stats, then 70 steps without (a NULL stats pointer still
+    # takes a ring slot): the first step's counters survive until the sync
+    ctx.reset_pool()
+    first = ctx.step(q, wl.n_queries, wl.n_blocks)
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(70):
+        assert ctx.lib.kvm_step(ctx.handle, q.data_ptr(), wl.n_queries, wl.n_blocks, None, s) == 0
+    ctx.sync()
+    assert (first["misses"], first["hits"]) == (wl.view_blocks, 0)
 
 
 def test_failed_launch_empties_the_pool(kvm):
