@@ -107,6 +107,21 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
         for (int k = 0; k < 32; ++k) tc::mbar_init(&xfull[k], 32);
         tc::fence_mbar_init();
     }
+    // the producer's first ring entries go out now, so that their HBM latency
+    // overlaps the staging of the query rows below (the stages are free)
+    const int n_load = sh.idle_producer ? 0 : n_tiles;   // an idle producer issues nothing
+    const int n_pre = min(n_load, kStages);
+    auto issue = [&](int i) {
+        const int s = i % kStages;
+        tc::mbar_expect_tx(&full[s], LY::TILE);
+        const int32_t y =
+            (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
+#pragma unroll
+        for (int a = 0; a < LY::KA; ++a)
+            tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s], a * 64, y);
+    };
+    if (tid == 0)
+        for (int i = 0; i < n_pre; ++i) issue(i);
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
@@ -156,20 +171,12 @@ score_tc_pass2_kernel(const __grid_constant__ CUtensorMap tmap,
 
     if (warp == 0) {
         if (lane == 0) {
-            // an idle producer (a test of the bounded waits) issues nothing
-            const int n_load = sh.idle_producer ? 0 : n_tiles;
-            int issued = 0;
-            for (int i = 0; i < n_load; ++i) {
+            int issued = n_pre;
+            for (int i = n_pre; i < n_load; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
                 if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitNs)) { atomicOr(err, 4); break; }
-                tc::mbar_expect_tx(&full[s], LY::TILE);
-                const int32_t y =
-                    (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
-#pragma unroll
-                for (int a = 0; a < LY::KA; ++a)
-                    tc::tma_load_2d(tiles + s * LY::TILE + a * LY::ATOM_TILE, &tmap, &full[s],
-                                    a * 64, y);
+                issue(i);
                 ++issued;
             }
             // every issued copy lands before the CTA ends: wait for the last

@@ -107,6 +107,21 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
         for (int k = 0; k < 2; ++k) tc::mbar_init(&xdbar[k], 32);
         tc::fence_mbar_init();
     }
+    // ring entry e = (tile, K atom) = (e / KA, e % KA); the producer's first
+    // entries go out now, so that their HBM latency overlaps the staging of the
+    // query rows below (the stages are free)
+    const int n_entries = (sh.idle_producer ? 0 : n_tiles) * LY::KA;   // an idle producer issues nothing
+    const int n_pre = min(n_entries, LY::STAGES);
+    auto issue = [&](int e) {
+        const int i = e / LY::KA, a = e - i * LY::KA;
+        const int s = e % LY::STAGES;
+        const int32_t y =
+            (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
+        tc::mbar_expect_tx(&full[s], LY::ATOM_TILE);
+        tc::tma_load_2d(tiles + s * LY::ATOM_TILE, &tmap, &full[s], a * 64, y);
+    };
+    if (tid == 0)
+        for (int e = 0; e < n_pre; ++e) issue(e);
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
@@ -157,21 +172,15 @@ score_tc_pass1_kernel(const __grid_constant__ CUtensorMap tmap,
 
     if (warp == 0) {
         if (lane == 0) {
-            // an idle producer (a test of the bounded waits) issues nothing
-            const int n_load = sh.idle_producer ? 0 : n_tiles;
-            int issued = 0;                         // ring entries
-            for (int i = 0; i < n_load; ++i) {
-                const int32_t y =
-                    (int32_t)((int64_t)lg * sh.index_cap + (cb0 + (int64_t)i * TB - b_index0));
-                bool ok = true;
-                for (int a = 0; a < LY::KA && ok; ++a) {
-                    const int2 e = ring(i, a);
-                    if (!tc::mbar_wait(&empty[e.x], e.y ^ 1, kWaitNs)) { ok = false; break; }
-                    tc::mbar_expect_tx(&full[e.x], LY::ATOM_TILE);
-                    tc::tma_load_2d(tiles + e.x * LY::ATOM_TILE, &tmap, &full[e.x], a * 64, y);
-                    ++issued;
+            int issued = n_pre;                     // ring entries
+            for (int e = n_pre; e < n_entries; ++e) {
+                const int2 r = ring(e / LY::KA, e % LY::KA);
+                if (!tc::mbar_wait(&empty[r.x], r.y ^ 1, kWaitNs)) {
+                    atomicOr(err, 4);
+                    break;
                 }
-                if (!ok) { atomicOr(err, 4); break; }
+                issue(e);
+                ++issued;
             }
             // every issued copy lands before the CTA ends: wait for the last
             // use of each ring stage (at once in a run without errors)
