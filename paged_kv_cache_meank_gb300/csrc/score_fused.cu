@@ -1,8 +1,15 @@
 // Tensor-core (tcgen05) scoring of Eq. (10), KVMem (Virtualizing Million-Token
-// Agent Workspaces on a Consumer GPU) §4.3, in one persistent launch: both
-// passes of the exact softmax over all candidate blocks, with the second pass
-// reading a (layer, kv head) slice of the Mean-K index again while it is still
-// in L2, so that the index crosses HBM once.
+// Agent Workspaces on a Consumer GPU) §4.3, in one persistent launch
+// (score_variant 2): both passes of the exact softmax over all candidate
+// blocks, with the second pass re-reading a (layer, kv head) slice of the
+// Mean-K index soon after the first, so that it can come from L2.
+//
+// Measured on GB300 this variant is slower than the two-pass kernels
+// (score_tc1.cu, score_tc.cu), which stay the default: with enough slices in
+// flight to fill the GPU the data touched between a tile's two reads exceeds
+// what L2 keeps (a 1.07 GB index still drew 2.02 GB from DRAM), a 10M-block
+// slice alone is 80 MB, and the per-slice group sync costs several
+// microseconds.  Both passes are bound by their exponentials in any case.
 //
 // The softmax of a query row runs over every block of its (layer l, kv head g)
 // slice, so pass 2 of a slice can start only once pass 1 has seen the whole
