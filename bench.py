@@ -233,12 +233,41 @@ class Step:
         K = args.extra_steps
         ms, parts, n_launches, clk = time_steps(r, K, args.warmup, dev, self.stream, dist)
         st = r.stats[-K:]
+        # the same step captured once into a CUDA graph and launched from it
+        # (the host enqueues one graph instead of seven kernels)
+        kvm = self.kvm
+        n0 = kvm.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=self.stream):
+            self.ctx.step(self.q, wl.n_queries, wl.n_blocks, stream=self.stream)
+        per_launch = kvm.launch_count() - n0
+
+        class GraphRecall:
+            parts = ["step"]
+
+            def run(self, ev=None):
+                outer.ctx.reset_pool()
+                if ev:
+                    ev[0].record(outer.stream)
+                with torch.cuda.stream(outer.stream):   # a graph launches on the current stream
+                    graph.replay()
+                if ev:
+                    ev[1].record(outer.stream)
+
+        gr = GraphRecall()
+        gr.ctx = self.ctx
+        _, gparts, _, gclk = time_steps(gr, K, args.warmup, dev, self.stream, dist)
+        del graph
         return {"ms": parts["step"], "steps": K, "gpu_launches": n_launches, "clocks": clk,
                 "definition": "kvm_step on the HBM-resident workspace, queries ready to page "
                               "table written (CUDA events; the residency diff runs on the GPU "
                               "between the selection and the assembly)",
                 "misses": float(np.mean([x["misses"] for x in st])),
-                "hits": float(np.mean([x["hits"] for x in st]))}
+                "hits": float(np.mean([x["hits"] for x in st])),
+                "graph": {"ms": gparts["step"], "gpu_launches": per_launch * K,
+                          "clocks_sm_mhz": gclk.get("sm_mhz") if isinstance(gclk, dict) else None,
+                          "definition": "the same kvm_step captured once into a CUDA graph, "
+                                        "each step one graph launch after the pool reset"}}
 
     def close(self):
         self.ctx.close()

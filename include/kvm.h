@@ -298,6 +298,16 @@ typedef struct {
  * the rest enqueued and fills `stats` before returning.  Both diffs give the
  * same pages.  kvm_bind and kvm_reset_pool empty the pool; they must not be
  * called while another thread enqueues a step on the same context.
+ * CUDA graphs: a step with the residency diff on the device and the index in
+ * device memory may be enqueued while `stream` is being captured; each launch
+ * of the graph then runs one step on the query buffer `q` as it holds at
+ * launch time, against the residency as the steps before it left it.  Such a
+ * step takes stats = NULL (its counters are not reported), waits at every
+ * launch for the latest kvm_reset_pool and kvm_stage_out, and a later
+ * kvm_reset_pool orders its clearing after the launches already enqueued.
+ * Steps, eager or launched from graphs, must follow one another on one stream.
+ * Errors under capture: KVM_ERR_INVALID_ARG when the diff runs on the host,
+ * the index is host-resident, or stats is not NULL; nothing is enqueued then.
  */
 kvm_status kvm_step(kvm_ctx *ctx, const void *q, int32_t n_queries, int64_t n_blocks,
                     kvm_step_stats *stats, kvm_stream stream);

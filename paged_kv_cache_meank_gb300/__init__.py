@@ -248,9 +248,17 @@ class Context:
     def reset_pool(self) -> None:
         check(self.lib.kvm_reset_pool(self.handle), "kvm_reset_pool")
 
-    def step(self, q, n_queries: int, n_blocks: int, stream=None) -> "StepStats":
+    def step(self, q, n_queries: int, n_blocks: int, stream=None, stats=None):
         """One kvm_step.  The returned counters are final once sync() returns
-        (a step whose residency diff runs on the device fills them then)."""
+        (a step whose residency diff runs on the device fills them then).
+        With stats=False, or by default while the current stream is being
+        captured into a CUDA graph, no counters are kept and None is returned."""
+        if stats is None:
+            stats = not (torch.cuda.is_available() and torch.cuda.is_current_stream_capturing())
+        if not stats:
+            check(self.lib.kvm_step(self.handle, _ptr(q), n_queries, n_blocks, None,
+                                    _stream(stream)), "kvm_step")
+            return None
         st = KvmStepStats()
         check(self.lib.kvm_step(self.handle, _ptr(q), n_queries, n_blocks, ctypes.byref(st),
                                 _stream(stream)), "kvm_step")

@@ -143,9 +143,10 @@ Layout layout_of(const kvm_config *c) {
     lo.sel = take(kvm::select_scratch_bytes());
     // the device-side residency of kvm_step (int32 each): page_of_block and
     // stamp per block; block_of_page, baked_pos, delta_count and a free list
-    // per page; a page per slot; kStatSlots steps of counters
+    // per page; a page per slot; kStatSlots steps of counters and one slot
+    // for steps captured into a CUDA graph
     lo.resid = take(((size_t)2 * c->max_blocks + (size_t)4 * c->pool_pages + c->view_blocks +
-                     (size_t)kStatSlots * 8 + 1) *
+                     (size_t)(kStatSlots + 1) * 8 + 1) *
                     sizeof(int32_t));
     lo.err = take(256);
     lo.total = off;
@@ -195,6 +196,7 @@ struct kvm_ctx {
             *d_baked_pos = nullptr, *d_delta_count = nullptr, *d_free_list = nullptr,
             *d_slot_page = nullptr, *d_counts = nullptr, *d_epoch = nullptr;
     int64_t n_dev_steps = 0;
+    bool graph_steps = false;            // a step was captured into a CUDA graph
     struct Pending {
         kvm_step_stats *out;
         int64_t step;                    // its step number: ring slot step % kStatSlots
@@ -204,6 +206,7 @@ struct kvm_ctx {
     std::vector<Pending> pending;        // steps whose counters kvm_sync copies out
     cudaEvent_t ev_reset = nullptr;      // the device residency was cleared on the copy stream
     cudaEvent_t ev_step = nullptr;       // the last device-diff step's work is enqueued
+                                         // (eagerly, or by a graph launch)
     bool reset_pending = false;
     kvm_tier *tier = nullptr;            // host-tier policy (host_tier_blocks > 0)
     // fault injection
@@ -252,7 +255,7 @@ cudaError_t reset_device(kvm_ctx *c, cudaStream_t after, bool has_after) {
         if ((e = cudaEventRecord(c->ev_main, after)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0)) != cudaSuccess)
             return e;
-    } else if (c->n_dev_steps > 0 &&
+    } else if ((c->n_dev_steps > 0 || c->graph_steps) &&
                (e = cudaStreamWaitEvent(c->copy_stream, c->ev_step, 0)) != cudaSuccess) {
         return e;   // after the last step enqueued
     }
@@ -278,6 +281,15 @@ void reset_pool(kvm_ctx *c, cudaStream_t after = nullptr, bool has_after = false
 }
 
 }  // namespace
+
+// Whether `s` is being captured into a CUDA graph.
+static kvm_status stream_capturing(cudaStream_t s, bool *capturing) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "stream capture status");
+    *capturing = cs == cudaStreamCaptureStatusActive;
+    return KVM_OK;
+}
 
 // The address a kernel uses for a caller buffer: device (or managed) memory as
 // is; pinned host memory through its device alias, so that kernels read or
@@ -365,7 +377,7 @@ kvm_status kvm_create(const kvm_config *cfg, void *workspace, size_t workspace_b
         c->d_free_list = c->d_delta_count + cfg->pool_pages;
         c->d_slot_page = c->d_free_list + cfg->pool_pages;
         c->d_counts = c->d_slot_page + cfg->view_blocks;
-        c->d_epoch = c->d_counts + kStatSlots * 8;
+        c->d_epoch = c->d_counts + (kStatSlots + 1) * 8;
     }
     // the diff runs on the device when the kernels read the repository
     // themselves; copy-engine transfers and the host-tier policy need the
@@ -608,6 +620,15 @@ kvm_status kvm_score_select(kvm_ctx *c, const void *q, int32_t n_queries, const 
         }
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c->cfg.index_location != KVM_DEVICE) {
+        // the tiled path orders its staging buffers with events recorded by
+        // earlier calls, which a graph launch would not see
+        bool capturing = false;
+        if ((st = stream_capturing(s, &capturing)) != KVM_OK) return st;
+        if (capturing)
+            return fail(KVM_ERR_INVALID_ARG,
+                        "scoring a host-resident index cannot be captured into a CUDA graph");
+    }
     const kvm::ScoreShape sh = shape_of(c, n_queries, c->cfg.max_blocks);
     int64_t c0 = 0, c1 = n_blocks;
     if (c->cfg.candidate_mode == 1) {
@@ -802,24 +823,38 @@ static kvm_status flush_pending(kvm_ctx *c) {
 // kvm_step when the residency diff runs on the device (the repository in
 // device memory, or in pinned host memory read by the GPU): selection ->
 // diff -> assembly, all enqueued on the stream with no wait on the host.
+//
+// Under stream capture the step becomes part of the caller's CUDA graph, and
+// each launch of the graph runs one step.  Its ordering with the host-issued
+// work of the context then has to hold at every launch, not at capture time:
+// the step waits on the latest pool reset (and stage-out) through external
+// event-wait nodes, and records ev_step through an external record node, so
+// that a later kvm_reset_pool orders its clearing after the launches already
+// enqueued.  Its counters go to a slot of their own and are not reported.
 static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
-                              kvm_step_stats *stats, cudaStream_t s) {
+                              kvm_step_stats *stats, cudaStream_t s, bool capturing) {
     const kvm_config &cfg = c->cfg;
     cudaError_t e;
-    if (!c->pending.empty() && c->n_dev_steps - c->pending.front().step >= kStatSlots) {
-        // this step's ring slot still holds the counters of a step waiting
-        // for them (steps without stats use slots too): copy them out first
-        if (kvm_status st = flush_pending(c); st != KVM_OK) return st;
-    }
-    if (c->reset_pending) {
-        KVM_CUDA(cudaStreamWaitEvent(s, c->ev_reset, 0));
-        c->reset_pending = false;
-    }
-    const int slot = (int)(c->n_dev_steps % kStatSlots);
     const bool pull = cfg.repo_location == KVM_HOST_PINNED;
+    if (capturing) {
+        KVM_CUDA(cudaStreamWaitEvent(s, c->ev_reset, cudaEventWaitExternal));
+        if (pull) KVM_CUDA(cudaStreamWaitEvent(s, c->ev_stage, cudaEventWaitExternal));
+    } else {
+        if (!c->pending.empty() && c->n_dev_steps - c->pending.front().step >= kStatSlots) {
+            // this step's ring slot still holds the counters of a step waiting
+            // for them (steps without stats use slots too): copy them out first
+            if (kvm_status st = flush_pending(c); st != KVM_OK) return st;
+        }
+        if (c->reset_pending) {
+            KVM_CUDA(cudaStreamWaitEvent(s, c->ev_reset, 0));
+            c->reset_pending = false;
+        }
+    }
+    const int slot = capturing ? kStatSlots : (int)(c->n_dev_steps % kStatSlots);
     auto abort_step = [&](kvm_status err) {
-        // the diff may have run: forget the whole pool, after this stream's work
-        reset_pool(c, s, true);
+        // the diff may have run: forget the whole pool, after this stream's
+        // work (a captured step ran nothing: the pool is as it was)
+        if (!capturing) reset_pool(c, s, true);
         return err;
     };
     kvm::ResidencyArgs a{};
@@ -850,7 +885,7 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
     if (injected(c, 2)) return abort_step(fail(KVM_ERR_INJECTED, "injected launch failure"));
     if ((e = kvm::launch_residency_diff(a, s)) != cudaSuccess)
         return abort_step(cuda_fail(e, "residency diff launch"));
-    if (pull && c->staged) {
+    if (pull && c->staged && !capturing) {
         // the kernel reads the host repository: order it after earlier stage-outs
         if ((e = cudaStreamWaitEvent(s, c->ev_stage, 0)) != cudaSuccess)
             return abort_step(cuda_fail(e, "stage-out wait"));
@@ -860,6 +895,11 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
                                            a.counts, cfg.n_layers * cfg.n_kv_heads, c->table,
                                            cfg.max_positions, c->err_dev, s)) != cudaSuccess)
         return abort_step(cuda_fail(e, "assemble launch"));
+    if (capturing) {
+        KVM_CUDA(cudaEventRecordWithFlags(c->ev_step, s, cudaEventRecordExternal));
+        c->graph_steps = true;
+        return KVM_OK;
+    }
     KVM_CUDA(cudaEventRecord(c->ev_step, s));
     ++c->n_dev_steps;
     if (stats) c->pending.push_back({stats, c->n_dev_steps - 1, n_blocks, n_sel});
@@ -870,11 +910,23 @@ static kvm_status step_body(kvm_ctx *c, const void *q, int32_t n_queries, int64_
                             kvm_step_stats *stats, kvm_stream stream) {
     const kvm_config &cfg = c->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool capturing = false;
+    if (kvm_status cst = stream_capturing(s, &capturing); cst != KVM_OK) return cst;
+    if (capturing) {
+        // only a step that enqueues everything with no wait on the host can
+        // become part of a graph
+        if (!c->device_diff)
+            return fail(KVM_ERR_INVALID_ARG,
+                        "kvm_step under stream capture needs the residency diff on the device "
+                        "(repository in device memory, or pinned and read by the GPU; no host tier)");
+        if (stats)
+            return fail(KVM_ERR_INVALID_ARG, "kvm_step under stream capture takes stats = NULL");
+    }
     int32_t n_sel = 0;
     kvm_status st = kvm_score_select(c, q, n_queries, c->bufs.index, n_blocks, c->bufs.scores,
                                      c->bufs.sel_ids, &n_sel, stream);
     if (st != KVM_OK) return st;
-    if (c->device_diff) return step_device(c, n_blocks, n_sel, stats, s);
+    if (c->device_diff) return step_device(c, n_blocks, n_sel, stats, s, capturing);
 
     // the selected ids drive the host-side residency diff
     std::vector<int32_t> sel(n_sel);

@@ -25,12 +25,12 @@ def kvm():
     return kvm
 
 
-def _context(kvm, wl, ws, repo_host, h2d_mode, seed_q):
+def _context(kvm, wl, ws, repo_host, h2d_mode, seed_q, **cfg_kw):
     """A bound context over the workspace, plus its pool and outputs."""
     N = wl.n_blocks
     cfg = kvm.config_for(wl, pool_pages=wl.view_blocks + 6,
                          repo_location=kvm.KVM_HOST_PINNED if repo_host else kvm.KVM_DEVICE,
-                         h2d_mode=h2d_mode)
+                         h2d_mode=h2d_mode, **cfg_kw)
     ctx = kvm.Context(cfg)
     kp = prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta)
     index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
