@@ -368,12 +368,14 @@ class HostStep:
     blocks are misses."""
     parts = ["step"]
 
-    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0, index_spill=1):
+    def __init__(self, wl, seed, device, stream, score_variant=0, h2d_mode=0, index_spill=1,
+                 spill_tiles=0):
         import paged_kv_cache_meank_gb300 as kvm
         self.kvm, self.wl, self.dev, self.stream = kvm, wl, device, stream
         self.score_variant, self.h2d_mode = score_variant, h2d_mode
         self.index_spill = index_spill if wl.index_loc == "host" else 0
-        cfg = self._config(self.index_spill)
+        self.spill_tiles = spill_tiles if self.index_spill else 0
+        cfg = self._config(self.index_spill, self.spill_tiles)
         self.ctx = kvm.Context(cfg, device=device, stream=stream)
         (self.raw_h, self.v_h, self.index, self.planted, u, _, _) = build_host_workspace(
             kvm, wl, seed, device, stream, self.ctx, wl.n_blocks, wl.index_loc == "host")
@@ -389,20 +391,20 @@ class HostStep:
         self._bind()
         self.stats = []
 
-    def _config(self, spill):
+    def _config(self, spill, spill_tiles=0):
         kvm, wl = self.kvm, self.wl
         return kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED,
                               index_location=kvm.KVM_HOST_PINNED if wl.index_loc == "host"
                               else kvm.KVM_DEVICE, h2d_batch_blocks=256,
                               score_variant=self.score_variant, h2d_mode=self.h2d_mode,
-                              index_spill=spill)
+                              index_spill=spill, spill_tiles=spill_tiles)
 
     def _bind(self):
         self.ctx.bind(index=self.index, raw_k=self.raw_h, v=self.v_h, pool_k=self.pool_k,
                       pool_v=self.pool_v, pool_raw_k=self.pool_raw, page_table=self.page_table,
                       scores=self.scores, sel_ids=self.sel)
 
-    def respill(self, spill):
+    def respill(self, spill, spill_tiles=0):
         """The same workspace under a new context with another index_spill
         setting; this step's context is closed and the returned step owns the
         host buffers."""
@@ -410,8 +412,9 @@ class HostStep:
         other = copy.copy(self)
         self.ctx.close()
         other.index_spill = spill if self.wl.index_loc == "host" else 0
-        other.ctx = self.kvm.Context(other._config(other.index_spill), device=self.dev,
-                                     stream=self.stream)
+        other.spill_tiles = spill_tiles if other.index_spill else 0
+        other.ctx = self.kvm.Context(other._config(other.index_spill, other.spill_tiles),
+                                     device=self.dev, stream=self.stream)
         other._bind()
         other.stats = []
         return other
@@ -441,13 +444,20 @@ class HostStep:
 
     def link_bytes(self):
         """Host-to-device bytes of one step: the index tiles (when the index is in
-        host memory: streamed once with index_spill, else once per scoring pass)
+        host memory: streamed once with index_spill, else once per scoring pass;
+        under a budget of m kept tiles of T, all but min(m, T) tiles twice)
         plus the missed blocks' raw K and V."""
         wl = self.wl
         idx = 0
         if wl.index_loc == "host":
-            idx = (1 if self.index_spill else 2) * wl.n_layers * wl.n_kv_heads * wl.n_blocks * \
-                wl.head_dim * 2
+            tile = self.ctx.cfg.tile_blocks
+            T = -(-wl.n_blocks // tile)
+            kept = (T if not self.spill_tiles else min(self.spill_tiles, T)) \
+                if self.index_spill else 0
+            # blocks of the tiles that cross the link a second time: every
+            # tile but the last `kept`, which hold the ragged end
+            again = wl.n_blocks if kept == 0 else (T - kept) * tile
+            idx = (wl.n_blocks + again) * wl.n_layers * wl.n_kv_heads * wl.head_dim * 2
         return idx + float(np.mean([s["h2d_bytes"] for s in self.stats[-8:]]))
 
     def cpu_sample(self, layers):
@@ -757,6 +767,7 @@ def bench_ours(args, wl, world, rank, local, dist):
 # index kept in HBM after its first crossing), the 10M-token scoring step and
 # the multi-step churn on its 16-layer slice.
 EXTRA = [("q27x16-1m", {"index_spill": 0}), ("q27x16-1m", {"index_spill": 1}),
+         ("q27x16-1m", {"index_spill": 1, "spill_tiles": 16}),
          ("q27-10m-score", {}), ("q27x16-512k-churn", {})]
 
 
@@ -768,7 +779,7 @@ def bench_extra(args, world, rank, dev, stream, dist):
         wl = configs.ALL[name]
         t_setup = time.perf_counter()
         if host_share is not None and name == host_share.wl.name:
-            step = host_share.respill(extra["index_spill"])
+            step = host_share.respill(extra["index_spill"], extra.get("spill_tiles", 0))
         else:
             if host_share is not None:
                 host_share.close()
@@ -779,7 +790,8 @@ def bench_extra(args, world, rank, dev, stream, dist):
         ms, parts, n_launches, clk = time_steps(step, K, args.warmup, dev, stream, dist)
         comps, roof = summarize(wl, step, ms, parts, clk, dev, stream)
         key = name + ("" if "index_spill" not in extra else
-                      ("-spill" if extra["index_spill"] else "-bounded"))
+                      ("-bounded" if not extra["index_spill"] else
+                       f"-spill{extra['spill_tiles']}" if extra.get("spill_tiles") else "-spill"))
         out[key] = {"value": job_throughput(world, wl.n_blocks, ms), "unit": "scored blocks/s",
                     "ms_per_step": ms, "steps": K, "warmup": args.warmup,
                     "config": {**workload_config(wl, world), **extra},

@@ -132,6 +132,13 @@ typedef struct {
                                     (the workspace then holds a copy of the whole
                                     index) and pass 2 reads it there, so each step
                                     moves the index over the link once. */
+    int32_t spill_tiles;     /* with index_spill = 1: 0 = keep every tile; m > 0 =
+                                keep at most m tiles (the last m of pass 1), which
+                                pass 2 scores first while the other tiles cross the
+                                link again through the two streaming buffers.  The
+                                workspace then holds m + 2 tiles, and a step moves
+                                (2T - min(m, T)) / T index reads over the link for T
+                                tiles.  Results do not depend on m. */
 } kvm_config;
 
 typedef struct kvm_ctx kvm_ctx;
@@ -139,7 +146,8 @@ typedef struct kvm_ctx kvm_ctx;
 /* Device workspace bytes a context needs for `cfg` (RoPE table, scoring
  * scratch including that of the one-launch variant, a copy of the queries for
  * a device index when they are passed in host memory, index staging tiles --
- * two, or one per index tile with index_spill -- step descriptors and the
+ * two, one per index tile with index_spill, or spill_tiles + 2 -- step
+ * descriptors and the
  * device-side residency of the page pool).  0 if cfg is invalid. */
 size_t kvm_workspace_bytes(const kvm_config *cfg);
 

@@ -39,14 +39,16 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
                max_queries: int | None = None, score_variant: int = 0,
                h2d_mode: int = 1, delta_rerope_limit: int = 0,
                candidate_mode: int = 0, host_tier_blocks: int = 0,
-               host_tier_lambda: float = 0.5, index_spill: int = 0) -> KvmConfig:
+               host_tier_lambda: float = 0.5, index_spill: int = 0,
+               spill_tiles: int = 0) -> KvmConfig:
     """A kvm_config for a workload shape.  With a host-resident repository the
     GPU reads missed blocks from pinned host memory itself (h2d_mode 1) unless
     h2d_mode=0 asks for copy-engine transfers.  candidate_mode=1 leaves sink and
     recent blocks out of the Eq. (10) softmax.  host_tier_blocks > 0 runs the
     host-tier policy (kvm_tier_step) over every step's selection.  index_spill=1
     makes a host-resident index cross the host link once per scoring call
-    instead of once per pass."""
+    instead of once per pass; spill_tiles=m > 0 caps the tiles it keeps in
+    device memory at m, and pass 2 re-streams the others."""
     mb = max_blocks if max_blocks is not None else wl.n_blocks + wl.steps * wl.append_blocks
     mp = max_positions if max_positions is not None else max(mb, wl.view_blocks) * BLOCK_TOKENS
     il = index_location if index_location is not None else (
@@ -64,7 +66,7 @@ def config_for(wl: Workload, *, max_blocks: int | None = None, max_positions: in
         index_location=il, repo_location=rl, h2d_batch_blocks=h2d_batch_blocks,
         h2d_mode=h2d_mode, score_variant=score_variant, delta_rerope_limit=delta_rerope_limit,
         candidate_mode=candidate_mode, host_tier_blocks=host_tier_blocks,
-        host_tier_lambda=host_tier_lambda, index_spill=index_spill)
+        host_tier_lambda=host_tier_lambda, index_spill=index_spill, spill_tiles=spill_tiles)
 
 
 def _ptr(t) -> int | None:

@@ -32,7 +32,7 @@ class KvmConfig(ctypes.Structure):
         ("h2d_mode", ctypes.c_int32), ("score_variant", ctypes.c_int32),
         ("delta_rerope_limit", ctypes.c_int32), ("candidate_mode", ctypes.c_int32),
         ("host_tier_blocks", ctypes.c_int64), ("host_tier_lambda", ctypes.c_double),
-        ("index_spill", ctypes.c_int32),
+        ("index_spill", ctypes.c_int32), ("spill_tiles", ctypes.c_int32),
     ]
 
 

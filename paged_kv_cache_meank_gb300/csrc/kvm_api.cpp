@@ -53,10 +53,11 @@ size_t elt_bytes(int dt) { return dt == KVM_E4M3 ? 1 : dt == KVM_BF16 ? 2 : 4; }
 constexpr int kStatSlots = 64;   // steps whose counters can wait for kvm_sync
 
 struct Layout {
-    size_t table, part_m, part_z, row_m, row_invz, partial, fused, qstage, stage0, stage1, desc,
-        sel, resid, err, total;
+    size_t table, part_m, part_z, row_m, row_invz, partial, fused, qstage, stage0, stage1, keep,
+        desc, sel, resid, err, total;
     size_t qstage_bytes;
     size_t stage_bytes;
+    int64_t keep_tiles;   // index tiles pass 1 keeps in device memory for pass 2
     int rows_max, chunk_cap;
 };
 
@@ -99,6 +100,8 @@ bool config_ok(const kvm_config *c, std::string *why) {
     if (c->host_tier_blocks > 0 && !(c->host_tier_lambda >= 0.0 && c->host_tier_lambda <= 1.0))
         return bad("host_tier_lambda must be in [0, 1]");
     if (c->index_spill != 0 && c->index_spill != 1) return bad("index_spill must be 0 or 1");
+    if (c->spill_tiles < 0) return bad("spill_tiles must be >= 0");
+    if (c->spill_tiles > 0 && !c->index_spill) return bad("spill_tiles needs index_spill = 1");
     return true;
 }
 
@@ -130,14 +133,21 @@ Layout layout_of(const kvm_config *c) {
     lo.stage_bytes = 0;
     if (c->index_location == KVM_HOST_PINNED)
         lo.stage_bytes = LG * (size_t)c->tile_blocks * c->head_dim * elt_bytes(c->index_dtype);
-    if (c->index_location == KVM_HOST_PINNED && c->index_spill) {
+    lo.keep_tiles = 0;
+    const int64_t tiles = (c->max_blocks + c->tile_blocks - 1) / c->tile_blocks;
+    if (c->index_location == KVM_HOST_PINNED && c->index_spill &&
+        (c->spill_tiles == 0 || c->spill_tiles >= tiles)) {
         // one staging tile per index tile: pass 2 reads what pass 1 staged
-        const int64_t tiles = (c->max_blocks + c->tile_blocks - 1) / c->tile_blocks;
-        lo.stage0 = take(lo.stage_bytes * (size_t)tiles);
-        lo.stage1 = lo.stage0;
+        lo.keep_tiles = tiles;
+        lo.keep = lo.stage0 = lo.stage1 = take(lo.stage_bytes * (size_t)tiles);
     } else {
+        // two streaming tiles, and with a spill budget the tiles pass 1 keeps
         lo.stage0 = take(lo.stage_bytes);
         lo.stage1 = take(lo.stage_bytes);
+        if (c->index_location == KVM_HOST_PINNED && c->index_spill) {
+            lo.keep_tiles = c->spill_tiles;
+            lo.keep = take(lo.stage_bytes * (size_t)lo.keep_tiles);
+        }
     }
     lo.desc = take((size_t)(c->pool_pages + c->view_blocks) * sizeof(kvm::SlotDesc));
     lo.sel = take(kvm::select_scratch_bytes());
@@ -531,8 +541,11 @@ static kvm_status score_device(kvm_ctx *c, const kvm::ScoreShape &sh, const void
 // buffers on the copy stream; the softmax stays global because pass 1 only
 // records per-chunk (max, sum) and the combine folds every tile's chunks
 // before pass 2 re-streams the tiles (KVMem §5, tiled retrieval).  With
-// index_spill every tile has its own staging buffer: pass 1 copies each tile
-// once and pass 2 reads the staged tiles without copying again.
+// index_spill the last m tiles of pass 1 (every tile, or at most spill_tiles)
+// stay in buffers of their own: pass 2 scores them first, with no copy, while
+// the copy stream re-streams the other tiles through the two buffers.  A
+// block's pass-2 sum depends only on its own tile, so the order of pass 2
+// does not change any result.
 static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q,
                                    const void *index, int64_t N, int64_t c0, int64_t c1,
                                    float *scores, cudaStream_t s) {
@@ -548,22 +561,26 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
     KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_main, 0));
     kvm::ScoreShape tsh = sh;
     tsh.index_cap = tile;
-    const bool spill = c->cfg.index_spill != 0;
+    // tiles first_kept .. T-1 keep their pass-1 copy
+    const int64_t m = std::min<int64_t>(c->lo.keep_tiles, T), first_kept = T - m;
     for (int pass = 1; pass <= 2 && c1 > c0; ++pass) {
-        for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < T; ++i) {
+            // pass 2 takes the kept tiles first
+            const int64_t t = pass == 1 ? i : (i < m ? first_kept + i : i - m);
+            const bool kept = t >= first_kept;
             const int buf = (int)(t & 1);
             const int64_t b0 = t * tile, nb = std::min(tile, N - b0);
             // the tile's part of the candidate range; an empty part still runs
             // pass 1 so that its chunks hold (-inf, 0) for the combine
             const int64_t lo = std::min(std::max(b0, c0), b0 + nb);
             const int64_t hi = std::max(std::min(b0 + nb, c1), lo);
-            void *tile_buf = spill ? static_cast<char *>(c->stage[0]) + (size_t)t * c->lo.stage_bytes
-                                   : c->stage[buf];
-            if (!spill || pass == 1) {
-                // a spilled tile's buffer is not reused within the call; the
-                // copy stream joined the caller's stream at the start, after
-                // the previous call's pass 2
-                if (!spill) KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
+            void *tile_buf = kept ? c->ws + c->lo.keep + (size_t)(t - first_kept) * c->lo.stage_bytes
+                                  : c->stage[buf];
+            if (!kept || pass == 1) {
+                // a kept tile's buffer is not reused within the call; the copy
+                // stream joined the caller's stream at the start, after the
+                // previous call's pass 2
+                if (!kept) KVM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_free[buf], 0));
                 KVM_CUDA(cudaMemcpy2DAsync(tile_buf, tile * row,
                                            static_cast<const char *>(index) + b0 * row,
                                            (size_t)c->cfg.max_blocks * row, nb * row, LG,
@@ -582,7 +599,7 @@ static kvm_status score_host_tiled(kvm_ctx *c, kvm::ScoreShape sh, const void *q
                                             tile_buf, b0, lo, hi, cpt, c->scr,
                                             c->cfg.max_blocks, s);
             if (e != cudaSuccess) return cuda_fail(e, "tiled score pass");
-            if (!spill) KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
+            if (!kept) KVM_CUDA(cudaEventRecord(c->ev_free[buf], s));
         }
         if (pass == 1 && (e = kvm::launch_score_combine(sh, (int)(T * cpt), c->scr, s)) != cudaSuccess)
             return cuda_fail(e, "score combine");

@@ -14,7 +14,8 @@ from recall_ref import prefill_k_pages
 
 
 def run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_step,
-               pool_extra=6, batch=7, h2d_mode=0, host_tier=None, index_spill=0):
+               pool_extra=6, batch=7, h2d_mode=0, host_tier=None, index_spill=0,
+               spill_tiles=0):
     from paged_kv_cache_meank_gb300 import workload
     N_max = max(n_blocks_per_step)
     ws = workload.make_workspace(wl, seed=11, n_blocks=N_max, with_q=False)
@@ -27,7 +28,8 @@ def run_steps(kvm, wl, repo_host: bool, index_host: bool, queries, n_blocks_per_
         index_location=kvm.KVM_HOST_PINNED if index_host else kvm.KVM_DEVICE,
         h2d_batch_blocks=batch, h2d_mode=h2d_mode,
         host_tier_blocks=host_tier[0] if host_tier else 0,
-        host_tier_lambda=host_tier[1] if host_tier else 0.5, index_spill=index_spill)
+        host_tier_lambda=host_tier[1] if host_tier else 0.5, index_spill=index_spill,
+        spill_tiles=spill_tiles)
     cfg.tile_blocks = 64
     tier_ref = oracle_tier.HostTier(*host_tier) if host_tier else None
     ctx = kvm.Context(cfg)

@@ -47,7 +47,8 @@ def test_workspace_bytes_and_validation(lib):
     for field, bad in [("head_dim", 96), ("block_tokens", 16), ("n_q_heads", 5),
                        ("view_blocks", 5), ("kv_dtype", 7), ("max_blocks", 0),
                        ("pool_pages", 1), ("max_queries", 1000), ("candidate_mode", 2),
-                       ("delta_rerope_limit", -1), ("h2d_mode", 3), ("index_spill", 2)]:
+                       ("delta_rerope_limit", -1), ("h2d_mode", 3), ("index_spill", 2),
+                       ("spill_tiles", -1), ("spill_tiles", 3)]:   # 3 needs index_spill
         c = config_for(configs.TINY)
         setattr(c, field, bad)
         assert lib.kvm_workspace_bytes(ctypes.byref(c)) == 0, field
@@ -100,6 +101,14 @@ def test_index_spill_workspace_holds_the_index(lib):
     tile = wl.n_layers * wl.n_kv_heads * base.tile_blocks * wl.head_dim * 2
     tiles = -(-base.max_blocks // base.tile_blocks)
     assert n1 - n0 == tiles * tile - 2 * tile
+    # a budget of m tiles: two streaming tiles and m kept ones; a budget of
+    # the whole index or more is the full spill
+    for m in (1, 5):
+        capped = config_for(wl, index_spill=1, spill_tiles=m)
+        assert lib.kvm_workspace_bytes(ctypes.byref(capped)) - n0 == m * tile
+    for m in (tiles, tiles + 7):
+        whole = config_for(wl, index_spill=1, spill_tiles=m)
+        assert lib.kvm_workspace_bytes(ctypes.byref(whole)) == n1
     # a device-resident index stages nothing either way
     dev = config_for(wl, index_location=0)
     dev_spill = config_for(wl, index_location=0, index_spill=1)

@@ -109,12 +109,14 @@ def test_score_select_fewer_queries_and_ragged(kvm, variant):
 
 
 @pytest.mark.parametrize("variant", [0, 1], ids=["tensor-cores", "cuda-cores"])
-@pytest.mark.parametrize("loc", ["device", "host-tiled", "host-tiled-spill"])
+@pytest.mark.parametrize("loc", ["device", "host-tiled", "host-tiled-spill",
+                                 "host-tiled-spill-budget"])
 def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
     """candidate_mode 1: the Eq. (10) softmax runs over the non-reserved blocks
     only; sink and recent blocks score exactly 0 and are still selected.  The
     host-tiled index puts the candidate range's ends inside 96-block tiles;
-    with index_spill pass 2 reads the tiles pass 1 staged."""
+    with index_spill pass 2 reads the tiles pass 1 staged (all 13, or the
+    last 4 under a spill budget, the first 9 crossing the link again)."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID.with_(n_blocks=1237, view_blocks=100)
     ws = workload.make_index_direct(wl, seed=4)
@@ -122,7 +124,8 @@ def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
     index = ws.index.to("cuda")
     if loc.startswith("host-tiled"):
         kw["index_location"] = kvm.KVM_HOST_PINNED
-        kw["index_spill"] = int(loc.endswith("spill"))
+        kw["index_spill"] = int("spill" in loc)
+        kw["spill_tiles"] = 4 if loc.endswith("budget") else 0
         index = ws.index.pin_memory()
     cfg = kvm.config_for(wl, **kw)
     if loc.startswith("host-tiled"):
@@ -140,6 +143,43 @@ def test_score_select_candidates_exclude_reserved(kvm, variant, loc):
     assert_scores_close(got[S:N - W], R[S:N - W], "candidates only")
     assert abs(got.sum() - wl.n_queries) < 1e-3 * wl.n_queries
     check_selection(sel.cpu().numpy(), R, S, W, wl.view_blocks, "candidates only")
+
+
+@pytest.mark.parametrize("candidate_mode", [0, 1])
+def test_host_tiled_results_do_not_depend_on_the_spill(kvm, candidate_mode):
+    """A host-resident index in 96-block tiles (13 tiles, the last one ragged):
+    streamed twice, kept whole, or kept up to a budget of 1, 4 or 12 tiles
+    (pass 2 then scores the kept tiles first), the scores and the selection
+    are bit-identical; the first also matches the oracle."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID.with_(n_blocks=1237, view_blocks=100)
+    ws = workload.make_index_direct(wl, seed=8)
+    index = ws.index.pin_memory()
+    q = ws.q.cuda()
+    N = wl.n_blocks
+    got = []
+    for spill, m in [(0, 0), (1, 0), (1, 1), (1, 4), (1, 12)]:
+        cfg = kvm.config_for(wl, index_location=kvm.KVM_HOST_PINNED, index_spill=spill,
+                             spill_tiles=m, candidate_mode=candidate_mode)
+        cfg.tile_blocks = 96
+        ctx = kvm.Context(cfg)
+        scores = torch.empty(N, device="cuda")
+        sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+        for _ in range(2):          # the second call reuses the kept tiles' buffers
+            ctx.score_select(q, wl.n_queries, index, N, scores, sel)
+        ctx.sync()
+        got.append((scores.cpu(), sel.cpu()))
+        ctx.close()
+    for sc, se in got[1:]:
+        assert torch.equal(sc, got[0][0]) and torch.equal(se, got[0][1])
+    q64 = ora.as_f64(to_np(ws.q, "bf16"), "bf16")
+    i64 = ora.as_f64(to_np(ws.index, "bf16"), "bf16")
+    S, W = wl.sink_blocks, wl.recent_blocks
+    R = (ora.block_relevance_excl(q64, i64, N, S, W) if candidate_mode
+         else ora.block_relevance(q64, i64, N))
+    lo, hi = (S, N - W) if candidate_mode else (0, N)
+    assert_scores_close(got[0][0].double().numpy()[lo:hi], R[lo:hi], "host tiles")
+    check_selection(got[0][1].numpy(), R, S, W, wl.view_blocks, "host tiles")
 
 
 @pytest.mark.parametrize("loc", ["device", "host-tiled"])

@@ -88,16 +88,19 @@ def test_step_host_tier_policy(kvm):
     assert sum(h["host_demoted"] for h in hist) > 0
 
 
-@pytest.mark.parametrize("index_spill", [0, 1], ids=["restream", "spill"])
-def test_step_host_index_tiled(kvm, index_spill):
+@pytest.mark.parametrize("index_spill,spill_tiles", [(0, 0), (1, 0), (1, 2)],
+                         ids=["restream", "spill", "spill-budget"])
+def test_step_host_index_tiled(kvm, index_spill, spill_tiles):
     """Index in pinned host memory, scored in 64-block tiles (KVMem §5); with
-    index_spill the tiles cross the host link once per step."""
+    index_spill the tiles cross the host link once per step, or all but the
+    last two of them twice under a two-tile budget."""
     from paged_kv_cache_meank_gb300 import workload
     wl = MID
     g = torch.Generator().manual_seed(22)
     u = workload.unit_vectors(1, wl.head_dim, g, "cpu")
     q = workload.make_queries(wl, g, "cpu", u[0])
-    run_steps(kvm, wl, True, True, [q, q], [300, 300], index_spill=index_spill)
+    run_steps(kvm, wl, True, True, [q, q], [300, 300], index_spill=index_spill,
+              spill_tiles=spill_tiles)
 
 
 def test_step_failure_injection(kvm):
