@@ -314,6 +314,8 @@ typedef struct {
  * launch for the latest kvm_reset_pool and kvm_stage_out, and a later
  * kvm_reset_pool orders its clearing after the launches already enqueued.
  * Steps, eager or launched from graphs, must follow one another on one stream.
+ * A graph keeps the buffers bound at capture time: after kvm_bind, capture
+ * again.
  * Errors under capture: KVM_ERR_INVALID_ARG when the diff runs on the host,
  * the index is host-resident, or stats is not NULL; nothing is enqueued then.
  */
