@@ -10,8 +10,8 @@
 // owns whole (layer, kv head) pairs, so no CTA barrier sits in the streaming
 // loop: a lane owns 16 bytes of the first half of a token row and the matching
 // 16 bytes of the second half (rotate-half partners) for a fixed column slice,
-// walks its share of the 32 tokens with all loads issued up front (256 bytes
-// in flight per lane), un-rotates them in float32, optionally writes the raw
+// walks its share of the 32 tokens with loads issued in groups of 128 bytes
+// per lane, un-rotates them in float32, optionally writes the raw
 // K, and keeps the token sum in registers; two shuffle rounds finish the sum
 // across the lanes that share a column slice.  HBM traffic per (layer, kv
 // head, block): 32*d elements read, 32*d written (raw K), d written.
@@ -21,9 +21,16 @@
 namespace kvm {
 
 constexpr int kMeanKWarps = 4;
+// CTAs per SM the register budget is sized for.  2- and 4-byte pages: four,
+// which leave 128 registers a thread, so nothing spills (six capped it at 80
+// and spilled 64 bytes at d = 128: the 256K build took 10.53 ms against
+// 10.40).  e4m3 pages carry half the bytes per load, and the extra warps of
+// six CTAs keep more of them in flight (5.47 ms against 6.20 with four).
+template <typename T>
+constexpr int meank_min_ctas() { return sizeof(T) == 1 ? 6 : 4; }
 
 template <typename T, typename TI, int D>
-__global__ void __launch_bounds__(kMeanKWarps * 32, 6)
+__global__ void __launch_bounds__(kMeanKWarps * 32, meank_min_ctas<T>())
 meank_kernel(const T *__restrict__ k_pages, T *__restrict__ raw_out, TI *__restrict__ index,
              int64_t index_cap, int64_t first_block, int LG, int lg_per_cta,
              const float2 *__restrict__ table) {
