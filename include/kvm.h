@@ -364,7 +364,7 @@ kvm_status kvm_tier_resident(const kvm_tier *tier, uint8_t *flags, int64_t n);
 kvm_status kvm_tier_destroy(kvm_tier *tier);
 
 /*
- * kvm_score_select without any device allocation: the paper has no
+ * kvm_score_select without any device allocation: KVMem has no
  * counterpart; this is a deployment convenience.
  *
  * Computes what kvm_score_select computes for a device-resident index, with
