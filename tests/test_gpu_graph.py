@@ -139,3 +139,62 @@ def test_capture_refusals(kvm):
         st = dev.step(q, wl.n_queries, wl.n_blocks)
         dev.sync(s)
     assert (st["hits"], st["misses"]) == (0, wl.view_blocks)
+
+
+def test_graph_launch_waits_for_stage_out(kvm):
+    """A step captured while the pinned host repository is still empty; the
+    index is then built and the repository staged out chunk by chunk (262 MB
+    of raw K and V on the copy stream), and the graph launched at once, with
+    no sync.
+    The launch waits for the stage-out copies through its external event
+    wait, so its view equals an eager step's over the same repository."""
+    from paged_kv_cache_meank_gb300 import workload
+    from gpu_helpers import from_np, to_np
+    from recall_ref import prefill_k_pages
+    wl = MID.with_(n_blocks=2000, view_blocks=60)
+    N, V = wl.n_blocks, wl.view_blocks
+    ws = workload.make_workspace(wl, seed=67)
+    kp = prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta)
+    q = ws.q.cuda()
+    s = torch.cuda.Stream()
+    outs = []
+    for graphed in (False, True):
+        cfg = kvm.config_for(wl, repo_location=kvm.KVM_HOST_PINNED, h2d_mode=1)
+        ctx = kvm.Context(cfg)
+        raw_h = torch.zeros(ctx.block_shape(N), dtype=ctx.kv_dtype, pin_memory=True)
+        v_h = torch.zeros_like(raw_h, pin_memory=True)
+        index = torch.zeros(ctx.index_shape(), dtype=torch.bfloat16, device="cuda")
+        P = cfg.pool_pages
+        b = {"pool_k": torch.zeros(ctx.block_shape(P), dtype=ctx.kv_dtype, device="cuda")}
+        b["pool_v"] = torch.zeros_like(b["pool_k"])
+        b["pool_raw_k"] = torch.zeros_like(b["pool_k"])
+        b["page_table"] = torch.empty(V, dtype=torch.int32, device="cuda")
+        b["scores"] = torch.empty(N, device="cuda")
+        b["sel_ids"] = torch.empty(V, dtype=torch.int32, device="cuda")
+        ctx.bind(index=index, raw_k=raw_h, v=v_h, **b)
+        torch.cuda.synchronize()
+        if graphed:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                ctx.step(q, wl.n_queries, N)
+        keep = []
+        with torch.cuda.stream(s):
+            for c0 in range(0, N, 256):
+                n = min(256, N - c0)
+                kp_d = from_np(kp[c0:c0 + n], "bf16")
+                v_d = ws.v[c0:c0 + n].cuda()
+                raw_d = torch.empty_like(kp_d)
+                ctx.build_index(kp_d, c0, n, index, raw_d)
+                ctx.stage_out(raw_d, v_d, c0, n)
+                keep += [kp_d, v_d, raw_d]       # alive until the copies are done
+            if graphed:
+                g.replay()
+            else:
+                ctx.step(q, wl.n_queries, N)
+            ctx.sync(s)
+        outs.append(b)
+    for k in _OUT + ("pool_raw_k",):
+        assert torch.equal(outs[0][k], outs[1][k]), k
+    pages = outs[1]["page_table"].long()
+    sel = outs[1]["sel_ids"].long().cpu()
+    assert torch.equal(outs[1]["pool_v"][pages].cpu(), ws.v[sel])
