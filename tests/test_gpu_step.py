@@ -60,6 +60,26 @@ def test_step_history_shrinks_and_grows(kvm, repo_host, h2d_mode):
 
 @pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 0), (True, 1)],
                          ids=["repo-device", "repo-host-copy-engine", "repo-host-gpu-pull"])
+def test_step_degenerate_histories(kvm, repo_host, h2d_mode):
+    """Histories of 1 and 2 blocks (inside the sink window), exactly the view
+    budget (60), one block more, and back to 1: the page table, counters and
+    pages follow the oracle at every step, on the device-side diff (device
+    repository, GPU pull) and the host-side one (copy engine)."""
+    from paged_kv_cache_meank_gb300 import workload
+    wl = MID
+    g = torch.Generator().manual_seed(25)
+    u = workload.unit_vectors(2, wl.head_dim, g, "cpu")
+    qa = workload.make_queries(wl, g, "cpu", u[0])
+    qb = workload.make_queries(wl, g, "cpu", u[1])
+    hist = run_steps(kvm, wl, repo_host, False, [qa, qb, qa, qb, qa, qb],
+                     [1, 2, 60, 61, 1, 60], h2d_mode=h2d_mode)
+    assert [h["n_sel"] for h in hist] == [1, 2, 60, 60, 1, 60]
+    assert hist[0]["misses"] == 1 and hist[1]["hits"] == 1 and hist[1]["misses"] == 1
+    assert hist[4]["hits"] == 1 and hist[4]["misses"] == 0
+
+
+@pytest.mark.parametrize("repo_host,h2d_mode", [(False, 0), (True, 0), (True, 1)],
+                         ids=["repo-device", "repo-host-copy-engine", "repo-host-gpu-pull"])
 def test_step_sequence_fp8_pages(kvm, repo_host, h2d_mode):
     """The same working-set sequence with 8-bit (e4m3) K / V pages: Mean-K from
     e4m3 prefill K, view K re-RoPE'd and rounded to e4m3, V bytes moved."""
