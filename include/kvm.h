@@ -258,7 +258,8 @@ kvm_status kvm_bind(kvm_ctx *ctx, const kvm_buffers *bufs);
  * and v must stay unchanged until the copies are done: kvm_sync waits for
  * them, and every later kvm_step orders its reads of the repository after them.
  * Errors: KVM_ERR_NOT_BOUND, KVM_ERR_INVALID_ARG (no host repository, NULL
- * buffers), KVM_ERR_CAPACITY (blocks beyond max_blocks).
+ * buffers, or `stream` being captured into a CUDA graph), KVM_ERR_CAPACITY
+ * (blocks beyond max_blocks).
  */
 kvm_status kvm_stage_out(kvm_ctx *ctx, const void *raw_k, const void *v, int64_t first_block,
                          int64_t n_blocks, kvm_stream stream);

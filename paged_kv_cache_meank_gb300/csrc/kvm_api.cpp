@@ -735,6 +735,12 @@ kvm_status kvm_stage_out(kvm_ctx *c, const void *raw_k, const void *v, int64_t f
         return fail(KVM_ERR_CAPACITY, "blocks beyond max_blocks");
     if (n_blocks == 0) return KVM_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the copies run on the context's copy stream, ordered by events that
+    // later eager calls wait on: not something a graph launch can replay
+    bool capturing = false;
+    if (kvm_status cst = stream_capturing(s, &capturing); cst != KVM_OK) return cst;
+    if (capturing)
+        return fail(KVM_ERR_INVALID_ARG, "kvm_stage_out cannot be captured into a CUDA graph");
     const size_t blk = block_bytes(c->cfg);
     char *dk = const_cast<char *>(static_cast<const char *>(c->bufs.raw_k)) + first_block * blk;
     char *dv = const_cast<char *>(static_cast<const char *>(c->bufs.v)) + first_block * blk;

@@ -99,7 +99,7 @@ def test_eager_steps_and_graph_launches_interleave(kvm):
 
 def test_capture_refusals(kvm):
     """Under capture, kvm_step with a stats pointer, kvm_step whose diff runs
-    on the host, and scoring of a host-resident index return
+    on the host, scoring of a host-resident index and kvm_stage_out return
     KVM_ERR_INVALID_ARG and enqueue nothing; the capture itself stays valid."""
     import ctypes
     from paged_kv_cache_meank_gb300 import workload
@@ -115,6 +115,7 @@ def test_capture_refusals(kvm):
     index_h = torch.zeros(host_idx.index_shape(), dtype=host_idx.index_dtype).pin_memory()
     scores = torch.empty(wl.n_blocks, device="cuda")
     sel = torch.empty(wl.view_blocks, dtype=torch.int32, device="cuda")
+    blk = torch.zeros(host_diff.block_shape(1), dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
     x = torch.zeros(4, device="cuda")
     codes = []
@@ -129,10 +130,12 @@ def test_capture_refusals(kvm):
         codes.append(host_idx.lib.kvm_score_select(host_idx.handle, q.data_ptr(), wl.n_queries,
                                                    index_h.data_ptr(), wl.n_blocks,
                                                    scores.data_ptr(), sel.data_ptr(), None, cs))
+        codes.append(host_diff.lib.kvm_stage_out(host_diff.handle, blk.data_ptr(),
+                                                 blk.data_ptr(), 0, 1, cs))
         x.add_(1)
     g.replay()
     torch.cuda.synchronize()
-    assert [STATUS[c] for c in codes] == ["KVM_ERR_INVALID_ARG"] * 3
+    assert [STATUS[c] for c in codes] == ["KVM_ERR_INVALID_ARG"] * 4
     assert x.tolist() == [1.0] * 4
     # the refused steps changed nothing: the first eager step misses every block
     with torch.cuda.stream(s):
@@ -198,3 +201,47 @@ def test_graph_launch_waits_for_stage_out(kvm):
     pages = outs[1]["page_table"].long()
     sel = outs[1]["sel_ids"].long().cpu()
     assert torch.equal(outs[1]["pool_v"][pages].cpu(), ws.v[sel])
+
+
+def test_build_score_assemble_capture(kvm):
+    """kvm_build_index, kvm_score_select on a device index and
+    kvm_assemble_view enqueue kernels on the caller's stream only: captured
+    together into one graph, a launch gives the eager calls' index, raw K,
+    scores, selection and view, bit for bit."""
+    from paged_kv_cache_meank_gb300 import workload
+    from gpu_helpers import from_np, to_np
+    from recall_ref import prefill_k_pages
+    wl = MID
+    N, V = wl.n_blocks, wl.view_blocks
+    ws = workload.make_workspace(wl, seed=69)
+    kp = from_np(prefill_k_pages(to_np(ws.raw_k, "bf16"), "bf16", wl.rope_theta), "bf16")
+    q, v = ws.q.cuda(), ws.v.cuda()
+    ctx = kvm.Context(kvm.config_for(wl))
+    s = torch.cuda.Stream()
+
+    def buffers():
+        return {"index": torch.zeros(ctx.index_shape(), dtype=ctx.index_dtype, device="cuda"),
+                "raw": torch.empty(ctx.block_shape(N), dtype=ctx.kv_dtype, device="cuda"),
+                "scores": torch.empty(N, device="cuda"),
+                "sel": torch.empty(V, dtype=torch.int32, device="cuda"),
+                "k": torch.empty(ctx.block_shape(V), dtype=ctx.kv_dtype, device="cuda"),
+                "v": torch.empty(ctx.block_shape(V), dtype=ctx.kv_dtype, device="cuda")}
+
+    def calls(b):
+        ctx.build_index(kp, 0, N, b["index"], b["raw"])
+        ctx.score_select(q, wl.n_queries, b["index"], N, b["scores"], b["sel"])
+        ctx.assemble_view(b["sel"], None, V, b["raw"], v, b["k"], b["v"])
+
+    eager, graphed = buffers(), buffers()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        calls(eager)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(graphed)
+    with torch.cuda.stream(s):
+        g.replay()
+        ctx.sync(s)
+    for k in eager:
+        assert torch.equal(eager[k], graphed[k]), k
