@@ -47,6 +47,24 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _bf16_peaks():
+    """Dense bf16 tensor peaks in TFLOP/s: (burst, sustained, kind)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return (float(d["bf16_tflops"]),
+                    float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 1900.0, 1700.0, "fallback"
+
+
+# ex2.approx results per clock per SM on GB300, measured with a timing kernel
+# (one 1024-thread CTA per SM, eight independent exponential chains a thread):
+# 31.8, twice the rate of earlier parts
+MUFU_EX2_PER_CLK_SM = 32
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -653,23 +671,36 @@ def summarize(wl, step, ms, parts, clk, dev, stream):
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_hbm"],
             "traffic": traffic, "algorithmic_bytes": ab[dom]}
     if dom == "score_select" and len(parts) == 1:
-        # scoring alone: each exact pass of Eq. (10) takes one exponential per
-        # (query row, block, layer, kv head) on the MUFU unit, 16 per clock per
-        # SM, and that binds as tightly as HBM does (reported beside it)
-        n_exp = 2 * wl.n_queries * wl.gqa * wl.n_blocks * wl.n_layers * wl.n_kv_heads
+        # scoring alone.  Per (layer, kv head, block) exact Eq. (10) in two
+        # passes takes 2 x 2*d*rows flops on the tensor pipe, 2*rows
+        # exponentials on MUFU and one 256-byte index read: the tensor floor is
+        # the highest of the three, so it is the roofline; HBM (one read, with
+        # the DRAM bytes the two passes actually move) and MUFU sit beside it
+        rows = wl.n_queries * wl.gqa
+        units = wl.n_blocks * wl.n_layers * wl.n_kv_heads
+        t = parts[dom] * 1e-3
+        flops = 2 * (2 * wl.head_dim * rows) * units
+        burst, sustained, tkind = _bf16_peaks()
+        ach_tf = flops / t / 1e12
+        n_exp = 2 * rows * units
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         max_mhz = float(clk.get("sm_max_mhz") or 2070.0)
-        ach = n_exp / (parts[dom] * 1e-3) / 1e9
-        mufu_peak = 16 * sms * max_mhz * 1e-3
+        ach_ex = n_exp / t / 1e9
+        mufu_peak = MUFU_EX2_PER_CLK_SM * sms * max_mhz * 1e-3
         hbm = dict(roof)
         if hbm.get("traffic"):
-            hbm["traffic_note"] = "DRAM bytes per scoring call, from the committed ncu summary"
-        roof = {"bound": "alu", "kernel": dom, "unit": "Gex2/s", "achieved": ach,
-                "peak": mufu_peak, "frac": ach / mufu_peak,
-                "peak_kind": f"MUFU ex2: 16 per clock per SM x {sms} SMs x {max_mhz:.0f} MHz",
-                "traffic": None, "algorithmic_ops": n_exp, "hbm": hbm}
-        if clk.get("sm_mhz"):
-            roof["frac_at_sampled_clock"] = ach / (16 * sms * float(clk["sm_mhz"]) * 1e-3)
+            hbm["traffic_note"] = ("DRAM bytes per scoring call, from the committed ncu summary: "
+                                   "the two passes read the index twice")
+        mufu = {"unit": "Gex2/s", "achieved": ach_ex, "peak": mufu_peak,
+                "frac": ach_ex / mufu_peak, "algorithmic_ops": n_exp,
+                "peak_kind": f"MUFU ex2: {MUFU_EX2_PER_CLK_SM} per clock per SM (measured) x "
+                             f"{sms} SMs x {max_mhz:.0f} MHz"}
+        roof = {"bound": "tensor", "kernel": dom, "unit": "TFLOP/s", "achieved": ach_tf,
+                "peak": sustained, "frac": ach_tf / sustained,
+                "peak_kind": f"{tkind} dense bf16, sustained (the loop runs under the power cap)",
+                "peak_burst": burst, "frac_burst": ach_tf / burst,
+                "traffic": hbm.get("traffic"), "algorithmic_flops": flops,
+                "hbm": hbm, "mufu": mufu}
     if link is not None and dom == "step":
         hp = h2d_peak(dev, stream)
         roof.update(bound="h2d", peak=hp, peak_kind="measured pinned H2D (256 MiB copy)",

@@ -9,7 +9,8 @@
 // flight to fill the GPU the data touched between a tile's two reads exceeds
 // what L2 keeps (a 1.07 GB index still drew 2.02 GB from DRAM), a 10M-block
 // slice alone is 80 MB, and the per-slice group sync costs several
-// microseconds.  Both passes are bound by their exponentials in any case.
+// microseconds.  Even with every second read from L2, the tensor pipe (both
+// passes' MMAs) would bind before HBM does.
 //
 // The softmax of a query row runs over every block of its (layer l, kv head g)
 // slice, so pass 2 of a slice can start only once pass 1 has seen the whole
