@@ -133,7 +133,9 @@ class Clocks:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((int(parts[0]), float(parts[1]), float(parts[2]), parts[5:9]))
+                pw = float(parts[3]) if parts[3].replace(".", "", 1).isdigit() else None
+                rows.append((int(parts[0]), float(parts[1]), float(parts[2]), parts[5:9], pw,
+                             parts[4]))
             except ValueError:
                 continue
         if not rows:
@@ -147,9 +149,14 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
                           if v.lower() == "active"})
+        powers = [r[4] for r in rows if r[4] is not None]
+        # the driver's bitmask of every active reason (0x4: software power cap)
+        masks = sorted({r[5] for r in rows})
         return {"sm_mhz": float(np.median([r[1] for r in rows])),
                 "sm_max_mhz": float(max(r[2] for r in rows)), "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows),
+                "power_w": float(np.median(powers)) if powers else None,
+                "reason_masks": masks}
 
 
 # ----------------------------------------------------------------------------
@@ -818,6 +825,9 @@ def bench_extra(args, world, rank, dev, stream, dist):
             step = make_step(args, wl, args.seed + rank, dev, stream, **extra)
         setup_s = time.perf_counter() - t_setup
         K = wl.steps if isinstance(step, ChurnStep) else args.extra_steps
+        if isinstance(step, ScoreStep):
+            # about 15 ms a step: 20 steps give the clock sampler six samples
+            K = max(K, 20)
         ms, parts, n_launches, clk = time_steps(step, K, args.warmup, dev, stream, dist)
         comps, roof = summarize(wl, step, ms, parts, clk, dev, stream)
         key = name + ("" if "index_spill" not in extra else
