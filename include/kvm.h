@@ -428,6 +428,17 @@ kvm_status kvm_score_select_static_status(kvm_stream stream);
  * report a raised device error flag (KVM_ERR_DEVICE), clearing it. */
 kvm_status kvm_sync(kvm_ctx *ctx, kvm_stream stream);
 
+/*
+ * The counters of the last kvm_step launched from a CUDA graph on this context
+ * (steps captured under stream capture report none through kvm_step; every
+ * captured step of the context writes the same slot, so this is the step that
+ * ran last).  Waits for `stream` (the stream the graph was launched on), then
+ * fills *stats (host) as kvm_sync fills an eager step's, with n_blocks and
+ * n_sel as given at capture time.  Errors: KVM_ERR_INVALID_ARG (NULL
+ * arguments, or no step of this context was captured), KVM_ERR_CUDA.
+ */
+kvm_status kvm_graph_step_stats(kvm_ctx *ctx, kvm_step_stats *stats, kvm_stream stream);
+
 const char *kvm_status_string(kvm_status s);
 
 /* Detail of the last error raised on the calling thread ("" if none). */

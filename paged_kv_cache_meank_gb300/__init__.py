@@ -267,6 +267,14 @@ class Context:
         self._pending.append(st)           # the library writes it until the next sync
         return StepStats(st)
 
+    def graph_step_stats(self, stream=None) -> "StepStats":
+        """The counters of the last kvm_step launched from a CUDA graph on this
+        context (waits for `stream`)."""
+        st = KvmStepStats()
+        check(self.lib.kvm_graph_step_stats(self.handle, ctypes.byref(st), _stream(stream)),
+              "kvm_graph_step_stats")
+        return StepStats(st)
+
     def sync(self, stream=None) -> None:
         check(self.lib.kvm_sync(self.handle, _stream(stream)), "kvm_sync")
         self._pending.clear()

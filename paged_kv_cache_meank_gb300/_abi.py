@@ -97,6 +97,7 @@ SIGNATURES = {
     "kvm_tier_resident": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]),
     "kvm_tier_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "kvm_sync": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "kvm_graph_step_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "kvm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvm_last_error": (ctypes.c_char_p, []),
     "kvm_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]),

@@ -207,6 +207,8 @@ struct kvm_ctx {
             *d_slot_page = nullptr, *d_counts = nullptr, *d_epoch = nullptr;
     int64_t n_dev_steps = 0;
     bool graph_steps = false;            // a step was captured into a CUDA graph
+    int64_t graph_n_blocks = 0;          // ... its history and view sizes
+    int32_t graph_n_sel = 0;
     struct Pending {
         kvm_step_stats *out;
         int64_t step;                    // its step number: ring slot step % kStatSlots
@@ -819,26 +821,28 @@ static int commit_residency(kvm_ctx *c, const std::vector<int32_t> &sel,
 
 // Copies the counters of every step still waiting for them to the caller's
 // stats (host tier fields 0); the steps' work must be complete.
+// A step's stats from its slot of the counter ring (host tier fields 0).
+static void fill_stats(const kvm_ctx *c, const int32_t *k, int64_t n_blocks, int32_t n_sel,
+                       kvm_step_stats *st) {
+    const bool pull = c->cfg.repo_location == KVM_HOST_PINNED;
+    *st = kvm_step_stats{};
+    st->n_blocks = n_blocks;
+    st->n_sel = n_sel;
+    st->hits = k[1];
+    st->misses = k[2];
+    st->reroped = k[0];
+    st->delta_reroped = k[3];
+    st->evicted = k[4];
+    st->h2d_bytes = pull ? 2 * (int64_t)k[2] * (int64_t)block_bytes(c->cfg) : 0;
+}
+
 static kvm_status flush_pending(kvm_ctx *c) {
     if (c->pending.empty()) return KVM_OK;
     int32_t ring[kStatSlots * 8];
     KVM_CUDA(cudaEventSynchronize(c->ev_step));
     KVM_CUDA(cudaMemcpy(ring, c->d_counts, sizeof ring, cudaMemcpyDeviceToHost));
-    const bool pull = c->cfg.repo_location == KVM_HOST_PINNED;
-    const int64_t blk = (int64_t)block_bytes(c->cfg);
-    for (const auto &pd : c->pending) {
-        const int32_t *k = ring + (pd.step % kStatSlots) * 8;
-        kvm_step_stats *st = pd.out;
-        *st = kvm_step_stats{};
-        st->n_blocks = pd.n_blocks;
-        st->n_sel = pd.n_sel;
-        st->hits = k[1];
-        st->misses = k[2];
-        st->reroped = k[0];
-        st->delta_reroped = k[3];
-        st->evicted = k[4];
-        st->h2d_bytes = pull ? 2 * (int64_t)k[2] * blk : 0;
-    }
+    for (const auto &pd : c->pending)
+        fill_stats(c, ring + (pd.step % kStatSlots) * 8, pd.n_blocks, pd.n_sel, pd.out);
     c->pending.clear();
     return KVM_OK;
 }
@@ -921,6 +925,8 @@ static kvm_status step_device(kvm_ctx *c, int64_t n_blocks, int32_t n_sel,
     if (capturing) {
         KVM_CUDA(cudaEventRecordWithFlags(c->ev_step, s, cudaEventRecordExternal));
         c->graph_steps = true;
+        c->graph_n_blocks = n_blocks;
+        c->graph_n_sel = n_sel;
         return KVM_OK;
     }
     KVM_CUDA(cudaEventRecord(c->ev_step, s));
@@ -1161,6 +1167,17 @@ kvm_status kvm_sync(kvm_ctx *c, kvm_stream stream) {
         if (flag & 4) return fail(KVM_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", flag);
         return fail(KVM_ERR_DEVICE, "device range check raised flag 0x%x", flag);
     }
+    return KVM_OK;
+}
+
+kvm_status kvm_graph_step_stats(kvm_ctx *c, kvm_step_stats *stats, kvm_stream stream) {
+    if (!c || !stats) return fail(KVM_ERR_INVALID_ARG, "ctx and stats are required");
+    if (!c->graph_steps)
+        return fail(KVM_ERR_INVALID_ARG, "no kvm_step of this context was captured");
+    KVM_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    int32_t k[8];
+    KVM_CUDA(cudaMemcpy(k, c->d_counts + kStatSlots * 8, sizeof k, cudaMemcpyDeviceToHost));
+    fill_stats(c, k, c->graph_n_blocks, c->graph_n_sel, stats);
     return KVM_OK;
 }
 

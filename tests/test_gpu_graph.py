@@ -50,9 +50,13 @@ def test_graph_launches_match_eager_steps(kvm, variant, repo_host, cfg_kw):
         assert graphed.step(q_static, wl.n_queries, wl.n_blocks) is None
     with torch.cuda.stream(s):
         for t, i in enumerate([0, 1, 1, 2, 0, 2]):
-            eager.step(qs[i], wl.n_queries, wl.n_blocks)
+            st = eager.step(qs[i], wl.n_queries, wl.n_blocks)
             q_static.copy_(qs[i])
             g.replay()
+            # the launch's counters equal the eager step's
+            gst = graphed.graph_step_stats(s)
+            eager.sync(s)
+            assert dict(gst) == dict(st), f"step {t}: counters"
             if t == 3:
                 eager.reset_pool()
                 graphed.reset_pool()
@@ -136,6 +140,11 @@ def test_capture_refusals(kvm):
     g.replay()
     torch.cuda.synchronize()
     assert [STATUS[c] for c in codes] == ["KVM_ERR_INVALID_ARG"] * 4
+    # no step of these contexts was captured: no graph counters to read
+    for ctx in (dev, host_diff):
+        with pytest.raises(kvm.KvmError) as ei:
+            ctx.graph_step_stats(s)
+        assert ei.value.name == "KVM_ERR_INVALID_ARG"
     assert x.tolist() == [1.0] * 4
     # the refused steps changed nothing: the first eager step misses every block
     with torch.cuda.stream(s):
