@@ -311,7 +311,8 @@ typedef struct {
  * device memory may be enqueued while `stream` is being captured; each launch
  * of the graph then runs one step on the query buffer `q` as it holds at
  * launch time, against the residency as the steps before it left it.  Such a
- * step takes stats = NULL (its counters are not reported), waits at every
+ * step takes stats = NULL (kvm_graph_step_stats reads the counters of the
+ * last one that ran), waits at every
  * launch for the latest kvm_reset_pool and kvm_stage_out, and a later
  * kvm_reset_pool orders its clearing after the launches already enqueued.
  * Steps, eager or launched from graphs, must follow one another on one stream.
